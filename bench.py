@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark: one step = one pass of the whole hot path over one synthetic batch.
+
+Step (all on the GPU, through the C ABI):
+  zigzag-shard q, k, v -> positions -> ring attention forward over C virtual
+  ranks (C batched partial-attention launches + C-1 LSE merges, K/V rotation
+  prefetched on a side stream) -> zigzag-unshard the output -> Ulysses
+  sequence-to-head relayout of the q, k, v shards (global order).
+Metric: algorithmic causal-attention TFLOP/s of the step (4*D FLOPs per visible
+(query, key) pair), plus per-kernel TFLOP/s and GB/s from CUDA events recorded
+on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload s32k]
+
+Under torchrun (N > 1) every rank runs an independent replica (the C virtual
+ranks of the method live on one GPU; nothing is exchanged between GPUs).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd TFLOP/s & % bf16 tensor peak; LSE-merge/relayout HBM GB/s"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def attn_source_hash():
+    h = hashlib.sha256()
+    for f in ("attn.cu", "cp_ptx.cuh"):
+        with open(os.path.join(ROOT, "context_causal_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "attn_fwd_kernel_%s.md" % workload)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source\s+([0-9a-f]+)\)", txt)
+    if not m or m.group(2) != attn_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline and the reference arm)
+# --------------------------------------------------------------------------
+def oracle_sample_run(w, q, k, v, rows, nthreads):
+    """Time the fp64 oracle on the given query rows (all heads); returns
+    (seconds, algorithmic flops of those rows)."""
+    import numpy as np
+    import oracle as O
+    gp = np.arange(w.S, dtype=np.int32)
+    t0 = time.perf_counter()
+    O.attn_rows(q, k, v, gp, gp, rows, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.B * w.N * w.D * float(np.sum(rows + 1))
+    return dt, flops
+
+
+def prepare_oracle_inputs(w, q, k, v):
+    import numpy as np
+    return tuple(t.float().numpy().astype(np.float64) for t in (q, k, v))
+
+
+def cpu_rows(w, n, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.integers(0, w.S, size=n)).astype(np.int64)
+
+
+def cpu_baseline(w, qkv64, target_s=12.0):
+    import oracle as O
+    cores = O.default_threads()
+    rows_total, secs, flops = 0, 0.0, 0.0
+    batch = 16
+    seed = 100
+    while secs < target_s and rows_total < 1 << 16:
+        rows = cpu_rows(w, batch, seed)
+        dt, fl = oracle_sample_run(w, *qkv64, rows, cores)
+        secs += dt
+        flops += fl
+        rows_total += batch
+        seed += 1
+        if dt < target_s / 8:
+            batch *= 2
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "%d random query rows x all %d heads of the %s workload (fp64 C oracle, %d threads), %.1f s"
+                      % (rows_total, w.N, w.name, cores, secs)}
+
+
+def run_reference(args, w):
+    """The oracle, as it stands, timed on the host cores (rank 0 only)."""
+    import cp_synth as SY
+    import oracle as O
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    q, k, v, _ = SY.make_qkv(w)
+    qkv64 = prepare_oracle_inputs(w, q, k, v)
+    cores = O.default_threads()
+    rows_per_step = 32
+    for i in range(args.warmup):
+        oracle_sample_run(w, *qkv64, cpu_rows(w, rows_per_step, 1000 + i), cores)
+    secs, flops = 0.0, 0.0
+    for i in range(args.steps):
+        dt, fl = oracle_sample_run(w, *qkv64, cpu_rows(w, rows_per_step, 2000 + i), cores)
+        secs += dt
+        flops += fl
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, prefetch=None),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d random query rows x all %d heads per step of the %s workload"
+                                   % (rows_per_step, w.N, w.name)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, prefetch):
+    cfg = {"workload": "%s: B=%d S=%d N=%d Nkv=%d D=%d, C=%d %s ring%s" % (
+        w.name, w.B, w.S, w.N, w.Nkv, w.D, w.C, w.layout, ", RoPE" if w.rope else ""),
+        "B": w.B, "S": w.S, "N": w.N, "Nkv": w.Nkv, "D": w.D, "C": w.C, "layout": w.layout,
+        "l2": "inputs larger than L2 (q, k, v %.0f MB each)" % (w.B * w.S * w.N * w.D * 2 / 1e6)}
+    if prefetch is not None:
+        cfg["prefetch"] = prefetch
+    return cfg
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import cp_synth as SY
+    from context_causal_attention_gb300 import build as cuda_build
+    from context_causal_attention_gb300 import ops as F
+
+    rank, world, local = dist_setup(args.gpus)
+    cuda_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    q, k, v, _ = SY.make_qkv(w)
+    C, S, B, N, Nkv, D = w.C, w.S, w.B, w.N, w.Nkv, w.D
+    s = S // C
+    lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
+    prefetch = 1 if args.prefetch else 0
+
+    # resident buffers
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    qs = torch.empty((C, B, s, N, D), dtype=torch.bfloat16, device=dev)
+    ks = torch.empty((C, B, s, Nkv, D), dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    pos = torch.empty((C, s), dtype=torch.int32, device=dev)
+    o_sh = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+    lse_sh = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
+    o_full = torch.empty((B, S, N, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32)), dtype=torch.uint8,
+                     device=dev)
+    qh = torch.empty((C, B, S, N // C, D), dtype=torch.bfloat16, device=dev)
+    kh = torch.empty((C, B, S, Nkv // C, D), dtype=torch.bfloat16, device=dev)
+    vh = torch.empty_like(kh)
+    n_ring_ev = 4 * C
+
+    def mk_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record()
+        return evs
+
+    def step(qin, kin, vin, ev):
+        """One pass of the hot path.  ev: dict of event lists or None."""
+        def mark(name, i):
+            if ev is not None:
+                ev[name][i].record()
+        mark("shard", 0)
+        F.cp_zigzag_shard(qin, C, lay, out=qs)
+        F.cp_zigzag_shard(kin, C, lay, out=ks)
+        F.cp_zigzag_shard(vin, C, lay, out=vs)
+        mark("shard", 1)
+        F.cp_zigzag_positions(S, C, lay, out=pos)
+        F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch, o_dtype=F.CP_F32, workspace=ws,
+                                o=o_sh, lse=lse_sh, events=ev["ring"] if ev is not None else None)
+        mark("unshard", 0)
+        F.cp_zigzag_unshard(o_sh, lay, out=o_full)
+        mark("unshard", 1)
+        mark("relayout", 0)
+        F.cp_ulysses_relayout(qs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=qh)
+        F.cp_ulysses_relayout(ks, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=kh)
+        F.cp_ulysses_relayout(vs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=vh)
+        mark("relayout", 1)
+
+    launches_per_step = 3 + 1 + C + (C - 1) + 1 + 3
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step(qd, kd, vd, None)
+    torch.cuda.synchronize()
+    # ---- timed region (device time), per-kernel events inside
+    evsets = [{"ring": mk_events(n_ring_ev), "shard": mk_events(2), "unshard": mk_events(2),
+               "relayout": mk_events(2)} for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t_start.record()
+    for i in range(args.steps):
+        step(qd, kd, vd, evsets[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    ms_total = t_start.elapsed_time(t_end)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    flops_step = w.flops
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    # ---- per-kernel numbers from the events
+    pairs_t = w.t
+    # exact visible pairs per (b, h) per ring step, all ranks together
+    if w.layout == "zigzag":
+        step_pairs = [C * (pairs_t * pairs_t + pairs_t * (pairs_t + 1))] + [C * 2 * pairs_t * pairs_t] * (C - 1)
+    else:
+        step_pairs = [C * s * (s + 1) // 2] + [(C - st) * s * s for st in range(1, C)]
+    attn_ms = [0.0] * C
+    merge_ms = [0.0] * C
+    shard_ms = unshard_ms = relayout_ms = 0.0
+    for e in evsets:
+        r = e["ring"]
+        for st in range(C):
+            attn_ms[st] += r[4 * st].elapsed_time(r[4 * st + 1]) / args.steps
+            if st > 0:
+                merge_ms[st] += r[4 * st + 2].elapsed_time(r[4 * st + 3]) / args.steps
+        shard_ms += e["shard"][0].elapsed_time(e["shard"][1]) / args.steps
+        unshard_ms += e["unshard"][0].elapsed_time(e["unshard"][1]) / args.steps
+        relayout_ms += e["relayout"][0].elapsed_time(e["relayout"][1]) / args.steps
+    attn_flops = [4.0 * B * N * D * p for p in step_pairs]
+    attn_total_ms = sum(attn_ms)
+    attn_tflops = sum(attn_flops) / (attn_total_ms * 1e-3) / 1e12
+    per_step_tflops = [f / (t * 1e-3) / 1e12 for f, t in zip(attn_flops, attn_ms)]
+    # merge algorithmic bytes: rows whose tile lse is finite move 3*4*D + 12 bytes, others 4
+    rows = C * B * N * s
+    merge_gbs = None
+    if C > 1:
+        if w.layout == "zigzag":
+            fin_rows = []
+            for st in range(1, C):
+                fr = 0
+                for rr in range(C):
+                    j = (rr - st) % C
+                    fr += B * N * (s if j < rr else s // 2)
+                fin_rows.append(fr)
+        else:
+            fin_rows = [B * N * s * (C - st) for st in range(1, C)]
+        merge_bytes = sum(fr * (12 * D + 12) + (rows - fr) * 4 for fr in fin_rows)
+        merge_gbs = merge_bytes / (sum(merge_ms) * 1e-3) / 1e9
+    qkv_bytes = (B * S * N * D + 2 * B * S * Nkv * D) * 2
+    shard_gbs = 2 * qkv_bytes / (shard_ms * 1e-3) / 1e9
+    unshard_gbs = 2 * (B * S * N * D * 4) / (unshard_ms * 1e-3) / 1e9
+    relayout_gbs = 2 * qkv_bytes / (relayout_ms * 1e-3) / 1e9
+    peak_tc = peaks["bf16_tflops_sustained"]
+    traffic = recorded_traffic(w.name)
+
+    # ---- end to end: pinned host inputs -> device, step, result -> host
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    ho = torch.empty((B, S, N, D), dtype=torch.float32).pin_memory()
+    hl = torch.empty((C, B, N, s), dtype=torch.float32).pin_memory()
+    for _ in range(1):
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        step(qd, kd, vd, None)
+        ho.copy_(o_full, non_blocking=True)
+        hl.copy_(lse_sh, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record()
+    for _ in range(args.steps):
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        step(qd, kd, vd, None)
+        ho.copy_(o_full, non_blocking=True)
+        hl.copy_(lse_sh, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    h2d = qkv_bytes
+    d2h = B * S * N * D * 4 + C * B * N * s * 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, prefetch),
+        "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": attn_tflops / peak_tc, "traffic": traffic,
+                     "kernel": "attn_fwd_kernel<%d>" % D,
+                     "peak_note": "bf16_tflops_sustained of %s peaks (kernel timed inside a long step); "
+                                  "frac of burst %.1f: %.3f" % (peaks["source"], peaks["bf16_tflops"],
+                                                                attn_tflops / peaks["bf16_tflops"])},
+        "e2e": {"value": flops_step * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "kernels": {
+            "attn_ms_per_ring_step": attn_ms, "attn_tflops_per_ring_step": per_step_tflops,
+            "merge_ms_per_ring_step": merge_ms[1:], "merge_gbs": merge_gbs,
+            "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "relayout_gbs": relayout_gbs,
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+            "merge_frac_hbm": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
+            "shard_frac_hbm": shard_gbs / peaks["hbm_gbs"], "relayout_frac_hbm": relayout_gbs / peaks["hbm_gbs"],
+        },
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        qkv64 = prepare_oracle_inputs(w, q, k, v)
+        line["cpu_baseline"] = cpu_baseline(w, qkv64, target_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="s32k")
+    ap.add_argument("--no-prefetch", dest="prefetch", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    import cp_synth as SY
+    w = SY.WORKLOADS.get(args.workload)
+    if w is None:
+        w = {x.name: x for x in SY.sweep_workloads()}[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,750 @@
+// attn.cu -- partial causal attention with explicit positions on the sm_103a
+// tensor cores (tcgen05 + TMEM + TMA), returning (o, lse).
+//
+// What it computes ("On Context Parallelism", Peer-to-peer / Forward:
+// attention(q, k, v, q_positions, kv_positions, scale) -> (tile_output,
+// tile_lse); "Context parallelism: Ring Attention and Ulysses", cp_common.py):
+// for every (rank, b, h, query row i) with visible keys V(i) = {j : k_pos[j] <=
+// q_pos[i]}, lse_i = ln sum_{j in V(i)} e^{scale <q_i,k_j>} and
+// o_i = sum_j e^{scale <q_i,k_j> - lse_i} v_j; rows with no visible key get
+// o = 0, lse = -inf.
+//
+// How: one persistent CTA per SM walks a list of work items (rank, b, h,
+// 256-row query block) ordered longest-first.  Inside a CTA:
+//   warp 0      TMA producer: Q block (two 128-row tiles) and a ring of K/V
+//               128-key stages, 128-byte swizzled;
+//   warp 1      TMEM allocator (512 columns: S0 | S1 | O0 | O1) and MMA
+//               issuer: S_i = Q_i K^T into TMEM (bf16 in, fp32 acc), and
+//               O_i += P_i V with P_i read from TMEM;
+//   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1: one
+//               thread per query row, online softmax in the log2 domain
+//               ("Context Parallelism & Ring Attention", "Softmax is
+//               decomposable": running max, running sum, rescaled output),
+//               P written back to TMEM over S as packed bf16, epilogue
+//               o = O / l and lse = (m + log2 l) ln 2.
+// Key tiles whose smallest position exceeds the block's largest query
+// position are skipped; tiles whose positions are all <= the tile's
+// smallest query position run unmasked; the rest are masked per element.
+// The running max m is kept an INTEGER in the log2 domain (the ceiling of the
+// tile max) and only moved when the tile max exceeds it by more than 8: O and
+// the sums stay consistent with the stale max, P stays <= 2^8, every rescale
+// is an exact power of two, and the bf16 rounding of P = 2^(x - m) does not
+// depend on how the keys are split into partials (so a ring of partials and
+// one monolithic call round P identically).  Two row sums are kept: l over the
+// fp32 P (for lse) and l_b over the bf16 P fed to the tensor core (the output
+// is normalised by l_b, so its weights sum to one exactly).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "cp_internal.h"
+#include "cp_ptx.cuh"
+
+namespace cpattn {
+
+// Sticky device status word of the library (CP_ERR_DEVICE_TIMEOUT when a
+// kernel gave up a bounded wait).  Read by cp_device_status().
+__device__ int g_cp_device_status = 0;
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzle atom block (64 bf16 columns)
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Cfg {
+    static constexpr int kAtoms = D / 64;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;
+    static constexpr int kOffTab = kOffV + kStages * kTileBytes;
+    static constexpr int kOffOrder = kOffTab + kMaxTables * 8;
+    static constexpr int kOffBar = kOffOrder + kMaxPairs * 4;
+    // barriers: q_full, q_empty, drain, k_full[S], v_full[S], kv_empty[S],
+    //           s_full[2], p_full[2], o_full[2], o_empty[2]
+    static constexpr int kNumBars = 3 + 3 * kStages + 8;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kMiscBytes = 16 + kMaxC * 4 + kMaxTables / 8;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct AttnArgs {
+    const int32_t *q_pos;
+    const int32_t *k_pos;
+    long long q_pos_stride, k_pos_stride;
+    float *o, *lse;
+    int C, B, N, Nkv, Sq, Sk;
+    int nqt, nkt, nqb;
+    int kv_shift, kpos_shift;
+    float scale_log2;
+    unsigned long long timeout_ns;
+};
+
+struct Bars {
+    uint64_t *q_full, *q_empty, *drain, *k_full, *v_full, *kv_empty, *s_full, *p_full, *o_full, *o_empty;
+};
+
+template <int D>
+__device__ __forceinline__ Bars bars_at(uint8_t *base) {
+    using K = Cfg<D>;
+    uint64_t *b = reinterpret_cast<uint64_t *>(base + K::kOffBar);
+    Bars r;
+    r.q_full = b + 0;
+    r.q_empty = b + 1;
+    r.drain = b + 2;
+    r.k_full = b + 3;
+    r.v_full = b + 3 + K::kStages;
+    r.kv_empty = b + 3 + 2 * K::kStages;
+    r.s_full = b + 3 + 3 * K::kStages;
+    r.p_full = r.s_full + 2;
+    r.o_full = r.s_full + 4;
+    r.o_empty = r.s_full + 6;
+    return r;
+}
+
+// Work item -> (rank, query block, b, h).
+struct Item {
+    int r, qb, b, h, owner, kvr;
+    int qmax;  // largest query position of the 256-row block (over valid rows)
+};
+
+__device__ __forceinline__ Item decode_item(int idx, const AttnArgs &a, const int *order, const int2 *qtab) {
+    Item it;
+    const int bn = a.B * a.N;
+    const int pr = order[idx / bn];
+    const int bh = idx % bn;
+    it.r = pr / a.nqb;
+    it.qb = pr % a.nqb;
+    it.b = bh / a.N;
+    it.h = bh % a.N;
+    it.owner = (it.r + a.kpos_shift) % a.C;
+    it.kvr = (it.r + a.kv_shift) % a.C;
+    const int qt0 = 2 * it.qb, qt1 = 2 * it.qb + 1;
+    int qmax = qtab[it.r * a.nqt + qt0].y;
+    if (qt1 < a.nqt) qmax = max(qmax, qtab[it.r * a.nqt + qt1].y);
+    it.qmax = qmax;
+    return it;
+}
+
+// Next key tile >= kt that this block must process (nkt if none).
+__device__ __forceinline__ int next_ktile(int kt, int nkt, const int2 *ktab_owner, int qmax, bool sorted) {
+    for (; kt < nkt; ++kt) {
+        if (ktab_owner[kt].x <= qmax) return kt;
+        if (sorted) return nkt;
+    }
+    return nkt;
+}
+
+template <int D>
+__global__ void __maxnreg__(200)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+    using K = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);  // [C*nkt] K tables, then [C*nqt] Q tables
+    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
+    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
+    // bit g set: K tile g holds consecutive positions kmin, kmin+1, ... (mask = column compare)
+    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);
+    const Bars bars = bars_at<D>(smem);
+    const int2 *ktab = tab;
+    const int2 *qtab = tab + a.C * a.nkt;
+
+    // ------------------------------------------------------------ set-up
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int w = 0; w < kMaxTables / 32; ++w) arith_bits[w] = 0u;
+        mbar_init(bars.q_full, 1);
+        mbar_init(bars.q_empty, 1);
+        mbar_init(bars.drain, 1);
+        for (int s = 0; s < K::kStages; ++s) {
+            mbar_init(bars.k_full + s, 1);
+            mbar_init(bars.v_full + s, 1);
+            mbar_init(bars.kv_empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.s_full + i, 1);
+            mbar_init(bars.p_full + i, 4);
+            mbar_init(bars.o_full + i, 1);
+            mbar_init(bars.o_empty + i, 4);
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+
+    __syncthreads();
+    // position tables: (min, max) of every 128-row tile, K tiles per owner rank
+    // first, then Q tiles per rank.
+    {
+        const int nk = a.C * a.nkt, total = nk + a.C * a.nqt;
+        for (int g = warp; g < total; g += kThreads / 32) {
+            const int32_t *p;
+            int rows0, lim;
+            if (g < nk) {
+                const int j = g / a.nkt, kt = g % a.nkt;
+                p = a.k_pos + j * a.k_pos_stride;
+                rows0 = kt * 128;
+                lim = a.Sk;
+            } else {
+                const int r = (g - nk) / a.nqt, qt = (g - nk) % a.nqt;
+                p = a.q_pos + r * a.q_pos_stride;
+                rows0 = qt * 128;
+                lim = a.Sq;
+            }
+            int mn = INT_MAX, mx = INT_MIN;
+            int vals[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int row = rows0 + lane + 32 * m;
+                vals[m] = (row < lim) ? __ldg(p + row) : 0;
+                if (row < lim) {
+                    mn = min(mn, vals[m]);
+                    mx = max(mx, vals[m]);
+                }
+            }
+            mn = __reduce_min_sync(0xffffffffu, mn);
+            mx = __reduce_max_sync(0xffffffffu, mx);
+            if (lane == 0) tab[g] = make_int2(mn, mx);
+            if (g < nk) {
+                const int first = __shfl_sync(0xffffffffu, vals[0], 0);
+                bool ok = true;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int row = rows0 + lane + 32 * m;
+                    if (row < lim) ok &= (static_cast<long long>(vals[m]) == static_cast<long long>(first) + lane + 32 * m);
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                if (lane == 0 && ok) atomicOr(arith_bits + (g >> 5), 1u << (g & 31));
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < a.C) {
+        int ok = 1;
+        for (int kt = 1; kt < a.nkt; ++kt) ok &= (ktab[tid * a.nkt + kt].x >= ktab[tid * a.nkt + kt - 1].x);
+        sorted_flag[tid] = ok;
+    }
+    __syncthreads();
+    // longest-first order of (rank, query block) pairs; the cost scratch lives
+    // in the K stage buffers, which are not in use yet.
+    {
+        int *cost = reinterpret_cast<int *>(smem + K::kOffK);
+        const int np = a.C * a.nqb;
+        for (int p = tid; p < np; p += kThreads) {
+            const int r = p / a.nqb, qb = p % a.nqb;
+            const int owner = (r + a.kpos_shift) % a.C;
+            int qmax = qtab[r * a.nqt + 2 * qb].y;
+            if (2 * qb + 1 < a.nqt) qmax = max(qmax, qtab[r * a.nqt + 2 * qb + 1].y);
+            const int2 *kt_o = ktab + owner * a.nkt;
+            int c = 0;
+            if (sorted_flag[owner]) {
+                int lo = 0, hi = a.nkt;  // first tile with kmin > qmax
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (kt_o[mid].x <= qmax) lo = mid + 1; else hi = mid;
+                }
+                c = lo;
+            } else {
+                for (int kt = 0; kt < a.nkt; ++kt) c += (kt_o[kt].x <= qmax);
+            }
+            cost[p] = c;
+        }
+        __syncthreads();
+        for (int p = tid; p < np; p += kThreads) {
+            const int c = cost[p];
+            int rank = 0;
+            for (int q = 0; q < np; ++q) {
+                const int cq = cost[q];
+                rank += (cq > c) || (cq == c && q < p);
+            }
+            order[rank] = p;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_items = a.C * a.nqb * a.B * a.N;
+    const int hq_per_kv = a.N / a.Nkv;
+    uint8_t *sQ = smem + K::kOffQ;
+    uint8_t *sK = smem + K::kOffK;
+    uint8_t *sV = smem + K::kOffV;
+
+    if (warp == 0) {
+        // -------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, it = 0;
+            bool ok = true;
+            uint32_t issued_mask = 0, parity_mask = 0;  // per stage: a load was issued / its phase parity
+            int q_parity = -1;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const Item itm = decode_item(idx, a, order, qtab);
+                const int2 *kt_o = ktab + itm.owner * a.nkt;
+                const bool srt = sorted_flag[itm.owner];
+                int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt);
+                if (kt >= a.nkt) continue;
+                if (!mbar_wait(bars.q_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                mbar_arrive_expect_tx(bars.q_full, 2 * K::kTileBytes);
+                q_parity = it & 1u;
+                const int qrow = itm.r * a.B + itm.b;
+                for (int i = 0; i < 2; ++i)
+                    for (int at = 0; at < K::kAtoms; ++at)
+                        tma_load_4d(sQ + i * K::kTileBytes + at * kAtomBytes, &tmQ, bars.q_full, 64 * at, itm.h,
+                                    (2 * itm.qb + i) * 128, qrow);
+                ++it;
+                const int hk = itm.h / hq_per_kv;
+                const int kvrow = itm.kvr * a.B + itm.b;
+                for (; kt < a.nkt; kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt)) {
+                    const uint32_t st = kv_it % K::kStages, ph = (kv_it / K::kStages) & 1u;
+                    if (!mbar_wait(bars.kv_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bars.k_full + st, K::kTileBytes);
+                    for (int at = 0; at < K::kAtoms; ++at)
+                        tma_load_4d(sK + st * K::kTileBytes + at * kAtomBytes, &tmK, bars.k_full + st, 64 * at, hk,
+                                    kt * 128, kvrow);
+                    mbar_arrive_expect_tx(bars.v_full + st, K::kTileBytes);
+                    for (int at = 0; at < K::kAtoms; ++at)
+                        tma_load_4d(sV + st * K::kTileBytes + at * kAtomBytes, &tmV, bars.v_full + st, 64 * at, hk,
+                                    kt * 128, kvrow);
+                    issued_mask |= 1u << st;
+                    parity_mask = (parity_mask & ~(1u << st)) | (ph << st);
+                    ++kv_it;
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before shared memory goes away
+                volatile int no_abort = 0;
+                const unsigned long long drain_ns = 100000000ull;
+                if (q_parity >= 0) mbar_wait(bars.q_full, q_parity, &no_abort, drain_ns);
+                for (int s = 0; s < K::kStages; ++s)
+                    if ((issued_mask >> s) & 1u) {
+                        mbar_wait(bars.k_full + s, (parity_mask >> s) & 1u, &no_abort, drain_ns);
+                        mbar_wait(bars.v_full + s, (parity_mask >> s) & 1u, &no_abort, drain_ns);
+                    }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+            const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
+            uint32_t kv_it = 0, it = 0;
+            bool ok = true;
+            auto issue_qk = [&](int i, uint32_t st) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+                    const uint64_t da = smem_desc_sw128(q_base + i * K::kTileBytes + off, 16, 1024);
+                    const uint64_t db = smem_desc_sw128(k_base + st * K::kTileBytes + off, 16, 1024);
+                    umma_ss(tmem + i * 128, da, db, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int i, uint32_t st, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t db = smem_desc_sw128(v_base + st * K::kTileBytes + kk * 2048, kAtomBytes, 1024);
+                    umma_ts(tmem + 256 + i * D, tmem + i * 128 + kk * 8, db, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const Item itm = decode_item(idx, a, order, qtab);
+                const int2 *kt_o = ktab + itm.owner * a.nkt;
+                const bool srt = sorted_flag[itm.owner];
+                int n = 0;
+                for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
+                     kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt))
+                    ++n;
+                if (n == 0) continue;
+                if (!mbar_wait(bars.q_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t prev_st = 0;
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t st = kv_it % K::kStages, ph = (kv_it / K::kStages) & 1u;
+                    if (!mbar_wait(bars.k_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int i = 0; i < 2; ++i) {
+                        if (j > 0) {
+                            const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
+                            if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                            if (j == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                            if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_pv(i, prev_st, j > 1);
+                            if (i == 1) umma_commit(bars.kv_empty + prev_st);
+                        }
+                        issue_qk(i, st);
+                        umma_commit(bars.s_full + i);
+                    }
+                    if (!ok) break;
+                    if (j == n - 1) umma_commit(bars.q_empty);
+                    prev_st = st;
+                    ++kv_it;
+                }
+                if (!ok) break;
+                // tail: P V of the last key tile, then hand O to the epilogue
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
+                    if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    if (n == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_pv(i, prev_st, n > 1);
+                    if (i == 1) umma_commit(bars.kv_empty + prev_st);
+                    umma_commit(bars.o_full + i);
+                }
+                ++it;
+            }
+            // no MMA may still be running when TMEM is released
+            umma_commit(bars.drain);
+            volatile int no_abort = 0;
+            mbar_wait(bars.drain, 0, &no_abort, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- softmax
+        const int wg = (warp - 2) >> 2;           // query tile 0 or 1
+        const int wq = warp & 3;                  // TMEM lane quarter (warp % 4)
+        const int row_in_tile = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + wg * 128;
+        const uint32_t tO = tmem + lane_off + 256 + wg * D;
+        const float sl2 = a.scale_log2;
+        uint32_t kv_count = 0, it = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            const Item itm = decode_item(idx, a, order, qtab);
+            const int2 *kt_o = ktab + itm.owner * a.nkt;
+            const bool srt = sorted_flag[itm.owner];
+            const int qt = 2 * itm.qb + wg;
+            const int row = qt * 128 + row_in_tile;
+            const bool row_valid = row < a.Sq;
+            const int qpos = row_valid ? __ldg(a.q_pos + itm.r * a.q_pos_stride + row) : INT_MIN;
+            const int qmin_t = (qt < a.nqt) ? qtab[itm.r * a.nqt + qt].x : INT_MAX;
+            const int32_t *kpos_o = a.k_pos + itm.owner * a.k_pos_stride;
+            const long long orow = static_cast<long long>(itm.r * a.B + itm.b) * a.Sq + row;
+            float *o_row = a.o + (orow * a.N + itm.h) * D;
+            float *lse_out = a.lse + (static_cast<long long>(itm.r * a.B + itm.b) * a.N + itm.h) * a.Sq + row;
+            float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
+            int j = 0;
+            for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
+                 kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt), ++j) {
+                if (!mbar_wait(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sa[64], sb[64];
+                tmem_ld64(tS, sa);
+                tmem_ld64(tS + 64, sb);
+                const int2 kmm = kt_o[kt];
+                const bool need_mask = (kmm.y > qmin_t) || (kt * 128 + 128 > a.Sk);
+                if (need_mask) {
+                    const int kbase = kt * 128;
+                    const int gk = itm.owner * a.nkt + kt;
+                    const int nvalid = min(128, a.Sk - kbase);
+                    if ((arith_bits[gk >> 5] >> (gk & 31)) & 1u) {
+                        // positions kmin + c: column c is visible iff c <= qpos - kmin
+                        const long long d = static_cast<long long>(qpos) - kmm.x;
+                        const int lim = d < 0 ? -1 : static_cast<int>(min(d, static_cast<long long>(nvalid - 1)));
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c > lim) sa[c] = 0xff800000u;
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (64 + c > lim) sb[c] = 0xff800000u;
+                    } else {
+                        // arbitrary positions: compare column by column, 16 loads at a time
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+#pragma unroll
+                            for (int c = c0; c < c0 + 16; ++c) {
+                                const int kp = (c < nvalid) ? __ldg(kpos_o + kbase + c) : INT_MAX;
+                                if (kp > qpos) sa[c] = 0xff800000u;
+                            }
+                            asm volatile("" ::: "memory");
+                        }
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+#pragma unroll
+                            for (int c = c0; c < c0 + 16; ++c) {
+                                const int kp = (64 + c < nvalid) ? __ldg(kpos_o + kbase + 64 + c) : INT_MAX;
+                                if (kp > qpos) sb[c] = 0xff800000u;
+                            }
+                            asm volatile("" ::: "memory");
+                        }
+                    }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    mx0 = fmaxf(mx0, fmaxf(__uint_as_float(sa[c]), __uint_as_float(sa[c + 1])));
+                    mx1 = fmaxf(mx1, fmaxf(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])));
+                }
+                const float m_tile = fmaxf(mx0, mx1) * sl2;
+                float factor = 1.f;
+                bool rescale = false;
+                if (m_tile > m_run + 8.f) {
+                    const float m_new = ceilf(m_tile);
+                    if (j > 0) {
+                        // exact 2^(m_run - m_new): both are integers (m_run may be -inf)
+                        const float dk = m_run - m_new;
+                        factor = (dk >= -126.f) ? __int_as_float((127 + static_cast<int>(dk)) << 23) : 0.f;
+                        rescale = true;
+                    }
+                    l_run *= factor;
+                    lb_run *= factor;
+                    m_run = m_new;
+                }
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                float sum0 = 0.f, sum1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+                uint32_t pa[32], pb[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sa[2 * c]), sl2, neg_m));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sa[2 * c + 1]), sl2, neg_m));
+                    const float p2 = fast_exp2(fmaf(__uint_as_float(sb[2 * c]), sl2, neg_m));
+                    const float p3 = fast_exp2(fmaf(__uint_as_float(sb[2 * c + 1]), sl2, neg_m));
+                    sum0 += p0 + p1;
+                    sum1 += p2 + p3;
+                    pa[c] = pack_bf16x2(p0, p1);
+                    pb[c] = pack_bf16x2(p2, p3);
+                    sb0 += __uint_as_float(pa[c] << 16) + __uint_as_float(pa[c] & 0xffff0000u);
+                    sb1 += __uint_as_float(pb[c] << 16) + __uint_as_float(pb[c] & 0xffff0000u);
+                }
+                l_run += sum0 + sum1;
+                lb_run += sb0 + sb1;
+                tmem_st32(tS, pa);
+                tmem_st32(tS + 32, pb);
+                // O is quiescent here (the P V of this tile waits for p_full below)
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + c0, ov);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * factor);
+                        tmem_st32(tO + c0, ov);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_full + wg);
+                ++kv_count;
+            }
+            if (!ok) break;
+            if (j == 0) {
+                // nothing visible for this whole block: o = 0, lse = -inf
+                if (row_valid) {
+                    float4 *o4 = reinterpret_cast<float4 *>(o_row);
+#pragma unroll
+                    for (int c = 0; c < D / 4; ++c) o4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *lse_out = -INFINITY;
+                }
+                continue;
+            }
+            if (!mbar_wait(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            const float inv_l = (lb_run > 0.f) ? 1.f / lb_run : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tO + c0, ov);
+                if (row_valid) {
+                    float4 *o4 = reinterpret_cast<float4 *>(o_row + c0);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        o4[c] = make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
+                                            __uint_as_float(ov[4 * c + 2]) * inv_l,
+                                            __uint_as_float(ov[4 * c + 3]) * inv_l);
+                }
+            }
+            if (row_valid) *lse_out = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.o_empty + wg);
+            ++it;
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0 && *abort_flag) atomicExch(&g_cp_device_status, static_cast<int>(CP_ERR_DEVICE_TIMEOUT));
+}
+
+// ------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D bf16 map over [outer][rows][heads][D], box = 64 columns x 1 head x 128 rows x 1.
+bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int64_t rows, int64_t outer) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(heads * D * 2),
+                             static_cast<cuuint64_t>(rows * heads * D * 2)};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
+    using K = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, p.q, D, p.N, p.Sq, p.C * p.B) || !make_map(&mk, p.k, D, p.Nkv, p.Sk, p.C * p.B) ||
+        !make_map(&mv, p.v, D, p.Nkv, p.Sk, p.C * p.B))
+        return CP_ERR_CUDA;
+    AttnArgs a;
+    a.q_pos = p.q_pos;
+    a.k_pos = p.k_pos;
+    a.q_pos_stride = p.q_pos_stride;
+    a.k_pos_stride = p.k_pos_stride;
+    a.o = p.o;
+    a.lse = p.lse;
+    a.C = p.C;
+    a.B = static_cast<int>(p.B);
+    a.N = static_cast<int>(p.N);
+    a.Nkv = static_cast<int>(p.Nkv);
+    a.Sq = static_cast<int>(p.Sq);
+    a.Sk = static_cast<int>(p.Sk);
+    a.nqt = static_cast<int>((p.Sq + 127) / 128);
+    a.nkt = static_cast<int>((p.Sk + 127) / 128);
+    a.nqb = (a.nqt + 1) / 2;
+    a.kv_shift = p.kv_shift;
+    a.kpos_shift = p.kpos_shift;
+    a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
+    a.timeout_ns = 2000000000ull;
+    const long long n_items = static_cast<long long>(p.C) * a.nqb * p.B * p.N;
+    if (n_items <= 0) return CP_OK;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        K::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return CP_ERR_CUDA;
+    const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
+    attn_fwd_kernel<D><<<grid, kThreads, K::kSmemBytes, stream>>>(mq, mk, mv, a);
+    return last_launch_status();
+}
+
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+cp_status validate_attn(const AttnProblem &p) {
+    if (!p.q || !p.k || !p.v || !p.q_pos || !p.k_pos || !p.o || !p.lse) return CP_ERR_NULL;
+    if (p.C < 1 || p.C > kMaxC || p.B < 1 || p.N < 1 || p.Nkv < 1 || p.Sq < 1 || p.Sk < 1) return CP_ERR_SHAPE;
+    if (p.D != 64 && p.D != 128) return CP_ERR_UNSUPPORTED;
+    if (p.N % p.Nkv != 0) return CP_ERR_DIVISIBILITY;
+    if (!(std::isfinite(p.scale) && p.scale > 0.f)) return CP_ERR_ARGUMENT;
+    if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.o) || !aligned16(p.q_pos) ||
+        !aligned16(p.k_pos) || !aligned16(p.lse))
+        return CP_ERR_ALIGNMENT;
+    const int64_t nqt = (p.Sq + 127) / 128, nkt = (p.Sk + 127) / 128;
+    if (p.C * (nqt + nkt) > kMaxTables || p.C * ((nqt + 1) / 2) > kMaxPairs) return CP_ERR_SHAPE;
+    if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.B * p.N * p.C > INT32_MAX / 4 ||
+        static_cast<int64_t>(p.C) * ((nqt + 1) / 2) * p.B * p.N > INT32_MAX)
+        return CP_ERR_SHAPE;
+    if (p.kv_shift < 0 || p.kv_shift >= p.C || p.kpos_shift < 0 || p.kpos_shift >= p.C) return CP_ERR_ARGUMENT;
+    return CP_OK;
+}
+
+cp_status launch_attn(const AttnProblem &p, cudaStream_t stream) {
+    cp_status st = validate_attn(p);
+    if (st != CP_OK) return st;
+    return p.D == 128 ? launch_typed<128>(p, stream) : launch_typed<64>(p, stream);
+}
+
+}  // namespace cpattn
+
+extern "C" cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int32_t *q_pos,
+                                     const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,
+                                     int64_t Nkv, int64_t D, float scale, float *o, float *lse,
+                                     cudaStream_t stream) {
+    cpattn::AttnProblem p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.q_pos = q_pos;
+    p.k_pos = k_pos;
+    p.q_pos_stride = 0;
+    p.k_pos_stride = 0;
+    p.o = o;
+    p.lse = lse;
+    p.C = 1;
+    p.B = B;
+    p.N = N;
+    p.Nkv = Nkv;
+    p.D = D;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.kv_shift = 0;
+    p.kpos_shift = 0;
+    p.scale = scale;
+    return cpattn::launch_attn(p, stream);
+}
+
+extern "C" cp_status cp_device_status(int *code, int clear, cudaStream_t stream) {
+    if (!code) return CP_ERR_NULL;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, cpattn::g_cp_device_status, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+    *code = v;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(cpattn::g_cp_device_status, &zero, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+    }
+    return CP_OK;
+}

@@ -1,0 +1,61 @@
+// cp_internal.h -- host-side declarations shared by the translation units of
+// libcpattn (validation helpers and internal launchers).  Not installed.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "../../include/cpattn.h"
+
+namespace cpattn {
+
+constexpr int kTileM = 128;          // query rows per tile
+constexpr int kTileN = 128;          // keys per tile
+constexpr int kMaxTables = 2048;     // C * (ceil(Sq/128) + ceil(Sk/128)) limit
+constexpr int kMaxPairs = 1024;      // C * ceil(Sq/256) limit
+constexpr int kMaxC = 64;            // virtual ranks per launch
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t dtype_size(cp_dtype d) { return d == CP_BF16 ? 2 : (d == CP_F32 ? 4 : 0); }
+
+inline cp_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return CP_OK;
+    return CP_ERR_CUDA;
+}
+
+// Reads and clears the sticky launch error of this thread.
+inline cp_status last_launch_status() { return cuda_status(cudaGetLastError()); }
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// One batched attention launch over C "rank" problems.  Rank r reads its
+// queries from q[r] (rank stride C-major: [C][B][Sq][N][D]), its K/V from rank
+// (r + kv_shift) mod C of k/v, its query positions from q_pos + r*q_pos_stride
+// and its key positions from k_pos + ((r + kpos_shift) mod C)*k_pos_stride.
+struct AttnProblem {
+    const void *q, *k, *v;
+    const int32_t *q_pos, *k_pos;
+    int64_t q_pos_stride, k_pos_stride;
+    float *o, *lse;               // o [C][B][Sq][N][D] fp32, lse [C][B][N][Sq]
+    int C;
+    int64_t B, N, Nkv, D, Sq, Sk;
+    int kv_shift, kpos_shift;
+    float scale;
+};
+
+// Host validation shared by cp_attn_partial and the ring.
+cp_status validate_attn(const AttnProblem &p);
+// Validate then enqueue the attention kernel on `stream`.
+cp_status launch_attn(const AttnProblem &p, cudaStream_t stream);
+
+// In-place LSE merge over `rows` rows of D fp32 values laid out as
+// o [B][Sq][N][D], lse [B][N][Sq] (B may fold the rank dimension).
+cp_status launch_merge(float *o_acc, float *lse_acc, const float *o_tile, const float *lse_tile, int64_t B,
+                       int64_t Sq, int64_t N, int64_t D, cudaStream_t stream);
+
+// fp32 -> bf16 (round to nearest even), n elements, n % 8 == 0.
+cp_status launch_f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t stream);
+
+}  // namespace cpattn

@@ -1,0 +1,174 @@
+"""Python binding of the libcpattn C ABI (same names as include/cpattn.h).
+
+Argument marshalling only: shapes and pointers are read from torch tensors,
+outputs are allocated with torch when not given, and the call is enqueued on
+the current torch CUDA stream.  All arithmetic happens in the CUDA library.
+"""
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_F32, CP_GLOBAL_ORDER, CP_HEAD_TO_SEQ, CP_RANK_ORDER,
+                   CP_SEQ_TO_HEAD, CP_ZIGZAG, CpError)
+
+__all__ = [
+    "cp_zigzag_shard", "cp_zigzag_unshard", "cp_zigzag_positions", "cp_ulysses_relayout", "cp_attn_partial",
+    "cp_lse_merge", "cp_ring_workspace_size", "cp_ring_attention_fwd", "cp_device_status", "cp_version",
+    "CP_BF16", "CP_F32", "CP_ZIGZAG", "CP_CONTIGUOUS", "CP_SEQ_TO_HEAD", "CP_HEAD_TO_SEQ", "CP_RANK_ORDER",
+    "CP_GLOBAL_ORDER", "CpError",
+]
+
+_DT = {torch.bfloat16: CP_BF16, torch.float32: CP_F32}
+
+
+def _dtype_code(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError("unsupported dtype %s (bf16 or fp32)" % t.dtype)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def cp_version():
+    return _lib.lib().cp_version().decode()
+
+
+def cp_zigzag_shard(x, C, layout=CP_ZIGZAG, out=None, stream=None):
+    """x [B,S,N,D] -> rank-major shards [C,B,S/C,N,D] (bit-exact permutation)."""
+    B, S, N, D = x.shape
+    if out is None:
+        out = torch.empty((C, B, S // C, N, D), dtype=x.dtype, device=x.device)
+    st = _lib.lib().cp_zigzag_shard(_ptr(x), _ptr(out), B, S, N, D, C, _dtype_code(x), layout, _stream(stream))
+    _lib.check("cp_zigzag_shard", st)
+    return out
+
+
+def cp_zigzag_unshard(x_sh, layout=CP_ZIGZAG, out=None, stream=None):
+    """Rank-major shards [C,B,s,N,D] -> x [B,C*s,N,D] in global order."""
+    C, B, s, N, D = x_sh.shape
+    if out is None:
+        out = torch.empty((B, C * s, N, D), dtype=x_sh.dtype, device=x_sh.device)
+    st = _lib.lib().cp_zigzag_unshard(_ptr(x_sh), _ptr(out), B, C * s, N, D, C, _dtype_code(x_sh), layout,
+                                      _stream(stream))
+    _lib.check("cp_zigzag_unshard", st)
+    return out
+
+
+def cp_zigzag_positions(S, C, layout=CP_ZIGZAG, device="cuda", out=None, stream=None):
+    """int32 [C, S/C] global positions of every local token."""
+    dev = torch.device(device)
+    if out is None:
+        out = torch.empty((C, S // C), dtype=torch.int32, device=dev)
+    on_dev = 1 if out.is_cuda else 0
+    st = _lib.lib().cp_zigzag_positions(_ptr(out), S, C, layout, on_dev, _stream(stream) if on_dev else None)
+    _lib.check("cp_zigzag_positions", st)
+    return out
+
+
+def cp_ulysses_relayout(x, C, direction=CP_SEQ_TO_HEAD, order=CP_RANK_ORDER, out=None, stream=None):
+    """[C,B,S/C,N,D] <-> [C,B,S,N/C,D] (Ulysses all-to-all as a local permutation)."""
+    if direction == CP_SEQ_TO_HEAD:
+        Cx, B, s, N, D = x.shape
+        S = C * s
+        shape = (C, B, S, N // C, D)
+    else:
+        Cx, B, S, nh, D = x.shape
+        N = nh * C
+        shape = (C, B, S // C, N, D)
+    if Cx != C:
+        raise ValueError("leading dimension must be C")
+    if out is None:
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    st = _lib.lib().cp_ulysses_relayout(_ptr(x), _ptr(out), B, S, N, D, C, _dtype_code(x), direction, order,
+                                        _stream(stream))
+    _lib.check("cp_ulysses_relayout", st)
+    return out
+
+
+def cp_attn_partial(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, stream=None):
+    """Partial causal attention -> (o fp32 [B,Sq,N,D], lse fp32 [B,N,Sq])."""
+    B, Sq, N, D = q.shape
+    Sk, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty((B, Sq, N, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, N, Sq), dtype=torch.float32, device=q.device)
+    st = _lib.lib().cp_attn_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D,
+                                    float(scale), _ptr(o), _ptr(lse), _stream(stream))
+    _lib.check("cp_attn_partial", st)
+    return o, lse
+
+
+def cp_lse_merge(o_acc, lse_acc, o_tile, lse_tile, stream=None):
+    """In-place merge of (o_tile, lse_tile) into (o_acc, lse_acc)."""
+    B, Sq, N, D = o_acc.shape
+    st = _lib.lib().cp_lse_merge(_ptr(o_acc), _ptr(lse_acc), _ptr(o_tile), _ptr(lse_tile), B, Sq, N, D,
+                                 _stream(stream))
+    _lib.check("cp_lse_merge", st)
+    return o_acc, lse_acc
+
+
+def cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch=0, o_dtype=CP_F32):
+    n = ctypes.c_size_t(0)
+    st = _lib.lib().cp_ring_workspace_size(B, S, N, Nkv, D, C, int(prefetch), o_dtype, ctypes.byref(n))
+    _lib.check("cp_ring_workspace_size", st)
+    return n.value
+
+
+def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, prefetch=0, o_dtype=CP_F32,
+                          workspace=None, o=None, lse=None, events=None, stream=None):
+    """Ring attention forward over C resident virtual ranks.
+
+    Returns (o_sh [C,B,s,N,D] of o_dtype, lse_sh fp32 [C,B,N,s]).  `events`, if
+    given, is a list of >= 4*C recorded torch.cuda.Event objects (see the C
+    header for their meaning)."""
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    S = C * s
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q_sh.device
+    if o is None:
+        o = torch.empty((C, B, s, N, D), dtype=torch.float32 if o_dtype == CP_F32 else torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
+    need = cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, o_dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    L = _lib.lib()
+    args = [_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, S, N, Nkv, D, C, float(scale), layout, int(prefetch),
+            _ptr(o), o_dtype, _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream)]
+    if events is None:
+        st = L.cp_ring_attention_fwd(*args)
+        _lib.check("cp_ring_attention_fwd", st)
+    else:
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        st = L.cp_ring_attention_fwd_traced(*args, arr, len(events))
+        _lib.check("cp_ring_attention_fwd_traced", st)
+    return o, lse
+
+
+def cp_device_status(clear=True, stream=None):
+    """Synchronise the stream and return the library's device status code."""
+    code = ctypes.c_int(0)
+    st = _lib.lib().cp_device_status(ctypes.byref(code), 1 if clear else 0, _stream(stream))
+    _lib.check("cp_device_status", st)
+    return code.value

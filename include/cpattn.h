@@ -1,0 +1,230 @@
+/*
+ * cpattn.h -- C ABI of libcpattn: blockwise causal attention with
+ * log-sum-exp merging for ring / zigzag context parallelism, for C virtual
+ * ranks held as buffers on ONE GB300 GPU (sm_103a).
+ *
+ * Source pages (cited by title and section):
+ *   [OCP]   "On Context Parallelism": All-gather, All-to-all, Peer-to-peer
+ *   [DAY74] "Context parallelism -- splitting the sequence across GPUs"
+ *   [RING]  "Context Parallelism & Ring Attention"
+ *   [HB]    "Context parallelism: Ring Attention and Ulysses"
+ *   [APPF]  "Appendix F: Context Parallelism and MoE Parallel Folding"
+ *
+ * General conventions (all entry points):
+ *   - Device pointers are raw CUDA device addresses owned by the caller; the
+ *     library never allocates device memory on these paths and never frees
+ *     caller memory.  Work that needs scratch takes a caller workspace.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) unless
+ *     stated otherwise; they return as soon as the work is enqueued.
+ *   - Arguments are validated on the host BEFORE anything is enqueued; on a
+ *     validation error nothing is launched and the call returns the status.
+ *     No call aborts, throws or prints.
+ *   - Tensors are dense, row-major, with the layouts given per call:
+ *       sequence-sharded, rank-major: X_sh [C][B][s][N][D], s = S/C
+ *       lse: [B][N][Sq] (rank-major shards: [C][B][N][s])
+ *     ([OCP] Peer-to-peer / Forward: output [B,S/C,N,D], lse [B,N,S/C].)
+ *   - Every device pointer must be 16-byte aligned; rows of N*D elements
+ *     must be a multiple of 16 bytes.
+ *   - Failures of a launch are reported as CP_ERR_CUDA (cudaGetLastError is
+ *     read and cleared).  A kernel that gives up a bounded device-side wait
+ *     records CP_ERR_DEVICE_TIMEOUT in a device status word, readable with
+ *     cp_device_status().
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cp_status {
+    CP_OK = 0,
+    CP_ERR_NULL = 1,          /* a required pointer is NULL */
+    CP_ERR_SHAPE = 2,         /* a size is <= 0 or out of the supported range */
+    CP_ERR_DIVISIBILITY = 3,  /* S % 2C (zigzag), S % C, N % C, Nkv % C or N % Nkv */
+    CP_ERR_DTYPE = 4,         /* unknown cp_dtype */
+    CP_ERR_ALIGNMENT = 5,     /* pointer or row not 16-byte aligned */
+    CP_ERR_WORKSPACE = 6,     /* workspace NULL or smaller than cp_ring_workspace_size */
+    CP_ERR_UNSUPPORTED = 7,   /* e.g. D not in {64, 128} for attention */
+    CP_ERR_CUDA = 8,          /* a CUDA runtime call or launch failed */
+    CP_ERR_DEVICE_TIMEOUT = 9,/* a kernel gave up a bounded wait (see cp_device_status) */
+    CP_ERR_ARGUMENT = 10      /* any other invalid argument (scale, enum, event count) */
+} cp_status;
+
+typedef enum cp_dtype { CP_BF16 = 0, CP_F32 = 1 } cp_dtype;
+typedef enum cp_layout { CP_ZIGZAG = 0, CP_CONTIGUOUS = 1 } cp_layout;
+typedef enum cp_dir { CP_SEQ_TO_HEAD = 0, CP_HEAD_TO_SEQ = 1 } cp_dir;
+typedef enum cp_seq_order { CP_RANK_ORDER = 0, CP_GLOBAL_ORDER = 1 } cp_seq_order;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *cp_status_string(cp_status status);
+
+/* Library version as "major.minor.patch" (static string). */
+const char *cp_version(void);
+
+/*
+ * cp_zigzag_shard -- split a full sequence into C rank-major shards.
+ * [OCP] All-gather: S is cut into 2C chunks of t = S/(2C) tokens and rank r
+ * owns [chunk r | chunk 2C-1-r] (layout CP_ZIGZAG; TE's "DualChunkSwap").
+ * [RING] "The last remaining axis": rank r owns tokens [r*s, (r+1)*s)
+ * (layout CP_CONTIGUOUS).
+ *   x     : device, [B][S][N][D] of `dtype`, read only
+ *   x_sh  : device, [C][B][S/C][N][D] of `dtype`, written (must not overlap x)
+ * Requires S % (2C) == 0 (zigzag) or S % C == 0 (contiguous), C >= 1.
+ * The result is a bit-exact permutation of x.
+ */
+cp_status cp_zigzag_shard(const void *x, void *x_sh, int64_t B, int64_t S, int64_t N, int64_t D,
+                          int C, cp_dtype dtype, cp_layout layout, cudaStream_t stream);
+
+/*
+ * cp_zigzag_unshard -- inverse of cp_zigzag_shard: gather the C shards back
+ * into global sequence order ([OCP] All-gather: the rank-order result
+ * [chunk 0, chunk 7, chunk 1, chunk 6, ...] reordered to sequence order).
+ *   x_sh  : device, [C][B][S/C][N][D], read only
+ *   x     : device, [B][S][N][D], written (must not overlap x_sh)
+ */
+cp_status cp_zigzag_unshard(const void *x_sh, void *x, int64_t B, int64_t S, int64_t N, int64_t D,
+                            int C, cp_dtype dtype, cp_layout layout, cudaStream_t stream);
+
+/*
+ * cp_zigzag_positions -- global position of every local token, int32 [C][S/C]:
+ * zigzag: pos[r] = [r*t .. r*t+t-1] ++ [(2C-1-r)*t .. (2C-1-r)*t+t-1]
+ * ([OCP] All-gather ownership; the ring's per-owner positions in
+ * Peer-to-peer / Forward); contiguous: pos[r] = [r*s .. r*s+s-1].
+ *   pos       : device (on_device != 0, written by a kernel on `stream`) or
+ *               host (on_device == 0, written synchronously; stream unused)
+ * Requires S <= INT32_MAX.
+ */
+cp_status cp_zigzag_positions(int32_t *pos, int64_t S, int C, cp_layout layout, int on_device,
+                              cudaStream_t stream);
+
+/*
+ * cp_ulysses_relayout -- the Ulysses all-to-all as a local permutation of
+ * rank-major buffers ([HB] "Ulysses" seq_to_head / head_to_seq; [OCP]
+ * All-to-all; [APPF] eq. (96) [B,S/C,H,d_h] -> [B,S,H/C,d_h]).
+ *   CP_SEQ_TO_HEAD: in [C][B][S/C][N][D] -> out [C][B][S][N/C][D] with
+ *       out[r][b][j*s+u][h'][d] = in[j][b][u][r*N/C + h'][d]
+ *     (rank r receives head group r from every shard, shards in rank order).
+ *   CP_HEAD_TO_SEQ: the exact inverse (out and in swap roles).
+ *   CP_GLOBAL_ORDER additionally puts the gathered sequence in global order
+ *     (row j*s+u -> zigzag position of row u of rank j; [OCP] All-to-all:
+ *     TE reorders the chunks into global order before attention).  Requires
+ *     S % (2C) == 0.  CP_RANK_ORDER is the literal all-to-all.
+ * Requires S % C == 0 and N % C == 0 (head divisibility, [OCP] All-to-all;
+ * [HB] "Ulysses").  in and out must not overlap.  Bit-exact permutation.
+ */
+cp_status cp_ulysses_relayout(const void *in, void *out, int64_t B, int64_t S, int64_t N, int64_t D,
+                              int C, cp_dtype dtype, cp_dir dir, cp_seq_order order,
+                              cudaStream_t stream);
+
+/*
+ * cp_attn_partial -- partial causal attention with explicit positions,
+ * returning the normalised output and the per-row log-sum-exp.
+ * [OCP] Peer-to-peer / Forward (attention(q, k, v, q_positions,
+ * kv_positions, scale) -> tile_output, tile_lse); [HB] cp_common.py;
+ * [DAY74] the causal softmax formula.  For each (b, h, i):
+ *   visible keys V(i) = { j : k_pos[j] <= q_pos[i] }
+ *   s_j = scale * <q_i, k_j>,  lse_i = ln sum_{j in V(i)} e^{s_j}
+ *   o_i = sum_{j in V(i)} e^{s_j - lse_i} v_j
+ *   a row with no visible key gets lse = -inf and o = 0.
+ *   q      : device bf16 [B][Sq][N][D]
+ *   k, v   : device bf16 [B][Sk][Nkv][D]; query head h reads KV head h/(N/Nkv)
+ *   q_pos  : device int32 [Sq];  k_pos : device int32 [Sk] (any values)
+ *   o      : device fp32 [B][Sq][N][D], written
+ *   lse    : device fp32 [B][N][Sq], written (natural log)
+ * Requires D in {64, 128}, N % Nkv == 0, scale finite and > 0,
+ * ceil(Sq/128) + ceil(Sk/128) <= 2048.  Runs on the tensor cores
+ * (bf16 products, fp32 accumulation and softmax).
+ */
+cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int32_t *q_pos,
+                          const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,
+                          int64_t Nkv, int64_t D, float scale, float *o, float *lse,
+                          cudaStream_t stream);
+
+/*
+ * cp_lse_merge -- merge a completed partial into an accumulator, in place.
+ * [OCP] Peer-to-peer / Forward, the tile merge:
+ *   lse = logaddexp(lse_acc, lse_tile)
+ *   o   = e^{lse_acc - lse} * o_acc + e^{lse_tile - lse} * o_tile
+ * ([HB] "Ring Attention" gives the same two formulas.)  A row whose
+ * lse_tile is -inf is left untouched; a row whose lse_acc is -inf takes the
+ * tile's values.
+ *   o_acc, lse_acc   : device fp32 [B][Sq][N][D] / [B][N][Sq], read+written
+ *   o_tile, lse_tile : device fp32, same shapes, read only
+ */
+cp_status cp_lse_merge(float *o_acc, float *lse_acc, const float *o_tile, const float *lse_tile,
+                       int64_t B, int64_t Sq, int64_t N, int64_t D, cudaStream_t stream);
+
+/*
+ * cp_ring_workspace_size -- bytes of device workspace cp_ring_attention_fwd
+ * needs for these sizes: the per-step partial (fp32 o and lse for all C
+ * ranks), an fp32 accumulator when o_dtype is CP_BF16, and with prefetch two
+ * K/V rotation buffers.  Host only; *bytes is written on success.
+ */
+cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
+                                 int prefetch, cp_dtype o_dtype, size_t *bytes);
+
+/*
+ * cp_ring_attention_fwd -- ring (P2P) context-parallel attention forward for
+ * C virtual ranks resident on this GPU.  [OCP] Peer-to-peer / Forward;
+ * [RING] "The ring"; [HB] "Ring Attention".  For step = 0 .. C-1 every rank
+ * r attends its queries to the K/V block of owner (r - step) mod C (with
+ * both sides' positions) and merges the partial into its running (o, lse);
+ * step 0 writes the accumulator directly.  All C ranks of a step run in one
+ * launch (zigzag makes their work equal, [RING] "The zigzag fix").
+ *   q_sh          : device bf16 [C][B][S/C][N][D]
+ *   k_sh, v_sh    : device bf16 [C][B][S/C][Nkv][D]
+ *   pos           : device int32 [C][S/C] global positions (cp_zigzag_positions)
+ *   layout        : selects the divisibility rule only (S % 2C for zigzag,
+ *                   S % C for contiguous); masks come from `pos`
+ *   prefetch      : 0 = zero-copy (each step reads the owner's resident
+ *                   block); 1 = the ring exchange is emulated by device
+ *                   copies of the next step's K/V on a second stream,
+ *                   overlapped with the current step and ordered by events
+ *   o_sh          : device [C][B][S/C][N][D] of o_dtype (CP_F32 or CP_BF16)
+ *   lse_sh        : device fp32 [C][B][N][S/C]
+ *   workspace     : device, >= cp_ring_workspace_size(...) bytes, 256-byte
+ *                   aligned, caller-owned, contents need not be initialised
+ * Same attention restrictions as cp_attn_partial.
+ */
+cp_status cp_ring_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh,
+                                const int32_t *pos, int64_t B, int64_t S, int64_t N, int64_t Nkv,
+                                int64_t D, int C, float scale, cp_layout layout, int prefetch,
+                                void *o_sh, cp_dtype o_dtype, float *lse_sh, void *workspace,
+                                size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * cp_ring_attention_fwd_traced -- cp_ring_attention_fwd that also records
+ * CUDA events on `stream` around every kernel it launches, for timing:
+ *   events[4*step + 0], events[4*step + 1] : before / after the attention
+ *                                            launch of `step`
+ *   events[4*step + 2], events[4*step + 3] : before / after the merge launch
+ *                                            of `step` (step >= 1; for
+ *                                            step 0 both are recorded
+ *                                            back to back)
+ * n_events must be >= 4*C; events are caller-created (cudaEventCreate).
+ */
+cp_status cp_ring_attention_fwd_traced(const void *q_sh, const void *k_sh, const void *v_sh,
+                                       const int32_t *pos, int64_t B, int64_t S, int64_t N,
+                                       int64_t Nkv, int64_t D, int C, float scale,
+                                       cp_layout layout, int prefetch, void *o_sh,
+                                       cp_dtype o_dtype, float *lse_sh, void *workspace,
+                                       size_t ws_bytes, cudaStream_t stream,
+                                       cudaEvent_t const *events, int n_events);
+
+/*
+ * cp_device_status -- synchronise `stream`, then read (and, if clear != 0,
+ * reset) the library's device status word on the current device.
+ * *code receives CP_OK, or CP_ERR_DEVICE_TIMEOUT if a kernel of this library
+ * gave up a bounded wait since the last reset.  Host-blocking.
+ */
+cp_status cp_device_status(int *code, int clear, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CPATTN_H */

@@ -1,0 +1,99 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects invalid arguments on the host before launching."""
+import ctypes
+
+import pytest
+
+from context_causal_attention_gb300 import _lib
+
+FAKE = ctypes.c_void_p(4096)          # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(4096 + 8)
+NULL = None
+
+
+def test_every_header_symbol_is_exported(cplib):
+    names = _lib.header_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(cplib, n), n
+
+
+def test_status_strings(cplib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert cplib.cp_status_string(code).decode().startswith(name)
+    assert cplib.cp_version().decode().count(".") == 2
+
+
+def _attn(cplib, q=FAKE, k=FAKE, v=FAKE, qp=FAKE, kp=FAKE, B=1, Sq=256, Sk=256, N=2, Nkv=2, D=64, scale=0.125,
+          o=FAKE, lse=FAKE):
+    return cplib.cp_attn_partial(q, k, v, qp, kp, B, Sq, Sk, N, Nkv, D, scale, o, lse, None)
+
+
+def test_attn_partial_validation(cplib):
+    assert _attn(cplib, q=NULL) == 1
+    assert _attn(cplib, lse=NULL) == 1
+    assert _attn(cplib, D=96) == 7
+    assert _attn(cplib, D=256) == 7
+    assert _attn(cplib, N=3, Nkv=2) == 3
+    assert _attn(cplib, Sq=0) == 2
+    assert _attn(cplib, scale=float("nan")) == 10
+    assert _attn(cplib, scale=-1.0) == 10
+    assert _attn(cplib, q=MISALIGNED) == 5
+    assert _attn(cplib, Sq=200000, Sk=200000) == 2  # position tables exceed the on-chip limit
+
+
+def test_shard_validation(cplib):
+    f = cplib.cp_zigzag_shard
+    assert f(NULL, FAKE, 1, 256, 2, 64, 2, 0, 0, None) == 1
+    assert f(FAKE, FAKE, 1, 250, 2, 64, 2, 0, 0, None) == 3   # S % 2C
+    assert f(FAKE, FAKE, 1, 251, 2, 64, 5, 0, 1, None) == 3   # S % C (contiguous)
+    assert f(FAKE, ctypes.c_void_p(1 << 30), 1, 256, 2, 64, 2, 7, 0, None) == 4  # dtype
+    assert f(FAKE, ctypes.c_void_p(1 << 30), 1, 256, 1, 4, 2, 0, 0, None) == 5   # row of 8 bytes
+    assert f(FAKE, FAKE, 1, 256, 2, 64, 2, 0, 0, None) == 10  # in/out overlap
+    assert cplib.cp_zigzag_unshard(FAKE, MISALIGNED, 1, 256, 2, 64, 2, 0, 0, None) == 5
+
+
+def test_positions_and_relayout_validation(cplib):
+    assert cplib.cp_zigzag_positions(NULL, 256, 2, 0, 0, None) == 1
+    assert cplib.cp_zigzag_positions(FAKE, 250, 2, 0, 1, None) == 3
+    r = cplib.cp_ulysses_relayout
+    assert r(FAKE, ctypes.c_void_p(1 << 30), 1, 4096, 15, 64, 4, 0, 0, 0, None) == 3   # N % C
+    assert r(FAKE, ctypes.c_void_p(1 << 30), 1, 4098, 16, 64, 4, 0, 0, 0, None) == 3   # S % C
+    assert r(FAKE, ctypes.c_void_p(1 << 30), 1, 4100, 16, 64, 4, 0, 0, 1, None) == 3   # S % 2C, global order
+    assert r(FAKE, ctypes.c_void_p(1 << 30), 1, 4096, 16, 64, 4, 0, 5, 0, None) == 10  # direction
+
+
+def test_positions_host_path_matches_oracle(cplib):
+    import numpy as np
+    import oracle as O
+    for layout in (0, 1):
+        for S, C in ((256, 2), (4096, 4), (96, 3) if layout == 1 else (96, 4)):
+            pos = np.zeros(S, dtype=np.int32)
+            st = cplib.cp_zigzag_positions(pos.ctypes.data_as(ctypes.c_void_p), S, C, layout, 0, None)
+            assert st == 0
+            assert np.array_equal(pos.reshape(C, S // C), O.positions(S, C, layout))
+
+
+def test_merge_and_ring_validation(cplib):
+    m = cplib.cp_lse_merge
+    assert m(NULL, FAKE, FAKE, FAKE, 1, 16, 2, 64, None) == 1
+    assert m(FAKE, FAKE, MISALIGNED, FAKE, 1, 16, 2, 64, None) == 5
+    n = ctypes.c_size_t(0)
+    assert cplib.cp_ring_workspace_size(1, 256, 2, 2, 64, 2, 0, 1, ctypes.byref(n)) == 0
+    assert n.value > 0
+    need = n.value
+    ring = cplib.cp_ring_attention_fwd
+    args = [FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 2, 64, 2, 0.125, 0, 0, FAKE, 1, FAKE]
+    assert ring(*args, NULL, 0, None) == 6                       # workspace missing
+    assert ring(*args, FAKE, need - 1, None) == 6                # workspace too small
+    bad = list(args)
+    bad[5] = 254                                                 # S % 2C
+    assert ring(*bad, FAKE, need, None) == 3
+    bad = list(args)
+    bad[14] = 9                                                  # o dtype
+    assert ring(*bad, FAKE, need, None) == 4
+    bad = list(args)
+    bad[8] = 80                                                  # D
+    assert ring(*bad, FAKE, 1 << 40, None) == 7
+    ev = (ctypes.c_void_p * 3)()
+    assert cplib.cp_ring_attention_fwd_traced(*args, FAKE, need, None, ev, 3) == 10  # needs 4C events
