@@ -55,6 +55,8 @@ def lib():
     L.cp_status_string.restype = ctypes.c_char_p
     L.cp_version.argtypes = []
     L.cp_version.restype = ctypes.c_char_p
+    L.cp_last_cuda_error.argtypes = []
+    L.cp_last_cuda_error.restype = ctypes.c_char_p
     L.cp_zigzag_shard.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, vp]
     L.cp_zigzag_unshard.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, vp]
     L.cp_zigzag_positions.argtypes = [vp, i64, i32, i32, i32, vp]
@@ -68,7 +70,7 @@ def lib():
                                                i32, vp, vp, sz, vp, vp, i32]
     L.cp_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
     for name in header_symbols():
-        if name not in ("cp_status_string", "cp_version"):
+        if name not in ("cp_status_string", "cp_version", "cp_last_cuda_error"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -77,4 +79,6 @@ def lib():
 def check(fn, status):
     if status != CP_OK:
         text = lib().cp_status_string(status).decode()
+        if status == 8:
+            text += " (%s)" % lib().cp_last_cuda_error().decode()
         raise CpError(fn, status, text)

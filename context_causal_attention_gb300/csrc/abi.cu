@@ -1,4 +1,6 @@
 // abi.cu -- status strings and version of the libcpattn C ABI.
+#include <cuda_runtime.h>
+
 #include "cp_internal.h"
 
 extern "C" const char *cp_status_string(cp_status status) {
@@ -19,3 +21,14 @@ extern "C" const char *cp_status_string(cp_status status) {
 }
 
 extern "C" const char *cp_version(void) { return "0.1.0"; }
+
+namespace cpattn {
+namespace {
+thread_local cudaError_t t_last_error = cudaSuccess;
+}
+void note_cuda_error(cudaError_t e) { t_last_error = e; }
+}  // namespace cpattn
+
+extern "C" const char *cp_last_cuda_error(void) {
+    return cpattn::t_last_error == cudaSuccess ? "no error" : cudaGetErrorString(cpattn::t_last_error);
+}

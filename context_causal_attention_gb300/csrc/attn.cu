@@ -16,7 +16,8 @@
 //   warp 1      TMEM allocator (512 columns: S0 | S1 | O0 | O1) and MMA
 //               issuer: S_i = Q_i K^T into TMEM (bf16 in, fp32 acc), and
 //               O_i += P_i V with P_i read from TMEM;
-//   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1: one
+//   warps 2-3   idle;
+//   warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1: one
 //               thread per query row, online softmax in the log2 domain
 //               ("Context Parallelism & Ring Attention", "Softmax is
 //               decomposable": running max, running sum, rescaled output),
@@ -52,7 +53,9 @@ __device__ int g_cp_device_status = 0;
 
 namespace {
 
-constexpr int kThreads = 320;
+// 12 warps: three per SM sub-partition, so at most 168 registers per thread
+// (each sub-partition holds 16K registers).
+constexpr int kThreads = 384;
 constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzle atom block (64 bf16 columns)
 constexpr uint32_t kTmemCols = 512;
 
@@ -144,7 +147,7 @@ __device__ __forceinline__ int next_ktile(int kt, int nkt, const int2 *ktab_owne
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
     using K = Cfg<D>;
@@ -423,9 +426,9 @@ __global__ void __maxnreg__(200)
             mbar_wait(bars.drain, 0, &no_abort, 100000000ull);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // -------------------------------------------------------- softmax
-        const int wg = (warp - 2) >> 2;           // query tile 0 or 1
+        const int wg = (warp - 4) >> 2;           // query tile 0 or 1
         const int wq = warp & 3;                  // TMEM lane quarter (warp % 4)
         const int row_in_tile = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;

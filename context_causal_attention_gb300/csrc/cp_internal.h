@@ -19,8 +19,12 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline size_t dtype_size(cp_dtype d) { return d == CP_BF16 ? 2 : (d == CP_F32 ? 4 : 0); }
 
+// Remembers the most recent CUDA error seen by this host thread (for
+// cp_last_cuda_error) and maps it to a status.
+void note_cuda_error(cudaError_t e);
 inline cp_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return CP_OK;
+    note_cuda_error(e);
     return CP_ERR_CUDA;
 }
 

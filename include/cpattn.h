@@ -66,6 +66,10 @@ const char *cp_status_string(cp_status status);
 /* Library version as "major.minor.patch" (static string). */
 const char *cp_version(void);
 
+/* Text of the most recent CUDA runtime error that made a call of this host
+ * thread return CP_ERR_CUDA ("no error" if none); static string. */
+const char *cp_last_cuda_error(void);
+
 /*
  * cp_zigzag_shard -- split a full sequence into C rank-major shards.
  * [OCP] All-gather: S is cut into 2C chunks of t = S/(2C) tokens and rank r
