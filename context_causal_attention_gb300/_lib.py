@@ -69,6 +69,8 @@ def lib():
     L.cp_ring_attention_fwd_traced.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, i32, vp,
                                                i32, vp, vp, sz, vp, vp, i32]
     L.cp_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, vp]
+    L.cp_ring_attention_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, i32, vp,
+                                                vp]
     for name in header_symbols():
         if name not in ("cp_status_string", "cp_version", "cp_last_cuda_error"):
             getattr(L, name).restype = ctypes.c_int

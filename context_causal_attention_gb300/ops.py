@@ -15,7 +15,8 @@ from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_F32, CP_GLOBAL_ORDER, CP_HEAD_TO_S
 
 __all__ = [
     "cp_zigzag_shard", "cp_zigzag_unshard", "cp_zigzag_positions", "cp_ulysses_relayout", "cp_attn_partial",
-    "cp_lse_merge", "cp_ring_workspace_size", "cp_ring_attention_fwd", "cp_device_status", "cp_version",
+    "cp_lse_merge", "cp_ring_workspace_size", "cp_ring_attention_fwd", "cp_ring_attention_fwd_noalloc",
+    "cp_device_status", "cp_version",
     "CP_BF16", "CP_F32", "CP_ZIGZAG", "CP_CONTIGUOUS", "CP_SEQ_TO_HEAD", "CP_HEAD_TO_SEQ", "CP_RANK_ORDER",
     "CP_GLOBAL_ORDER", "CpError",
 ]
@@ -163,6 +164,23 @@ def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, p
         arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         st = L.cp_ring_attention_fwd_traced(*args, arr, len(events))
         _lib.check("cp_ring_attention_fwd_traced", st)
+    return o, lse
+
+
+def cp_ring_attention_fwd_noalloc(q_sh, k_sh, v_sh, pos, o, lse, scale=None, layout=CP_ZIGZAG, o_dtype=CP_F32,
+                                  stream=None):
+    """Ring forward that allocates nothing: for callers that may not call
+    cudaMalloc (or cannot pass a workspace).  Its scratch is a fixed-size array
+    inside the library (CP_NOALLOC_SCRATCH_BYTES); outputs o and lse must be
+    given.  Calls on one device share that array: do not overlap them."""
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = _lib.lib().cp_ring_attention_fwd_noalloc(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, C * s, N, Nkv,
+                                                  D, C, float(scale), layout, _ptr(o), o_dtype, _ptr(lse),
+                                                  _stream(stream))
+    _lib.check("cp_ring_attention_fwd_noalloc", st)
     return o, lse
 
 

@@ -221,6 +221,39 @@ cp_status cp_ring_attention_fwd_traced(const void *q_sh, const void *k_sh, const
                                        cudaEvent_t const *events, int n_events);
 
 /*
+ * cp_ring_attention_fwd_noalloc -- cp_ring_attention_fwd for callers that
+ * cannot allocate device memory.  The source pages have no counterpart: this
+ * entry point exists for callers that may not call cudaMalloc or cannot hand
+ * the library a workspace -- code running inside a custom allocator's
+ * callbacks, runtimes that forbid allocation after start-up, or processes
+ * whose device memory pool belongs to another framework.
+ *   Same arguments and result as cp_ring_attention_fwd with prefetch = 0
+ *   (zero-copy owner rotation) and no workspace argument; the caller still
+ *   passes all inputs and outputs.
+ *   Scratch: the call uses one file-scope device array of
+ *   CP_NOALLOC_SCRATCH_BYTES bytes inside the library (every GPU on which the
+ *   library is loaded keeps it until the process exits).  Sizes whose
+ *   cp_ring_workspace_size(..., prefetch = 0, o_dtype, ...) exceeds
+ *   CP_NOALLOC_SCRATCH_BYTES are rejected with CP_ERR_WORKSPACE before
+ *   anything is enqueued.  The call never calls cudaMalloc, cudaFree or any
+ *   allocating routine.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make
+ *   that first call before any stream capture on that device.
+ *   Sharing: all calls on a device share the array, which keeps the last
+ *   call's contents (nothing needs clearing: every scratch byte a call reads
+ *   it has written itself).  Calls whose executions overlap on the GPU (for
+ *   instance on two streams) race on the array and give wrong results:
+ *   serialise them.
+ */
+#define CP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+cp_status cp_ring_attention_fwd_noalloc(const void *q_sh, const void *k_sh, const void *v_sh,
+                                        const int32_t *pos, int64_t B, int64_t S, int64_t N,
+                                        int64_t Nkv, int64_t D, int C, float scale, cp_layout layout,
+                                        void *o_sh, cp_dtype o_dtype, float *lse_sh,
+                                        cudaStream_t stream);
+
+/*
  * cp_device_status -- synchronise `stream`, then read (and, if clear != 0,
  * reset) the library's device status word on the current device.
  * *code receives CP_OK, or CP_ERR_DEVICE_TIMEOUT if a kernel of this library
