@@ -10,7 +10,7 @@
 // o = 0, lse = -inf.
 //
 // How: one persistent CTA per SM walks a list of work items (rank, b, h,
-// 256-row query block) ordered longest-first.  Inside a CTA:
+// 256-row query block) ordered longest-first and dealt out boustrophedon.  Inside a CTA:
 //   warp 0      TMA producer: Q block (two 128-row tiles) and a ring of K/V
 //               128-key stages, 128-byte swizzled;
 //   warp 1      TMEM allocator (512 columns: S0 | S1 | O0 | O1) and MMA
@@ -26,14 +26,13 @@
 // Key tiles whose smallest position exceeds the block's largest query
 // position are skipped; tiles whose positions are all <= the tile's
 // smallest query position run unmasked; the rest are masked per element.
-// The running max m is kept an INTEGER in the log2 domain (the ceiling of the
-// tile max) and only moved when the tile max exceeds it by more than 8: O and
-// the sums stay consistent with the stale max, P stays <= 2^8, every rescale
-// is an exact power of two, and the bf16 rounding of P = 2^(x - m) does not
+// The running max m is kept an INTEGER in the log2 domain: the ceiling of the
+// row max of the first key tile the row can see.  Later tiles use it as is and
+// only move it (to the ceiling of their own max) when their P sum would exceed
+// 2^64; O and the sums stay consistent with the stale max, every rescale is an
+// exact power of two, and the bf16 rounding of P = 2^(x - m) does not
 // depend on how the keys are split into partials (so a ring of partials and
-// one monolithic call round P identically).  Two row sums are kept: l over the
-// fp32 P (for lse) and l_b over the bf16 P fed to the tensor core (the output
-// is normalised by l_b, so its weights sum to one exactly).
+// one monolithic call round P identically).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -69,7 +68,8 @@ struct Cfg {
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffTab = kOffV + kStages * kTileBytes;
     static constexpr int kOffOrder = kOffTab + kMaxTables * 8;
-    static constexpr int kOffBar = kOffOrder + kMaxPairs * 4;
+    static constexpr int kOffCost = kOffOrder + kMaxPairs * 4;
+    static constexpr int kOffBar = kOffCost + kMaxPairs * 4;
     // barriers: q_full, q_empty, drain, k_full[S], v_full[S], kv_empty[S],
     //           s_full[2], p_full[2], o_full[2], o_empty[2]
     static constexpr int kNumBars = 3 + 3 * kStages + 8;
@@ -78,6 +78,26 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
+
+// Division by a runtime-invariant divisor 1 <= d < 2^31 for numerators
+// 0 <= n < 2^31 via a multiply-high: q = (n * m) >> (31 + l) with
+// l = ceil(log2 d) and m = ceil(2^(31+l) / d) < 2^32 (round-up method; the
+// error m*d - 2^(31+l) < d keeps the quotient exact for n < 2^31).
+struct FastDiv {
+    uint32_t d, m, sh;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    f.sh = 31 + l;
+    f.m = static_cast<uint32_t>(((1ull << f.sh) + d - 1) / d);
+    return f;
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    return static_cast<uint32_t>((static_cast<uint64_t>(n) * f.m) >> f.sh);
+}
 
 struct AttnArgs {
     const int32_t *q_pos;
@@ -89,6 +109,7 @@ struct AttnArgs {
     int kv_shift, kpos_shift;
     float scale_log2;
     unsigned long long timeout_ns;
+    FastDiv div_bn, div_nqb, div_n;  // by B*N, nqb, N (work-item decoding)
 };
 
 struct Bars {
@@ -121,20 +142,33 @@ struct Item {
 
 __device__ __forceinline__ Item decode_item(int idx, const AttnArgs &a, const int *order, const int2 *qtab) {
     Item it;
-    const int bn = a.B * a.N;
-    const int pr = order[idx / bn];
-    const int bh = idx % bn;
-    it.r = pr / a.nqb;
-    it.qb = pr % a.nqb;
-    it.b = bh / a.N;
-    it.h = bh % a.N;
-    it.owner = (it.r + a.kpos_shift) % a.C;
-    it.kvr = (it.r + a.kv_shift) % a.C;
+    const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bn);
+    const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bn.d;
+    const uint32_t pr = static_cast<uint32_t>(order[pi]);
+    it.r = static_cast<int>(fdiv(pr, a.div_nqb));
+    it.qb = static_cast<int>(pr - static_cast<uint32_t>(it.r) * a.div_nqb.d);
+    it.b = static_cast<int>(fdiv(bh, a.div_n));
+    it.h = static_cast<int>(bh - static_cast<uint32_t>(it.b) * a.div_n.d);
+    it.owner = it.r + a.kpos_shift;
+    if (it.owner >= a.C) it.owner -= a.C;
+    it.kvr = it.r + a.kv_shift;
+    if (it.kvr >= a.C) it.kvr -= a.C;
     const int qt0 = 2 * it.qb, qt1 = 2 * it.qb + 1;
     int qmax = qtab[it.r * a.nqt + qt0].y;
     if (qt1 < a.nqt) qmax = max(qmax, qtab[it.r * a.nqt + qt1].y);
     it.qmax = qmax;
     return it;
+}
+
+// Work item of this CTA in round k of the persistent schedule: items are
+// sorted longest first and dealt out boustrophedon (even rounds CTA 0..G-1,
+// odd rounds G-1..0), so one CTA's long and short items pair up.  Returns -1
+// past the end.
+__device__ __forceinline__ int item_of_round(int k, int n_items) {
+    const int G = gridDim.x;
+    const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x))
+                                                                     : static_cast<int>(blockIdx.x));
+    return idx < n_items ? static_cast<int>(idx) : -1;
 }
 
 // Next key tile >= kt that this block must process (nkt if none).
@@ -144,6 +178,86 @@ __device__ __forceinline__ int next_ktile(int kt, int nkt, const int2 *ktab_owne
         if (sorted) return nkt;
     }
     return nkt;
+}
+
+// This thread's 128 scores of the current key tile from TMEM, with the causal
+// mask applied (scores of keys the row may not see become -inf).  `arith`:
+// the tile's positions are kmin, kmin+1, ...; else positions are read from kpos.
+__device__ __forceinline__ void load_scores(uint32_t tS, bool need_mask, bool arith, int qpos, int kmin, int nvalid,
+                                            const int32_t *kpos, uint32_t (&sa)[64], uint32_t (&sb)[64]) {
+    tmem_ld128(tS, sa, sb);
+    if (!need_mask) return;
+    if (arith) {
+        // column c is visible iff c <= qpos - kmin
+        const long long d = static_cast<long long>(qpos) - kmin;
+        const int lim = d < 0 ? -1 : static_cast<int>(min(d, static_cast<long long>(nvalid - 1)));
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (c > lim) sa[c] = 0xff800000u;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (64 + c > lim) sb[c] = 0xff800000u;
+    } else {
+        // arbitrary positions: compare column by column, 16 loads at a time
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+#pragma unroll
+            for (int c = c0; c < c0 + 16; ++c) {
+                const int kp = (c < nvalid) ? __ldg(kpos + c) : INT_MAX;
+                if (kp > qpos) sa[c] = 0xff800000u;
+            }
+            asm volatile("" ::: "memory");
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+#pragma unroll
+            for (int c = c0; c < c0 + 16; ++c) {
+                const int kp = (64 + c < nvalid) ? __ldg(kpos + 64 + c) : INT_MAX;
+                if (kp > qpos) sb[c] = 0xff800000u;
+            }
+            asm volatile("" ::: "memory");
+        }
+    }
+}
+
+// Row max of the 128 scores of one thread (raw fp32 bits), 8 independent chains.
+__device__ __forceinline__ float row_max128(const uint32_t (&sa)[64], const uint32_t (&sb)[64]) {
+    float mx[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 64; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            mx[u] = fmax3(mx[u], __uint_as_float(sa[c + 2 * u]), __uint_as_float(sa[c + 2 * u + 1]));
+            mx[4 + u] = fmax3(mx[4 + u], __uint_as_float(sb[c + 2 * u]), __uint_as_float(sb[c + 2 * u + 1]));
+        }
+    }
+    return fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+}
+
+// p = 2^(s * sl2 - m) for the 128 scores of one thread, packed to bf16 pairs
+// in pa/pb; returns the sum of the fp32 p in *sum.
+__device__ __forceinline__ void exp_pack128(const uint32_t (&sa)[64], const uint32_t (&sb)[64], float sl2,
+                                            float neg_m, uint32_t (&pa)[32], uint32_t (&pb)[32], float *sum) {
+    const uint64_t sl2x2 = f2_packf(sl2, sl2), nmx2 = f2_packf(neg_m, neg_m);
+    uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(sa[2 * c], sa[2 * c + 1]), sl2x2, nmx2), x0, x1);
+        f2_unpack(f2_fma(f2_pack(sb[2 * c], sb[2 * c + 1]), sl2x2, nmx2), x2, x3);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        const float p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+        sum2[c & 1] = f2_add(sum2[c & 1], f2_packf(p0, p1));
+        sum2[2 + (c & 1)] = f2_add(sum2[2 + (c & 1)], f2_packf(p2, p3));
+        pa[c] = pack_bf16x2(p0, p1);
+        pb[c] = pack_bf16x2(p2, p3);
+    }
+    const uint64_t t = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
+    float lo, hi;
+    f2_unpack(t, lo, hi);
+    *sum = lo + hi;
 }
 
 template <int D>
@@ -159,6 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);  // [C*nkt] K tables, then [C*nqt] Q tables
     int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
+    // per (rank, query block): number of key tiles it processes
+    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
     int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
@@ -249,10 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sorted_flag[tid] = ok;
     }
     __syncthreads();
-    // longest-first order of (rank, query block) pairs; the cost scratch lives
-    // in the K stage buffers, which are not in use yet.
+    // longest-first order of (rank, query block) pairs
     {
-        int *cost = reinterpret_cast<int *>(smem + K::kOffK);
         const int np = a.C * a.nqb;
         for (int p = tid; p < np; p += kThreads) {
             const int r = p / a.nqb, qb = p % a.nqb;
@@ -290,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int n_items = a.C * a.nqb * a.B * a.N;
+    const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     const int hq_per_kv = a.N / a.Nkv;
     uint8_t *sQ = smem + K::kOffQ;
     uint8_t *sK = smem + K::kOffK;
@@ -302,7 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             uint32_t issued_mask = 0, parity_mask = 0;  // per stage: a load was issued / its phase parity
             int q_parity = -1;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            for (int rk = 0; rk < n_rounds && ok; ++rk) {
+                const int idx = item_of_round(rk, n_items);
+                if (idx < 0) continue;
                 const Item itm = decode_item(idx, a, order, qtab);
                 const int2 *kt_o = ktab + itm.owner * a.nkt;
                 const bool srt = sorted_flag[itm.owner];
@@ -356,30 +473,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
             uint32_t kv_it = 0, it = 0;
             bool ok = true;
+            // descriptors of the k-step-0 / key-0 sub-tiles, built once; the MMA
+            // groups add immediate offsets (the issuing warp shares its SM
+            // sub-partition with two busy softmax warps, so it is kept short)
+            const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
+            const uint64_t dq1 = smem_desc_sw128(q_base + K::kTileBytes, 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(k_base, 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(v_base, kAtomBytes, 1024);
+            constexpr uint64_t kStageDesc = K::kTileBytes >> 4;  // one stage in descriptor units
             auto issue_qk = [&](int i, uint32_t st) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-                    const uint64_t da = smem_desc_sw128(q_base + i * K::kTileBytes + off, 16, 1024);
-                    const uint64_t db = smem_desc_sw128(k_base + st * K::kTileBytes + off, 16, 1024);
-                    umma_ss(tmem + i * 128, da, db, kIdescQK, kk > 0 ? 1u : 0u);
-                }
+                umma_qk_group<D / 16>(tmem + i * 128, i ? dq1 : dq0, dk0 + st * kStageDesc, kIdescQK);
             };
             auto issue_pv = [&](int i, uint32_t st, bool acc) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t db = smem_desc_sw128(v_base + st * K::kTileBytes + kk * 2048, kAtomBytes, 1024);
-                    umma_ts(tmem + 256 + i * D, tmem + i * 128 + kk * 8, db, kIdescPV, (acc || kk > 0) ? 1u : 0u);
-                }
+                umma_pv_group(tmem + 256 + i * D, tmem + i * 128, dv0 + st * kStageDesc, kIdescPV, acc ? 1u : 0u);
             };
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            for (int rk = 0; rk < n_rounds && ok; ++rk) {
+                const int idx = item_of_round(rk, n_items);
+                if (idx < 0) continue;
                 const Item itm = decode_item(idx, a, order, qtab);
-                const int2 *kt_o = ktab + itm.owner * a.nkt;
-                const bool srt = sorted_flag[itm.owner];
-                int n = 0;
-                for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
-                     kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt))
-                    ++n;
+                const int n = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
                 if (n == 0) continue;
                 if (!mbar_wait(bars.q_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
@@ -437,7 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = a.scale_log2;
         uint32_t kv_count = 0, it = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        for (int rk = 0; rk < n_rounds && ok; ++rk) {
+            const int idx = item_of_round(rk, n_items);
+            if (idx < 0) continue;
             const Item itm = decode_item(idx, a, order, qtab);
             const int2 *kt_o = ktab + itm.owner * a.nkt;
             const bool srt = sorted_flag[itm.owner];
@@ -450,94 +564,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long orow = static_cast<long long>(itm.r * a.B + itm.b) * a.Sq + row;
             float *o_row = a.o + (orow * a.N + itm.h) * D;
             float *lse_out = a.lse + (static_cast<long long>(itm.r * a.B + itm.b) * a.N + itm.h) * a.Sq + row;
-            float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
+            float m_run = -INFINITY, l_run = 0.f;
             int j = 0;
             for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
                  kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt), ++j) {
                 if (!mbar_wait(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sa[64], sb[64];
-                tmem_ld64(tS, sa);
-                tmem_ld64(tS + 64, sb);
                 const int2 kmm = kt_o[kt];
                 const bool need_mask = (kmm.y > qmin_t) || (kt * 128 + 128 > a.Sk);
-                if (need_mask) {
-                    const int kbase = kt * 128;
-                    const int gk = itm.owner * a.nkt + kt;
-                    const int nvalid = min(128, a.Sk - kbase);
-                    if ((arith_bits[gk >> 5] >> (gk & 31)) & 1u) {
-                        // positions kmin + c: column c is visible iff c <= qpos - kmin
-                        const long long d = static_cast<long long>(qpos) - kmm.x;
-                        const int lim = d < 0 ? -1 : static_cast<int>(min(d, static_cast<long long>(nvalid - 1)));
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c > lim) sa[c] = 0xff800000u;
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (64 + c > lim) sb[c] = 0xff800000u;
-                    } else {
-                        // arbitrary positions: compare column by column, 16 loads at a time
-#pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
-#pragma unroll
-                            for (int c = c0; c < c0 + 16; ++c) {
-                                const int kp = (c < nvalid) ? __ldg(kpos_o + kbase + c) : INT_MAX;
-                                if (kp > qpos) sa[c] = 0xff800000u;
-                            }
-                            asm volatile("" ::: "memory");
-                        }
-#pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
-#pragma unroll
-                            for (int c = c0; c < c0 + 16; ++c) {
-                                const int kp = (64 + c < nvalid) ? __ldg(kpos_o + kbase + 64 + c) : INT_MAX;
-                                if (kp > qpos) sb[c] = 0xff800000u;
-                            }
-                            asm volatile("" ::: "memory");
-                        }
-                    }
+                const int kbase = kt * 128;
+                const int gk = itm.owner * a.nkt + kt;
+                const int nvalid = min(128, a.Sk - kbase);
+                const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
+                load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
+                // The running max is only computed where none is set yet (first visible
+                // tile of the row); later tiles use the stale integer max directly and
+                // move it only if their P would exceed 2^64 (tile sum check below).
+                if (m_run == -INFINITY) {
+                    const float m_tile = row_max128(sa, sb) * sl2;
+                    if (m_tile > -INFINITY) m_run = ceilf(m_tile);
                 }
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    mx0 = fmaxf(mx0, fmaxf(__uint_as_float(sa[c]), __uint_as_float(sa[c + 1])));
-                    mx1 = fmaxf(mx1, fmaxf(__uint_as_float(sb[c]), __uint_as_float(sb[c + 1])));
-                }
-                const float m_tile = fmaxf(mx0, mx1) * sl2;
+                uint32_t pa[32], pb[32];
+                float t_sum;
+                exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
                 float factor = 1.f;
                 bool rescale = false;
-                if (m_tile > m_run + 8.f) {
-                    const float m_new = ceilf(m_tile);
-                    if (j > 0) {
-                        // exact 2^(m_run - m_new): both are integers (m_run may be -inf)
+                const bool big = !(t_sum <= 0x1p64f);  // also true for inf / nan
+                if (__any_sync(0xffffffffu, big)) {
+                    // rare: scores grew by more than 2^64 over the running max; S is still in TMEM
+                    load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
+                    if (big) {
+                        const float m_new = ceilf(row_max128(sa, sb) * sl2);
+                        // exact 2^(m_run - m_new): both are integers
                         const float dk = m_run - m_new;
                         factor = (dk >= -126.f) ? __int_as_float((127 + static_cast<int>(dk)) << 23) : 0.f;
                         rescale = true;
+                        l_run *= factor;
+                        m_run = m_new;
                     }
-                    l_run *= factor;
-                    lb_run *= factor;
-                    m_run = m_new;
+                    // every lane recomputes (unchanged rows reproduce their values)
+                    exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
                 }
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                float sum0 = 0.f, sum1 = 0.f, sb0 = 0.f, sb1 = 0.f;
-                uint32_t pa[32], pb[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sa[2 * c]), sl2, neg_m));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sa[2 * c + 1]), sl2, neg_m));
-                    const float p2 = fast_exp2(fmaf(__uint_as_float(sb[2 * c]), sl2, neg_m));
-                    const float p3 = fast_exp2(fmaf(__uint_as_float(sb[2 * c + 1]), sl2, neg_m));
-                    sum0 += p0 + p1;
-                    sum1 += p2 + p3;
-                    pa[c] = pack_bf16x2(p0, p1);
-                    pb[c] = pack_bf16x2(p2, p3);
-                    sb0 += __uint_as_float(pa[c] << 16) + __uint_as_float(pa[c] & 0xffff0000u);
-                    sb1 += __uint_as_float(pb[c] << 16) + __uint_as_float(pb[c] & 0xffff0000u);
-                }
-                l_run += sum0 + sum1;
-                lb_run += sb0 + sb1;
-                tmem_st32(tS, pa);
-                tmem_st32(tS + 32, pb);
+                l_run += t_sum;
+                tmem_st64(tS, pa, pb);
                 // O is quiescent here (the P V of this tile waits for p_full below)
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -558,27 +628,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j == 0) {
                 // nothing visible for this whole block: o = 0, lse = -inf
                 if (row_valid) {
-                    float4 *o4 = reinterpret_cast<float4 *>(o_row);
 #pragma unroll
-                    for (int c = 0; c < D / 4; ++c) o4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = 0; c < D; c += 8) st_global_v8(o_row + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
                     *lse_out = -INFINITY;
                 }
                 continue;
             }
             if (!mbar_wait(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
             tc_fence_after();
-            const float inv_l = (lb_run > 0.f) ? 1.f / lb_run : 0.f;
+            const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t ov[32];
                 tmem_ld32(tO + c0, ov);
                 if (row_valid) {
-                    float4 *o4 = reinterpret_cast<float4 *>(o_row + c0);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        o4[c] = make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
-                                            __uint_as_float(ov[4 * c + 2]) * inv_l,
-                                            __uint_as_float(ov[4 * c + 3]) * inv_l);
+                    for (int c = 0; c < 32; c += 8)
+                        st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l,
+                                     __uint_as_float(ov[c + 2]) * inv_l, __uint_as_float(ov[c + 3]) * inv_l,
+                                     __uint_as_float(ov[c + 4]) * inv_l, __uint_as_float(ov[c + 5]) * inv_l,
+                                     __uint_as_float(ov[c + 6]) * inv_l, __uint_as_float(ov[c + 7]) * inv_l);
                 }
             }
             if (row_valid) *lse_out = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
@@ -657,6 +726,9 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.kpos_shift = p.kpos_shift;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
     a.timeout_ns = 2000000000ull;
+    a.div_bn = make_fastdiv(static_cast<uint32_t>(a.B * a.N));
+    a.div_nqb = make_fastdiv(static_cast<uint32_t>(a.nqb));
+    a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
     const long long n_items = static_cast<long long>(p.C) * a.nqb * p.B * p.N;
     if (n_items <= 0) return CP_OK;
     static std::once_flag attr_once;
@@ -692,9 +764,11 @@ cp_status validate_attn(const AttnProblem &p) {
     if (p.D != 64 && p.D != 128) return CP_ERR_UNSUPPORTED;
     if (p.N % p.Nkv != 0) return CP_ERR_DIVISIBILITY;
     if (!(std::isfinite(p.scale) && p.scale > 0.f)) return CP_ERR_ARGUMENT;
-    if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.o) || !aligned16(p.q_pos) ||
-        !aligned16(p.k_pos) || !aligned16(p.lse))
+    if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.q_pos) || !aligned16(p.k_pos) ||
+        !aligned16(p.lse))
         return CP_ERR_ALIGNMENT;
+    // the epilogue writes o rows with 32-byte stores
+    if (reinterpret_cast<uintptr_t>(p.o) & 31u) return CP_ERR_ALIGNMENT;
     const int64_t nqt = (p.Sq + 127) / 128, nkt = (p.Sk + 127) / 128;
     if (p.C * (nqt + nkt) > kMaxTables || p.C * ((nqt + 1) / 2) > kMaxPairs) return CP_ERR_SHAPE;
     if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.B * p.N * p.C > INT32_MAX / 4 ||

@@ -142,6 +142,64 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// S = Q K^T for one 128-row tile: D/16 MMAs (K = 16 each) over the 128-byte
+// swizzled K-major tiles whose descriptors for k-step 0 are `a` and `b`; k-step
+// kk starts (kk / 4) * 16 KB + (kk % 4) * 32 B further (descriptor units of
+// 16 B: (kk / 4) * 1024 + (kk % 4) * 2).  The first MMA overwrites D.
+template <int NK>
+__device__ __forceinline__ void umma_qk_group(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+    static_assert(NK == 4 || NK == 8, "head dim 64 or 128");
+    if (NK == 8) {
+        asm volatile(
+            "{\n\t.reg .pred t, f;\n\t.reg .b64 a1, b1;\n\t"
+            "setp.ne.b32 t, %4, 0;\n\tsetp.eq.b32 f, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 1024;\n\tadd.s64 b1, %2, 1024;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 1026;\n\tadd.s64 b1, %2, 1026;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 1028;\n\tadd.s64 b1, %2, 1028;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 1030;\n\tadd.s64 b1, %2, 1030;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(1u)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred t, f;\n\t.reg .b64 a1, b1;\n\t"
+            "setp.ne.b32 t, %4, 0;\n\tsetp.eq.b32 f, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(1u)
+            : "memory");
+    }
+}
+// O (+)= P V for one 128-row tile and 128 keys: 8 MMAs (K = 16 keys each), P
+// read from TMEM starting at column `a_tmem` (8 columns per k-step), V from
+// the MN-major swizzled tile whose descriptor for keys 0..15 is `b` (next 16
+// keys: +2048 B, i.e. +128 in descriptor units).  `acc` = 0 overwrites O with
+// the first product.
+__device__ __forceinline__ void umma_pv_group(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred t, p;\n\t.reg .b64 b1;\n\t.reg .b32 a1;\n\t"
+        "setp.ne.b32 t, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.s64 b1, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 16;\n\tadd.s64 b1, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 24;\n\tadd.s64 b1, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 32;\n\tadd.s64 b1, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 40;\n\tadd.s64 b1, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 48;\n\tadd.s64 b1, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 56;\n\tadd.s64 b1, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
@@ -183,6 +241,42 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         : "r"(taddr), "r"(taddr + 32u)
         : "memory");
 }
+// Four 32-column loads in flight before one wait (128 columns, two arrays).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&a)[64], uint32_t (&b)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : CP_R8(a, 0), CP_R8(a, 8), CP_R8(a, 16), CP_R8(a, 24), CP_R8(a, 32), CP_R8(a, 40), CP_R8(a, 48),
+          CP_R8(a, 56), CP_R8(b, 0), CP_R8(b, 8), CP_R8(b, 16), CP_R8(b, 24), CP_R8(b, 32), CP_R8(b, 40),
+          CP_R8(b, 48), CP_R8(b, 56)
+        : "r"(taddr), "r"(taddr + 32u), "r"(taddr + 64u), "r"(taddr + 96u)
+        : "memory");
+}
+// Store 64 consecutive columns (two arrays of 32) and wait once.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], "
+        "{%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,"
+        "%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(taddr + 32u), CP_W8(a, 0), CP_W8(a, 8), CP_W8(a, 16), CP_W8(a, 24), CP_W8(b, 0), CP_W8(b, 8),
+        CP_W8(b, 16), CP_W8(b, 24)
+        : "memory");
+}
 // Store 32 consecutive 32-bit TMEM columns of this thread's lane and wait.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -192,6 +286,53 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
         CP_W8(r, 0), CP_W8(r, 8), CP_W8(r, 16), CP_W8(r, 24)
         : "memory");
+}
+
+// ---------------------------------------------------------------- packed fp32 math
+// Two fp32 values in one 64-bit register (low word = first).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo_bits, uint32_t hi_bits) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_packf(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// acc + lo(pk) + hi(pk), where pk holds two bf16 values (exact widening adds).
+__device__ __forceinline__ float add_bf16x2(float acc, uint32_t pk) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(pk));
+    return acc;
+}
+
+// 32-byte global store (8 fp32); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float *p, float a, float b, float c, float d, float e, float f, float g,
+                                             float h) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d), "f"(e), "f"(f), "f"(g), "f"(h)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- misc

@@ -138,7 +138,7 @@ cp_status cp_ulysses_relayout(const void *in, void *out, int64_t B, int64_t S, i
  *   q      : device bf16 [B][Sq][N][D]
  *   k, v   : device bf16 [B][Sk][Nkv][D]; query head h reads KV head h/(N/Nkv)
  *   q_pos  : device int32 [Sq];  k_pos : device int32 [Sk] (any values)
- *   o      : device fp32 [B][Sq][N][D], written
+ *   o      : device fp32 [B][Sq][N][D], written; 32-byte aligned
  *   lse    : device fp32 [B][N][Sq], written (natural log)
  * Requires D in {64, 128}, N % Nkv == 0, scale finite and > 0,
  * ceil(Sq/128) + ceil(Sk/128) <= 2048.  Runs on the tensor cores
@@ -189,7 +189,8 @@ cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, i
  *                   block); 1 = the ring exchange is emulated by device
  *                   copies of the next step's K/V on a second stream,
  *                   overlapped with the current step and ordered by events
- *   o_sh          : device [C][B][S/C][N][D] of o_dtype (CP_F32 or CP_BF16)
+ *   o_sh          : device [C][B][S/C][N][D] of o_dtype (CP_F32 or CP_BF16);
+ *                   32-byte aligned when o_dtype is CP_F32
  *   lse_sh        : device fp32 [C][B][N][S/C]
  *   workspace     : device, >= cp_ring_workspace_size(...) bytes, 256-byte
  *                   aligned, caller-owned, contents need not be initialised

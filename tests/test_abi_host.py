@@ -39,6 +39,7 @@ def test_attn_partial_validation(cplib):
     assert _attn(cplib, scale=float("nan")) == 10
     assert _attn(cplib, scale=-1.0) == 10
     assert _attn(cplib, q=MISALIGNED) == 5
+    assert _attn(cplib, o=ctypes.c_void_p(4096 + 16)) == 5  # o needs 32-byte alignment
     assert _attn(cplib, Sq=200000, Sk=200000) == 2  # position tables exceed the on-chip limit
 
 
