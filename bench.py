@@ -137,14 +137,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Largest value of x over all ranks (the slowest replica sets the job time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job throughput: the units all ranks processed over the max-over-ranks time."""
+    return units_per_rank * world / (ms_max * 1e-3)
 
 
 # --------------------------------------------------------------------------
@@ -330,7 +336,7 @@ def run_ours(args, w):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
     flops_step = w.flops
-    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops_step, world, ms_step) / 1e12
 
     # ---- per-kernel numbers from the events
     pairs_t = w.t
@@ -443,6 +449,127 @@ def run_ours(args, w):
     return 0
 
 
+# --------------------------------------------------------------------------
+# sweep: work balance per virtual rank, contiguous vs zigzag
+# --------------------------------------------------------------------------
+def exact_pairs_per_rank(S, C, layout):
+    """Visible (query, key) pairs per rank (per batch and head), closed forms."""
+    s = S // C
+    if layout == "zigzag":
+        t = S // (2 * C)
+        return [(2 * C - 1) * t * t + t * (t + 1)] * C
+    return [r * s * s + s * (s + 1) // 2 for r in range(C)]
+
+
+def run_sweep(args):
+    """One JSON line per sweep workload: ring TFLOP/s, per-rank pairs and per-rank
+    time (each rank's C partials launched on their own, timed with events),
+    merge / shard / unshard / prefetch-copy GB/s."""
+    import torch
+
+    import cp_synth as SY
+    from context_causal_attention_gb300 import build as cuda_build
+    from context_causal_attention_gb300 import ops as F
+
+    cuda_build.build()
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    names = args.sweep_only.split(",") if args.sweep_only else None
+    for w in SY.sweep_workloads():
+        if names and w.name not in names:
+            continue
+        C, S, B, N, D = w.C, w.S, w.B, w.N, w.D
+        s = S // C
+        lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
+        g = torch.Generator("cpu").manual_seed(0)
+        q, k, v = (torch.randn(B, S, N, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(3))
+        qs, ks, vs = (F.cp_zigzag_shard(t, C, lay) for t in (q, k, v))
+        pos = F.cp_zigzag_positions(S, C, lay, device=dev)
+        o = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+        lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, N, D, C, 1, F.CP_F32)), dtype=torch.uint8,
+                         device=dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * C)]
+        for e in ev:
+            e.record()
+
+        def ring(events=None):
+            F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1, workspace=ws, o=o, lse=lse,
+                                    events=events)
+
+        for _ in range(3):
+            ring()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps)
+        e0.record()
+        for _ in range(reps):
+            ring()
+        e1.record()
+        torch.cuda.synchronize()
+        ring_ms = e0.elapsed_time(e1) / reps
+        ring(ev)
+        torch.cuda.synchronize()
+        merge_ms = sum(ev[4 * st + 2].elapsed_time(ev[4 * st + 3]) for st in range(1, C))
+        attn_ms = sum(ev[4 * st].elapsed_time(ev[4 * st + 1]) for st in range(C))
+        # per-rank diagnostic: rank r's C partials launched on their own
+        o1 = torch.empty((B, s, N, D), dtype=torch.float32, device=dev)
+        l1 = torch.empty((B, N, s), dtype=torch.float32, device=dev)
+        rank_ms = []
+        for r in range(C):
+            def partials():
+                for st in range(C):
+                    j = (r - st) % C
+                    F.cp_attn_partial(qs[r], ks[j], vs[j], pos[r], pos[j], o=o1, lse=l1)
+            partials()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            for _ in range(2):
+                partials()
+            a1.record()
+            torch.cuda.synchronize()
+            rank_ms.append(a0.elapsed_time(a1) / 2)
+        # permutations and the prefetch copy (one K rotation = the bytes the ring exchange moves per step)
+        x = torch.empty_like(q)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(5):
+            F.cp_zigzag_shard(q, C, lay, out=qs)
+        t1.record()
+        torch.cuda.synchronize()
+        shard_gbs = 2 * q.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
+        t0.record()
+        for _ in range(5):
+            F.cp_zigzag_unshard(qs, lay, out=x)
+        t1.record()
+        torch.cuda.synchronize()
+        unshard_gbs = 2 * q.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
+        kbuf = torch.empty_like(ks)
+        t0.record()
+        for _ in range(5):
+            kbuf.copy_(ks)
+        t1.record()
+        torch.cuda.synchronize()
+        copy_gbs = 2 * ks.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
+        pairs = exact_pairs_per_rank(S, C, w.layout)
+        flops = 4.0 * B * N * D * S * (S + 1) / 2
+        rows = C * B * N * s
+        line = {
+            "sweep": w.name, "S": S, "C": C, "layout": w.layout,
+            "ring_ms": ring_ms, "ring_tflops": flops / (ring_ms * 1e-3) / 1e12,
+            "attn_ms_in_ring": attn_ms, "merge_ms_in_ring": merge_ms,
+            "pairs_per_rank": pairs, "pairs_max_over_mean": max(pairs) / (sum(pairs) / C),
+            "rank_ms": rank_ms, "rank_ms_max_over_mean": max(rank_ms) / (sum(rank_ms) / C),
+            "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "kv_rotation_copy_gbs": copy_gbs,
+            "hbm_peak_gbs": peaks["hbm_gbs"],
+            "merge_rows_per_step": rows,
+        }
+        print(json.dumps(line), flush=True)
+        del q, k, v, qs, ks, vs, o, lse, ws, x, kbuf, o1, l1
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,7 +580,11 @@ def main():
     ap.add_argument("--no-prefetch", dest="prefetch", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sweep", action="store_true", help="run the contiguous-vs-zigzag sweep instead")
+    ap.add_argument("--sweep-only", default="", help="comma-separated sweep workload names")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
     import cp_synth as SY
     w = SY.WORKLOADS.get(args.workload)
     if w is None:

@@ -70,9 +70,9 @@ struct Cfg {
     static constexpr int kOffOrder = kOffTab + kMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kMaxPairs * 4;
     static constexpr int kOffBar = kOffCost + kMaxPairs * 4;
-    // barriers: q_full, q_empty, drain, k_full[S], v_full[S], kv_empty[S],
+    // barriers: q_full, q_empty, drain, k_full[S], v_full[S], k_empty[S], v_empty[S],
     //           s_full[2], p_full[2], o_full[2], o_empty[2]
-    static constexpr int kNumBars = 3 + 3 * kStages + 8;
+    static constexpr int kNumBars = 3 + 4 * kStages + 8;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMiscBytes = 16 + kMaxC * 4 + kMaxTables / 8;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
@@ -113,7 +113,7 @@ struct AttnArgs {
 };
 
 struct Bars {
-    uint64_t *q_full, *q_empty, *drain, *k_full, *v_full, *kv_empty, *s_full, *p_full, *o_full, *o_empty;
+    uint64_t *q_full, *q_empty, *drain, *k_full, *v_full, *k_empty, *v_empty, *s_full, *p_full, *o_full, *o_empty;
 };
 
 template <int D>
@@ -126,8 +126,9 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
     r.drain = b + 2;
     r.k_full = b + 3;
     r.v_full = b + 3 + K::kStages;
-    r.kv_empty = b + 3 + 2 * K::kStages;
-    r.s_full = b + 3 + 3 * K::kStages;
+    r.k_empty = b + 3 + 2 * K::kStages;
+    r.v_empty = b + 3 + 3 * K::kStages;
+    r.s_full = b + 3 + 4 * K::kStages;
     r.p_full = r.s_full + 2;
     r.o_full = r.s_full + 4;
     r.o_empty = r.s_full + 6;
@@ -294,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < K::kStages; ++s) {
             mbar_init(bars.k_full + s, 1);
             mbar_init(bars.v_full + s, 1);
-            mbar_init(bars.kv_empty + s, 1);
+            mbar_init(bars.k_empty + s, 1);
+            mbar_init(bars.v_empty + s, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.s_full + i, 1);
@@ -413,10 +415,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // -------------------------------------------------------- TMA producer
         if (lane == 0) {
-            uint32_t kv_it = 0, it = 0;
+            // K runs one tile ahead of V: a K stage is freed after the second
+            // tile's Q K^T, a V stage only after the second tile's P V.
+            uint32_t k_it = 0, v_it = 0, it = 0;
             bool ok = true;
-            uint32_t issued_mask = 0, parity_mask = 0;  // per stage: a load was issued / its phase parity
+            uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;  // per stage: issued / phase parity
             int q_parity = -1;
+            bool pend = false;  // a V tile waits to be issued
+            int pend_kt = 0, pend_hk = 0, pend_row = 0;
+            auto issue_v = [&]() -> bool {
+                const uint32_t st = v_it % K::kStages, ph = (v_it / K::kStages) & 1u;
+                if (!mbar_wait(bars.v_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) return false;
+                mbar_arrive_expect_tx(bars.v_full + st, K::kTileBytes);
+                for (int at = 0; at < K::kAtoms; ++at)
+                    tma_load_4d(sV + st * K::kTileBytes + at * kAtomBytes, &tmV, bars.v_full + st, 64 * at, pend_hk,
+                                pend_kt * 128, pend_row);
+                v_issued |= 1u << st;
+                v_par = (v_par & ~(1u << st)) | (ph << st);
+                ++v_it;
+                pend = false;
+                return true;
+            };
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
@@ -425,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool srt = sorted_flag[itm.owner];
                 int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt);
                 if (kt >= a.nkt) continue;
+                if (pend && !issue_v()) { ok = false; break; }  // last V of the previous item
                 if (!mbar_wait(bars.q_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 mbar_arrive_expect_tx(bars.q_full, 2 * K::kTileBytes);
                 q_parity = it & 1u;
@@ -437,31 +457,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int hk = itm.h / hq_per_kv;
                 const int kvrow = itm.kvr * a.B + itm.b;
                 for (; kt < a.nkt; kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt)) {
-                    const uint32_t st = kv_it % K::kStages, ph = (kv_it / K::kStages) & 1u;
-                    if (!mbar_wait(bars.kv_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    const uint32_t st = k_it % K::kStages, ph = (k_it / K::kStages) & 1u;
+                    if (!mbar_wait(bars.k_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                     mbar_arrive_expect_tx(bars.k_full + st, K::kTileBytes);
                     for (int at = 0; at < K::kAtoms; ++at)
                         tma_load_4d(sK + st * K::kTileBytes + at * kAtomBytes, &tmK, bars.k_full + st, 64 * at, hk,
                                     kt * 128, kvrow);
-                    mbar_arrive_expect_tx(bars.v_full + st, K::kTileBytes);
-                    for (int at = 0; at < K::kAtoms; ++at)
-                        tma_load_4d(sV + st * K::kTileBytes + at * kAtomBytes, &tmV, bars.v_full + st, 64 * at, hk,
-                                    kt * 128, kvrow);
-                    issued_mask |= 1u << st;
-                    parity_mask = (parity_mask & ~(1u << st)) | (ph << st);
-                    ++kv_it;
+                    k_issued |= 1u << st;
+                    k_par = (k_par & ~(1u << st)) | (ph << st);
+                    ++k_it;
+                    if (pend && !issue_v()) { ok = false; break; }
+                    pend = true;
+                    pend_kt = kt;
+                    pend_hk = hk;
+                    pend_row = kvrow;
                 }
             }
+            if (ok && pend && !issue_v()) ok = false;
             if (!ok) {
                 // let every copy already issued land before shared memory goes away
                 volatile int no_abort = 0;
                 const unsigned long long drain_ns = 100000000ull;
                 if (q_parity >= 0) mbar_wait(bars.q_full, q_parity, &no_abort, drain_ns);
-                for (int s = 0; s < K::kStages; ++s)
-                    if ((issued_mask >> s) & 1u) {
-                        mbar_wait(bars.k_full + s, (parity_mask >> s) & 1u, &no_abort, drain_ns);
-                        mbar_wait(bars.v_full + s, (parity_mask >> s) & 1u, &no_abort, drain_ns);
-                    }
+                for (int st = 0; st < K::kStages; ++st) {
+                    if ((k_issued >> st) & 1u) mbar_wait(bars.k_full + st, (k_par >> st) & 1u, &no_abort, drain_ns);
+                    if ((v_issued >> st) & 1u) mbar_wait(bars.v_full + st, (v_par >> st) & 1u, &no_abort, drain_ns);
+                }
             }
         }
         __syncwarp();
@@ -508,11 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
                             tc_fence_after();
                             issue_pv(i, prev_st, j > 1);
-                            if (i == 1) umma_commit(bars.kv_empty + prev_st);
+                            if (i == 1) umma_commit(bars.v_empty + prev_st);
                         }
                         issue_qk(i, st);
                         umma_commit(bars.s_full + i);
                     }
+                    if (ok) umma_commit(bars.k_empty + st);  // both tiles' Q K^T read this K stage
                     if (!ok) break;
                     if (j == n - 1) umma_commit(bars.q_empty);
                     prev_st = st;
@@ -527,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
                     issue_pv(i, prev_st, n > 1);
-                    if (i == 1) umma_commit(bars.kv_empty + prev_st);
+                    if (i == 1) umma_commit(bars.v_empty + prev_st);
                     umma_commit(bars.o_full + i);
                 }
                 ++it;

@@ -1,0 +1,62 @@
+"""Host-side logic of bench.py (no GPU): closed-form work counts against the
+oracle, and the multi-process aggregation (barrier + max over ranks) on a
+world_size-2 gloo group."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import oracle as O
+
+
+@pytest.mark.parametrize("S,C", [(64, 2), (128, 4), (256, 8), (96, 3)])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+def test_exact_pairs_closed_form_matches_oracle(S, C, layout):
+    if layout == "zigzag" and S % (2 * C):
+        pytest.skip("zigzag needs S % 2C == 0")
+    pos = O.positions(S, C, O.ZIGZAG if layout == "zigzag" else O.CONTIGUOUS)
+    want = O.pair_counts(pos).sum(axis=1).tolist()
+    assert bench.exact_pairs_per_rank(S, C, layout) == want
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        ms = [3.0, 5.0][rank]                      # rank 1 is the slow replica
+        m = bench.max_over_ranks(ms, world, device="cpu")
+        value = bench.job_throughput(1e9, world, m)
+        out[rank] = (m, value)
+        bench.barrier(world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    for r in range(world):
+        m, value = out[r]
+        assert m == 5.0                              # max over ranks
+        assert value == pytest.approx(2e9 / 5e-3)    # units of all ranks over the slowest time
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(7.0, 1) == 7.0
+    assert bench.job_throughput(10.0, 1, 1000.0) == pytest.approx(10.0)
