@@ -21,7 +21,7 @@
 //               thread per query row, online softmax in the log2 domain
 //               ("Context Parallelism & Ring Attention", "Softmax is
 //               decomposable": running max, running sum, rescaled output),
-//               P written back to TMEM over S as packed bf16, epilogue
+//               P written back to TMEM over S columns 64..127 as packed bf16, epilogue
 //               o = O / l and lse = (m + log2 l) ln 2.
 // Key tiles whose smallest position exceeds the block's largest query
 // position are skipped; tiles whose positions are all <= the tile's
@@ -219,6 +219,51 @@ __device__ __forceinline__ void load_scores(uint32_t tS, bool need_mask, bool ar
             asm volatile("" ::: "memory");
         }
     }
+}
+
+// Causal mask of one 64-column half (columns c0 .. c0+63 of the key tile).
+__device__ __forceinline__ void mask_half(bool arith, int qpos, int kmin, int nvalid, const int32_t *kpos, int c0,
+                                          uint32_t (&h)[64]) {
+    if (arith) {
+        const long long d = static_cast<long long>(qpos) - kmin;
+        const int lim = d < 0 ? -1 : static_cast<int>(min(d, static_cast<long long>(nvalid - 1)));
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (c0 + c > lim) h[c] = 0xff800000u;
+    } else {
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 16) {
+#pragma unroll
+            for (int c = cc; c < cc + 16; ++c) {
+                const int kp = (c0 + c < nvalid) ? __ldg(kpos + c0 + c) : INT_MAX;
+                if (kp > qpos) h[c] = 0xff800000u;
+            }
+            asm volatile("" ::: "memory");
+        }
+    }
+}
+
+// p = 2^(s * sl2 - m) for 64 scores, packed to 32 bf16 pairs; returns the
+// fp32 sum of p.
+__device__ __forceinline__ float exp_pack64(const uint32_t (&h)[64], float sl2, float neg_m, uint32_t (&pk)[32]) {
+    const uint64_t sl2x2 = f2_packf(sl2, sl2), nmx2 = f2_packf(neg_m, neg_m);
+    uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(h[2 * c], h[2 * c + 1]), sl2x2, nmx2), x0, x1);
+        f2_unpack(f2_fma(f2_pack(h[2 * c + 2], h[2 * c + 3]), sl2x2, nmx2), x2, x3);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        const float p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+        sum2[(c >> 1) & 1] = f2_add(sum2[(c >> 1) & 1], f2_packf(p0, p1));
+        sum2[2 + ((c >> 1) & 1)] = f2_add(sum2[2 + ((c >> 1) & 1)], f2_packf(p2, p3));
+        pk[c] = pack_bf16x2(p0, p1);
+        pk[c + 1] = pack_bf16x2(p2, p3);
+    }
+    const uint64_t t = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
+    float lo, hi;
+    f2_unpack(t, lo, hi);
+    return lo + hi;
 }
 
 // Row max of the 128 scores of one thread (raw fp32 bits), 8 independent chains.
@@ -506,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_qk_group<D / 16>(tmem + i * 128, i ? dq1 : dq0, dk0 + st * kStageDesc, kIdescQK);
             };
             auto issue_pv = [&](int i, uint32_t st, bool acc) {
-                umma_pv_group(tmem + 256 + i * D, tmem + i * 128, dv0 + st * kStageDesc, kIdescPV, acc ? 1u : 0u);
+                umma_pv_group(tmem + 256 + i * D, tmem + i * 128 + 64, dv0 + st * kStageDesc, kIdescPV,
+                              acc ? 1u : 0u);
             };
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
@@ -599,23 +645,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int gk = itm.owner * a.nkt + kt;
                 const int nvalid = min(128, a.Sk - kbase);
                 const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
-                load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
-                // The running max is only computed where none is set yet (first visible
-                // tile of the row); later tiles use the stale integer max directly and
-                // move it only if their P would exceed 2^64 (tile sum check below).
-                if (m_run == -INFINITY) {
-                    const float m_tile = row_max128(sa, sb) * sl2;
-                    if (m_tile > -INFINITY) m_run = ceilf(m_tile);
-                }
+                // P (bf16 pairs) goes to columns 64..127 of the S region, so S
+                // columns 0..63 stay readable until this tile's P V is issued.
                 uint32_t pa[32], pb[32];
                 float t_sum;
-                exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
+                bool stored = false;
+                // TMEM loads/stores are warp-collective: the path must be warp-uniform
+                if (__all_sync(0xffffffffu, m_run != -INFINITY)) {
+                    // Steady state (max already set): pipeline the tile in two halves --
+                    // the second half's TMEM load and the first half's P store overlap
+                    // exp work.
+                    tmem_ld64_nowait(tS, sa);
+                    tmem_wait_ld(sa);
+                    tmem_ld64_nowait(tS + 64, sb);
+                    if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
+                    const float s0 = exp_pack64(sa, sl2, -m_run, pa);
+                    tmem_wait_ld(sb);  // columns 64..127 read: P may overwrite them
+                    tmem_st32_nowait(tS + 64, pa);
+                    if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 64, sb);
+                    const float s1 = exp_pack64(sb, sl2, -m_run, pb);
+                    tmem_st32_nowait(tS + 96, pb);
+                    t_sum = s0 + s1;
+                    stored = true;
+                } else {
+                    load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
+                    // rows without a running max yet (first visible tile): set it
+                    if (m_run == -INFINITY) {
+                        const float m_tile = row_max128(sa, sb) * sl2;
+                        if (m_tile > -INFINITY) m_run = ceilf(m_tile);
+                    }
+                    exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
+                }
                 float factor = 1.f;
                 bool rescale = false;
                 const bool big = !(t_sum <= 0x1p64f);  // also true for inf / nan
                 if (__any_sync(0xffffffffu, big)) {
-                    // rare: scores grew by more than 2^64 over the running max; S is still in TMEM
-                    load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
+                    // rare: scores grew by more than 2^64 over the running max.  Columns
+                    // 0..63 of S are still in TMEM; columns 64..127 are still in sb.
+                    if (stored) tmem_wait_st();
+                    tmem_ld64(tS, sa);
+                    if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
                     if (big) {
                         const float m_new = ceilf(row_max128(sa, sb) * sl2);
                         // exact 2^(m_run - m_new): both are integers
@@ -627,9 +696,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // every lane recomputes (unchanged rows reproduce their values)
                     exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
+                    stored = false;
                 }
                 l_run += t_sum;
-                tmem_st64(tS, pa, pb);
+                if (stored) {
+                    tmem_wait_st();
+                } else {
+                    tmem_st64(tS + 64, pa, pb);
+                }
                 // O is quiescent here (the P V of this tile waits for p_full below)
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll

@@ -277,6 +277,42 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&a)[32
         CP_W8(b, 16), CP_W8(b, 24)
         : "memory");
 }
+// Issue a 64-column load (two x32 shapes) WITHOUT waiting; the registers must
+// not be read before tmem_wait_ld(r) on the same array.
+__device__ __forceinline__ void tmem_ld64_nowait(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];"
+        : CP_R8(r, 0), CP_R8(r, 8), CP_R8(r, 16), CP_R8(r, 24), CP_R8(r, 32), CP_R8(r, 40), CP_R8(r, 48),
+          CP_R8(r, 56)
+        : "r"(taddr), "r"(taddr + 32u)
+        : "memory");
+}
+#define CP_RW8(a, i) "+r"(a[i]), "+r"(a[i + 1]), "+r"(a[i + 2]), "+r"(a[i + 3]), "+r"(a[i + 4]), "+r"(a[i + 5]), \
+                     "+r"(a[i + 6]), "+r"(a[i + 7])
+// Wait for every outstanding tcgen05.ld of this thread; the registers of `r`
+// are declared as produced here, so the compiler cannot read them earlier.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[64]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : CP_RW8(r, 0), CP_RW8(r, 8), CP_RW8(r, 16), CP_RW8(r, 24), CP_RW8(r, 32), CP_RW8(r, 40),
+                   CP_RW8(r, 48), CP_RW8(r, 56)
+                 :
+                 : "memory");
+}
+// Issue a 32-column store without waiting (tmem_wait_st completes it).
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        CP_W8(r, 0), CP_W8(r, 8), CP_W8(r, 16), CP_W8(r, 24)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Store 32 consecutive 32-bit TMEM columns of this thread's lane and wait.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
