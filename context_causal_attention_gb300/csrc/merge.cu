@@ -3,11 +3,10 @@
 // lse = logaddexp(lse_acc, lse_tile); o = e^{lse_acc - lse} o_acc +
 // e^{lse_tile - lse} o_tile), plus the fp32 -> bf16 output conversion.
 //
-// Bandwidth kernel: D/4 threads own one row (b, i, h) of D fp32 values and
-// move it with 16-byte vectors; both lse values of the row are read once per
-// warp (broadcast).  Rows whose tile lse is -inf (a causal partial that saw
-// nothing) cost one 4-byte read and are otherwise skipped; rows whose
-// accumulator lse is -inf take the tile without reading the accumulator.
+// Bandwidth kernel with 16-byte vectors.  Rows whose tile lse is -inf (a
+// causal partial that saw nothing) cost one 4-byte read and are otherwise
+// skipped; rows whose accumulator lse is -inf take the tile (weight 0 on the
+// accumulator).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -19,39 +18,83 @@
 namespace cpattn {
 namespace {
 
-__global__ void __launch_bounds__(256) lse_merge_kernel(float *__restrict__ o_acc, float *__restrict__ lse_acc,
+// One warp merges 32 consecutive query rows i0..i0+31 of one (b, h): the two
+// lse vectors of those rows arrive in one coalesced load each, a ballot keeps
+// the rows whose tile saw anything, and those rows are merged four at a time
+// with all their o loads in flight before any is used.  Lane k computes the
+// merged lse of row i0+k and its two weights; every lane then blends one or
+// more 16-byte pieces of each row's D values.
+__global__ void __launch_bounds__(256, 4) lse_merge_kernel(float *__restrict__ o_acc, float *__restrict__ lse_acc,
                                                         const float *__restrict__ o_t,
-                                                        const float *__restrict__ lse_t, long long rows,
-                                                        long long Sq, int N, int tpr_shift, int D) {
-    const int tpr = 1 << tpr_shift;  // threads per row = D / 4
-    const long long gthreads = static_cast<long long>(gridDim.x) * blockDim.x;
-    const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int sub = static_cast<int>(gid & (tpr - 1));
-    for (long long row = gid >> tpr_shift; row < rows; row += gthreads >> tpr_shift) {
-        // row = (b * Sq + i) * N + h
-        const long long bi = row / N;
-        const int h = static_cast<int>(row - bi * N);
-        const long long b = bi / Sq, i = bi - b * Sq;
-        const long long li = (b * N + h) * Sq + i;
-        const float lt = __ldg(lse_t + li);
-        if (lt == -INFINITY) continue;
-        const float la = lse_acc[li];
-        float4 *oa = reinterpret_cast<float4 *>(o_acc + row * D);
-        const float4 *ot = reinterpret_cast<const float4 *>(o_t + row * D);
-        if (la == -INFINITY) {
-            for (int c = sub; c < D / 4; c += tpr) oa[c] = __ldg(ot + c);
-            if (sub == 0) lse_acc[li] = lt;
-            continue;
+                                                        const float *__restrict__ lse_t, long long B,
+                                                        long long Sq, int N, int D) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long nib = (Sq + 31) >> 5;  // 32-row blocks per (b, h)
+    const long long units = B * N * nib;
+    const int nvec = D >> 2;                // float4 per row
+    for (long long u = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
+         u += warps) {
+        const long long bh = u / nib;
+        const long long i0 = (u - bh * nib) << 5;
+        const long long b = bh / N;
+        const int h = static_cast<int>(bh - b * N);
+        const long long i = i0 + lane;
+        const bool valid = i < Sq;
+        const long long li = bh * Sq + i;  // lse index (b*N + h)*Sq + i
+        const float lt = valid ? __ldg(lse_t + li) : -INFINITY;
+        const float la = valid ? lse_acc[li] : -INFINITY;
+        // merged lse and weights of this lane's row
+        float lse = la, wa = 1.f, wt = 0.f;
+        if (lt != -INFINITY) {
+            if (la == -INFINITY) {
+                lse = lt;
+                wa = 0.f;
+                wt = 1.f;
+            } else {
+                const float mx = fmaxf(la, lt), mn = fminf(la, lt);
+                lse = mx + log1pf(expf(mn - mx));
+                wa = expf(la - lse);
+                wt = expf(lt - lse);
+            }
         }
-        const float mx = fmaxf(la, lt), mn = fminf(la, lt);
-        const float lse = mx + log1pf(expf(mn - mx));
-        const float wa = expf(la - lse), wt = expf(lt - lse);
-        for (int c = sub; c < D / 4; c += tpr) {
-            const float4 x = oa[c];
-            const float4 y = __ldg(ot + c);
-            oa[c] = make_float4(wa * x.x + wt * y.x, wa * x.y + wt * y.y, wa * x.z + wt * y.z, wa * x.w + wt * y.w);
+        unsigned todo = __ballot_sync(0xffffffffu, lt != -INFINITY);
+        const long long row0 = (b * Sq + i0) * N + h;  // o row of i0; row of i0+k is row0 + k*N
+        while (todo) {
+            // next (up to) four rows of this block with a non-empty tile
+            int ks[4];
+            float wsa[4], wst[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ks[q] = todo ? __ffs(todo) - 1 : -1;
+                todo &= todo - 1;  // no-op once empty
+                // weights of that row, from its lane (all lanes take part)
+                wsa[q] = __shfl_sync(0xffffffffu, wa, ks[q] < 0 ? 0 : ks[q]);
+                wst[q] = __shfl_sync(0xffffffffu, wt, ks[q] < 0 ? 0 : ks[q]);
+            }
+            for (int c = lane; c < nvec; c += 32) {
+                float4 xa[4], xt[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (ks[q] >= 0) {
+                        const long long off = (row0 + static_cast<long long>(ks[q]) * N) * D;
+                        xa[q] = reinterpret_cast<const float4 *>(o_acc + off)[c];
+                        xt[q] = __ldg(reinterpret_cast<const float4 *>(o_t + off) + c);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (ks[q] >= 0) {
+                        const float a = wsa[q], t = wst[q];
+                        const long long off = (row0 + static_cast<long long>(ks[q]) * N) * D;
+                        reinterpret_cast<float4 *>(o_acc + off)[c] =
+                            make_float4(a * xa[q].x + t * xt[q].x, a * xa[q].y + t * xt[q].y,
+                                        a * xa[q].z + t * xt[q].z, a * xa[q].w + t * xt[q].w);
+                    }
+                }
+            }
         }
-        if (sub == 0) lse_acc[li] = lse;
+        if (valid && lt != -INFINITY) lse_acc[li] = lse;
     }
 }
 
@@ -71,12 +114,6 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4 *__restri
     }
 }
 
-int ilog2_pow2(long long v) {
-    if (v <= 0 || (v & (v - 1))) return -1;
-    int s = 0;
-    while ((1LL << s) < v) ++s;
-    return s;
-}
 
 }  // namespace
 
@@ -87,21 +124,13 @@ cp_status launch_merge(float *o_acc, float *lse_acc, const float *o_tile, const 
     if (D % 4 != 0 || !aligned16(o_acc) || !aligned16(o_tile)) return CP_ERR_ALIGNMENT;
     if ((reinterpret_cast<uintptr_t>(lse_acc) & 3u) || (reinterpret_cast<uintptr_t>(lse_tile) & 3u))
         return CP_ERR_ALIGNMENT;
-    long long tpr = D / 4;
-    if (tpr > 32) tpr = 32;
-    int shift = ilog2_pow2(tpr);
-    while (shift < 0) {  // largest power of two <= D/4
-        --tpr;
-        shift = ilog2_pow2(tpr);
-    }
-    const long long rows = B * Sq * N;
-    long long blocks = (rows * tpr + 255) / 256;
+    const long long units = B * N * ((Sq + 31) / 32);
+    long long blocks = (units + 7) / 8;  // 8 warps per block
     const long long cap = static_cast<long long>(sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    lse_merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_acc, lse_acc, o_tile, lse_tile, rows, Sq,
-                                                                       static_cast<int>(N), shift,
-                                                                       static_cast<int>(D));
+    lse_merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_acc, lse_acc, o_tile, lse_tile, B, Sq,
+                                                                       static_cast<int>(N), static_cast<int>(D));
     return last_launch_status();
 }
 
