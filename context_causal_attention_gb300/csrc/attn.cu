@@ -107,6 +107,8 @@ struct AttnArgs {
     int C, B, N, Nkv, Sq, Sk;
     int nqt, nkt, nqb;
     int kv_shift, kpos_shift;
+    int kv_shared;  // all ranks read the same K/V (rank index 0)
+    int kpr;        // key-position ranks with tables: 1 if shared, else C
     float scale_log2;
     unsigned long long timeout_ns;
     FastDiv div_bn, div_nqb, div_n;  // by B*N, nqb, N (work-item decoding)
@@ -152,8 +154,10 @@ __device__ __forceinline__ Item decode_item(int idx, const AttnArgs &a, const in
     it.h = static_cast<int>(bh - static_cast<uint32_t>(it.b) * a.div_n.d);
     it.owner = it.r + a.kpos_shift;
     if (it.owner >= a.C) it.owner -= a.C;
+    if (a.kpr == 1) it.owner = 0;
     it.kvr = it.r + a.kv_shift;
     if (it.kvr >= a.C) it.kvr -= a.C;
+    if (a.kv_shared) it.kvr = 0;
     const int qt0 = 2 * it.qb, qt1 = 2 * it.qb + 1;
     int qmax = qtab[it.r * a.nqt + qt0].y;
     if (qt1 < a.nqt) qmax = max(qmax, qtab[it.r * a.nqt + qt1].y);
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);
     const Bars bars = bars_at<D>(smem);
     const int2 *ktab = tab;
-    const int2 *qtab = tab + a.C * a.nkt;
+    const int2 *qtab = tab + a.kpr * a.nkt;
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
@@ -363,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // position tables: (min, max) of every 128-row tile, K tiles per owner rank
     // first, then Q tiles per rank.
     {
-        const int nk = a.C * a.nkt, total = nk + a.C * a.nqt;
+        const int nk = a.kpr * a.nkt, total = nk + a.C * a.nqt;
         for (int g = warp; g < total; g += kThreads / 32) {
             const int32_t *p;
             int rows0, lim;
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    if (tid < a.C) {
+    if (tid < a.kpr) {
         int ok = 1;
         for (int kt = 1; kt < a.nkt; ++kt) ok &= (ktab[tid * a.nkt + kt].x >= ktab[tid * a.nkt + kt - 1].x);
         sorted_flag[tid] = ok;
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int np = a.C * a.nqb;
         for (int p = tid; p < np; p += kThreads) {
             const int r = p / a.nqb, qb = p % a.nqb;
-            const int owner = (r + a.kpos_shift) % a.C;
+            const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
             int qmax = qtab[r * a.nqt + 2 * qb].y;
             if (2 * qb + 1 < a.nqt) qmax = max(qmax, qtab[r * a.nqt + 2 * qb + 1].y);
             const int2 *kt_o = ktab + owner * a.nkt;
@@ -799,8 +803,9 @@ template <int D>
 cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     using K = Cfg<D>;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, D, p.N, p.Sq, p.C * p.B) || !make_map(&mk, p.k, D, p.Nkv, p.Sk, p.C * p.B) ||
-        !make_map(&mv, p.v, D, p.Nkv, p.Sk, p.C * p.B))
+    const int64_t kv_outer = p.kv_shared ? p.B : p.C * p.B;
+    if (!make_map(&mq, p.q, D, p.N, p.Sq, p.C * p.B) || !make_map(&mk, p.k, D, p.Nkv, p.Sk, kv_outer) ||
+        !make_map(&mv, p.v, D, p.Nkv, p.Sk, kv_outer))
         return CP_ERR_CUDA;
     AttnArgs a;
     a.q_pos = p.q_pos;
@@ -819,6 +824,8 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.nkt = static_cast<int>((p.Sk + 127) / 128);
     a.nqb = (a.nqt + 1) / 2;
     a.kv_shift = p.kv_shift;
+    a.kv_shared = p.kv_shared ? 1 : 0;
+    a.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
     a.kpos_shift = p.kpos_shift;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
     a.timeout_ns = 2000000000ull;
@@ -866,7 +873,8 @@ cp_status validate_attn(const AttnProblem &p) {
     // the epilogue writes o rows with 32-byte stores
     if (reinterpret_cast<uintptr_t>(p.o) & 31u) return CP_ERR_ALIGNMENT;
     const int64_t nqt = (p.Sq + 127) / 128, nkt = (p.Sk + 127) / 128;
-    if (p.C * (nqt + nkt) > kMaxTables || p.C * ((nqt + 1) / 2) > kMaxPairs) return CP_ERR_SHAPE;
+    const int64_t kpr = (p.k_pos_stride == 0) ? 1 : p.C;
+    if (kpr * nkt + p.C * nqt > kMaxTables || p.C * ((nqt + 1) / 2) > kMaxPairs) return CP_ERR_SHAPE;
     if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.B * p.N * p.C > INT32_MAX / 4 ||
         static_cast<int64_t>(p.C) * ((nqt + 1) / 2) * p.B * p.N > INT32_MAX)
         return CP_ERR_SHAPE;

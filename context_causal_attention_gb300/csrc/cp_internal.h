@@ -36,8 +36,11 @@ int sm_count();
 
 // One batched attention launch over C "rank" problems.  Rank r reads its
 // queries from q[r] (rank stride C-major: [C][B][Sq][N][D]), its K/V from rank
-// (r + kv_shift) mod C of k/v, its query positions from q_pos + r*q_pos_stride
-// and its key positions from k_pos + ((r + kpos_shift) mod C)*k_pos_stride.
+// (r + kv_shift) mod C of k/v ([C][B][Sk][Nkv][D]) -- or, with kv_shared, from
+// the one K/V tensor [B][Sk][Nkv][D] all ranks share -- its query positions
+// from q_pos + r*q_pos_stride and its key positions from
+// k_pos + ((r + kpos_shift) mod C)*k_pos_stride (k_pos_stride 0: one shared
+// key-position array).
 struct AttnProblem {
     const void *q, *k, *v;
     const int32_t *q_pos, *k_pos;
@@ -46,6 +49,7 @@ struct AttnProblem {
     int C;
     int64_t B, N, Nkv, D, Sq, Sk;
     int kv_shift, kpos_shift;
+    bool kv_shared;
     float scale;
 };
 

@@ -1,0 +1,176 @@
+// strategies.cu -- the all-gather and the all-to-all (Ulysses) forms of
+// context-parallel causal attention, for C virtual ranks on one GPU, built
+// from the library's own kernels.
+//
+// All-gather ("On Context Parallelism", All-gather / Forward): every rank
+// keeps its local queries; K and V are gathered from all ranks and put back in
+// global order (here: cp_zigzag_unshard of the resident shards), and each
+// rank's queries attend to the full sequence with their own global positions
+// against positions 0..S-1.  All C ranks run in one launch sharing the
+// gathered K/V.
+//
+// All-to-all ("On Context Parallelism", All-to-all; "Context parallelism:
+// Ring Attention and Ulysses", Ulysses): q, k and v are relaid from sequence
+// sharding [C][B][S/C][N][D] to head sharding [C][B][S][N/C][D] (in global
+// sequence order), every head-group rank computes ordinary causal attention
+// over the whole sequence for its N/C heads, and the output is relaid back.
+// The C head-group ranks are independent problems with the same positions,
+// so they run as one launch with the rank folded into the batch.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cp_internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct AgLayout {
+    size_t k = 0, v = 0, pos = 0, total = 0;
+};
+AgLayout ag_layout(int64_t B, int64_t S, int64_t Nkv, int64_t D) {
+    AgLayout L;
+    const size_t kv = static_cast<size_t>(B) * S * Nkv * D * 2;
+    L.k = 0;
+    L.v = round_up(kv);
+    L.pos = 2 * round_up(kv);
+    L.total = L.pos + round_up(static_cast<size_t>(S) * 4);
+    return L;
+}
+
+struct UlLayout {
+    size_t q = 0, k = 0, v = 0, o = 0, pos = 0, total = 0;
+};
+UlLayout ul_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D) {
+    UlLayout L;
+    const size_t qb = static_cast<size_t>(B) * S * N * D * 2, kvb = static_cast<size_t>(B) * S * Nkv * D * 2;
+    L.q = 0;
+    L.k = round_up(qb);
+    L.v = L.k + round_up(kvb);
+    L.o = L.v + round_up(kvb);
+    L.pos = L.o + round_up(static_cast<size_t>(B) * S * N * D * 4);
+    L.total = L.pos + round_up(static_cast<size_t>(S) * 4);
+    return L;
+}
+
+cp_status check_common(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, cp_layout layout) {
+    if (layout != CP_ZIGZAG && layout != CP_CONTIGUOUS) return CP_ERR_ARGUMENT;
+    if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
+    if (D != 64 && D != 128) return CP_ERR_UNSUPPORTED;
+    if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
+    if (S > INT32_MAX / 2) return CP_ERR_SHAPE;
+    return CP_OK;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" cp_status cp_allgather_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
+                                                 size_t *bytes) {
+    if (!bytes) return CP_ERR_NULL;
+    if (C < 1 || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
+    *bytes = ag_layout(B, S, Nkv, D).total;
+    return CP_OK;
+}
+
+extern "C" cp_status cp_allgather_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh,
+                                                const int32_t *pos, int64_t B, int64_t S, int64_t N, int64_t Nkv,
+                                                int64_t D, int C, float scale, cp_layout layout, float *o_sh,
+                                                float *lse_sh, void *workspace, size_t ws_bytes,
+                                                cudaStream_t stream) {
+    if (!q_sh || !k_sh || !v_sh || !pos || !o_sh || !lse_sh) return CP_ERR_NULL;
+    cp_status st = check_common(B, S, N, Nkv, D, C, layout);
+    if (st != CP_OK) return st;
+    const AgLayout L = ag_layout(B, S, Nkv, D);
+    if (!workspace || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return CP_ERR_ALIGNMENT;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *k_full = ws + L.k, *v_full = ws + L.v;
+    int32_t *gpos = reinterpret_cast<int32_t *>(ws + L.pos);
+    const int64_t s = S / C;
+    AttnProblem p{};
+    p.q = q_sh;
+    p.k = k_full;
+    p.v = v_full;
+    p.kv_shared = true;
+    p.q_pos = pos;
+    p.q_pos_stride = s;
+    p.k_pos = gpos;
+    p.k_pos_stride = 0;
+    p.o = o_sh;
+    p.lse = lse_sh;
+    p.C = C;
+    p.B = B;
+    p.N = N;
+    p.Nkv = Nkv;
+    p.D = D;
+    p.Sq = s;
+    p.Sk = S;
+    p.scale = scale;
+    st = validate_attn(p);  // everything checked before anything is enqueued
+    if (st != CP_OK) return st;
+    st = cp_zigzag_unshard(k_sh, k_full, B, S, Nkv, D, C, CP_BF16, layout, stream);
+    if (st == CP_OK) st = cp_zigzag_unshard(v_sh, v_full, B, S, Nkv, D, C, CP_BF16, layout, stream);
+    if (st == CP_OK) st = cp_zigzag_positions(gpos, S, 1, CP_CONTIGUOUS, 1, stream);  // 0 .. S-1
+    if (st == CP_OK) st = launch_attn(p, stream);
+    return st;
+}
+
+extern "C" cp_status cp_ulysses_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
+                                               size_t *bytes) {
+    if (!bytes) return CP_ERR_NULL;
+    if (C < 1 || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
+    *bytes = ul_layout(B, S, N, Nkv, D).total;
+    return CP_OK;
+}
+
+extern "C" cp_status cp_ulysses_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh, int64_t B,
+                                              int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, float scale,
+                                              cp_layout layout, float *o_sh, float *lse_h, void *workspace,
+                                              size_t ws_bytes, cudaStream_t stream) {
+    if (!q_sh || !k_sh || !v_sh || !o_sh || !lse_h) return CP_ERR_NULL;
+    cp_status st = check_common(B, S, N, Nkv, D, C, layout);
+    if (st != CP_OK) return st;
+    if (N % C != 0 || Nkv % C != 0) return CP_ERR_DIVISIBILITY;
+    const UlLayout L = ul_layout(B, S, N, Nkv, D);
+    if (!workspace || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return CP_ERR_ALIGNMENT;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *q_h = ws + L.q, *k_h = ws + L.k, *v_h = ws + L.v;
+    float *o_h = reinterpret_cast<float *>(ws + L.o);
+    int32_t *gpos = reinterpret_cast<int32_t *>(ws + L.pos);
+    // contiguous shards concatenated in rank order already are global order
+    const cp_seq_order order = (layout == CP_ZIGZAG) ? CP_GLOBAL_ORDER : CP_RANK_ORDER;
+    AttnProblem p{};
+    p.q = q_h;
+    p.k = k_h;
+    p.v = v_h;
+    p.q_pos = gpos;
+    p.k_pos = gpos;
+    p.q_pos_stride = 0;
+    p.k_pos_stride = 0;
+    p.o = o_h;
+    p.lse = lse_h;
+    p.C = 1;          // head-group ranks folded into the batch: [C*B][S][N/C][D]
+    p.B = C * B;
+    p.N = N / C;
+    p.Nkv = Nkv / C;
+    p.D = D;
+    p.Sq = S;
+    p.Sk = S;
+    p.scale = scale;
+    st = validate_attn(p);
+    if (st != CP_OK) return st;
+    st = cp_ulysses_relayout(q_sh, q_h, B, S, N, D, C, CP_BF16, CP_SEQ_TO_HEAD, order, stream);
+    if (st == CP_OK) st = cp_ulysses_relayout(k_sh, k_h, B, S, Nkv, D, C, CP_BF16, CP_SEQ_TO_HEAD, order, stream);
+    if (st == CP_OK) st = cp_ulysses_relayout(v_sh, v_h, B, S, Nkv, D, C, CP_BF16, CP_SEQ_TO_HEAD, order, stream);
+    if (st == CP_OK) st = cp_zigzag_positions(gpos, S, 1, CP_CONTIGUOUS, 1, stream);
+    if (st == CP_OK) st = launch_attn(p, stream);
+    if (st == CP_OK) st = cp_ulysses_relayout(o_h, o_sh, B, S, N, D, C, CP_F32, CP_HEAD_TO_SEQ, order, stream);
+    return st;
+}

@@ -16,6 +16,7 @@ from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_F32, CP_GLOBAL_ORDER, CP_HEAD_TO_S
 __all__ = [
     "cp_zigzag_shard", "cp_zigzag_unshard", "cp_zigzag_positions", "cp_ulysses_relayout", "cp_attn_partial",
     "cp_lse_merge", "cp_ring_workspace_size", "cp_ring_attention_fwd", "cp_ring_attention_fwd_noalloc",
+    "cp_allgather_attention_fwd", "cp_ulysses_attention_fwd",
     "cp_device_status", "cp_version",
     "CP_BF16", "CP_F32", "CP_ZIGZAG", "CP_CONTIGUOUS", "CP_SEQ_TO_HEAD", "CP_HEAD_TO_SEQ", "CP_RANK_ORDER",
     "CP_GLOBAL_ORDER", "CpError",
@@ -164,6 +165,56 @@ def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, p
         arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         st = L.cp_ring_attention_fwd_traced(*args, arr, len(events))
         _lib.check("cp_ring_attention_fwd_traced", st)
+    return o, lse
+
+
+def cp_allgather_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, workspace=None, o=None,
+                               lse=None, stream=None):
+    """All-gather CP forward over C resident virtual ranks -> (o_sh fp32, lse_sh fp32)."""
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    S = C * s
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q_sh.device
+    if o is None:
+        o = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
+    L = _lib.lib()
+    n = ctypes.c_size_t(0)
+    _lib.check("cp_allgather_workspace_size", L.cp_allgather_workspace_size(B, S, N, Nkv, D, C, ctypes.byref(n)))
+    if workspace is None:
+        workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
+    st = L.cp_allgather_attention_fwd(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, S, N, Nkv, D, C,
+                                      float(scale), layout, _ptr(o), _ptr(lse), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream))
+    _lib.check("cp_allgather_attention_fwd", st)
+    return o, lse
+
+
+def cp_ulysses_attention_fwd(q_sh, k_sh, v_sh, scale=None, layout=CP_ZIGZAG, workspace=None, o=None, lse=None,
+                             stream=None):
+    """Ulysses (all-to-all) CP forward -> (o_sh fp32 [C,B,s,N,D], lse_h fp32 [C,B,N/C,S])."""
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    S = C * s
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q_sh.device
+    if o is None:
+        o = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((C, B, N // C, S), dtype=torch.float32, device=dev)
+    L = _lib.lib()
+    n = ctypes.c_size_t(0)
+    _lib.check("cp_ulysses_workspace_size", L.cp_ulysses_workspace_size(B, S, N, Nkv, D, C, ctypes.byref(n)))
+    if workspace is None:
+        workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
+    st = L.cp_ulysses_attention_fwd(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), B, S, N, Nkv, D, C, float(scale), layout,
+                                    _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _lib.check("cp_ulysses_attention_fwd", st)
     return o, lse
 
 

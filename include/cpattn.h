@@ -222,6 +222,52 @@ cp_status cp_ring_attention_fwd_traced(const void *q_sh, const void *k_sh, const
                                        cudaEvent_t const *events, int n_events);
 
 /*
+ * cp_allgather_workspace_size / cp_allgather_attention_fwd -- all-gather
+ * context-parallel attention forward for C virtual ranks on this GPU.
+ * [OCP] All-gather / Forward: each rank keeps its local queries, K and V are
+ * gathered from every rank and reordered to global sequence order, and each
+ * rank's queries attend to the full sequence (query positions `pos`, key
+ * positions 0..S-1).  Here the gather is cp_zigzag_unshard of the resident
+ * shards into the workspace, and all C ranks share one launch.
+ *   q_sh, k_sh, v_sh, pos, layout : as for cp_ring_attention_fwd
+ *   o_sh   : device fp32 [C][B][S/C][N][D] (32-byte aligned), written
+ *   lse_sh : device fp32 [C][B][N][S/C], written
+ *   workspace : device, >= cp_allgather_workspace_size bytes (the gathered
+ *               K and V, bf16 [B][S][Nkv][D] each, and S int32 positions),
+ *               256-byte aligned
+ * The result equals cp_ring_attention_fwd's (same partial kernel, one
+ * partial instead of C merged ones).
+ */
+cp_status cp_allgather_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
+                                      size_t *bytes);
+cp_status cp_allgather_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh,
+                                     const int32_t *pos, int64_t B, int64_t S, int64_t N, int64_t Nkv,
+                                     int64_t D, int C, float scale, cp_layout layout, float *o_sh,
+                                     float *lse_sh, void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * cp_ulysses_workspace_size / cp_ulysses_attention_fwd -- all-to-all
+ * (Ulysses) context-parallel attention forward for C virtual ranks.
+ * [OCP] All-to-all; [HB] "Ulysses": q, k, v are relaid from sequence
+ * sharding to head sharding (cp_ulysses_relayout, global sequence order),
+ * each head-group rank computes causal attention over the whole sequence for
+ * its N/C heads, and the output is relaid back to sequence sharding.
+ *   q_sh : device bf16 [C][B][S/C][N][D]; k_sh, v_sh : [C][B][S/C][Nkv][D]
+ *          (sharded with `layout`; N % C == 0 and Nkv % C == 0)
+ *   o_sh : device fp32 [C][B][S/C][N][D], written
+ *   lse_h: device fp32 [C][B][N/C][S], written: the log-sum-exp of head
+ *          r*N/C + h' for global query position i is lse_h[r][b][h'][i]
+ *          (head-sharded layout, global order, as the attention computes it)
+ *   workspace : device, >= cp_ulysses_workspace_size bytes, 256-byte aligned
+ */
+cp_status cp_ulysses_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
+                                    size_t *bytes);
+cp_status cp_ulysses_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh, int64_t B,
+                                   int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, float scale,
+                                   cp_layout layout, float *o_sh, float *lse_h, void *workspace,
+                                   size_t ws_bytes, cudaStream_t stream);
+
+/*
  * cp_ring_attention_fwd_noalloc -- cp_ring_attention_fwd for callers that
  * cannot allocate device memory.  The source pages have no counterpart: this
  * entry point exists for callers that may not call cudaMalloc or cannot hand

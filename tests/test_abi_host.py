@@ -98,3 +98,33 @@ def test_merge_and_ring_validation(cplib):
     assert ring(*bad, FAKE, 1 << 40, None) == 7
     ev = (ctypes.c_void_p * 3)()
     assert cplib.cp_ring_attention_fwd_traced(*args, FAKE, need, None, ev, 3) == 10  # needs 4C events
+
+
+def test_allgather_and_ulysses_validation(cplib):
+    n = ctypes.c_size_t(0)
+    assert cplib.cp_allgather_workspace_size(1, 256, 2, 2, 64, 2, ctypes.byref(n)) == 0 and n.value > 0
+    need_ag = n.value
+    ag = cplib.cp_allgather_attention_fwd
+    args = [FAKE, FAKE, FAKE, FAKE, 1, 256, 2, 2, 64, 2, 0.125, 0, FAKE, FAKE]
+    assert ag(*args, NULL, 0, None) == 6
+    assert ag(*args, FAKE, need_ag - 1, None) == 6
+    bad = list(args)
+    bad[8] = 96
+    assert ag(*bad, FAKE, 1 << 40, None) == 7          # D
+    bad = list(args)
+    bad[5] = 250
+    assert ag(*bad, FAKE, 1 << 40, None) == 3          # S % 2C
+    bad = list(args)
+    bad[0] = NULL
+    assert ag(*bad, FAKE, need_ag, None) == 1
+    assert cplib.cp_ulysses_workspace_size(1, 256, 4, 4, 64, 2, ctypes.byref(n)) == 0 and n.value > 0
+    need_ul = n.value
+    ul = cplib.cp_ulysses_attention_fwd
+    uargs = [FAKE, FAKE, FAKE, 1, 256, 4, 4, 64, 2, 0.125, 0, FAKE, FAKE]
+    assert ul(*uargs, FAKE, need_ul - 1, None) == 6
+    bad = list(uargs)
+    bad[5] = 3                                          # N % C
+    assert ul(*bad, FAKE, 1 << 40, None) == 3
+    bad = list(uargs)
+    bad[6] = 1                                          # Nkv % C
+    assert ul(*bad, FAKE, 1 << 40, None) == 3
