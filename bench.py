@@ -264,6 +264,7 @@ def run_ours(args, w):
     s = S // C
     lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
     prefetch = 1 if args.prefetch else 0
+    fused = bool(args.fused_merge)
 
     # resident buffers
     qd, kd, vd = (t.to(dev) for t in (q, k, v))
@@ -274,8 +275,8 @@ def run_ours(args, w):
     o_sh = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
     lse_sh = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
     o_full = torch.empty((B, S, N, D), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32)), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32, fused)),
+                     dtype=torch.uint8, device=dev)
     qh = torch.empty((C, B, S, N // C, D), dtype=torch.bfloat16, device=dev)
     kh = torch.empty((C, B, S, Nkv // C, D), dtype=torch.bfloat16, device=dev)
     vh = torch.empty_like(kh)
@@ -299,7 +300,8 @@ def run_ours(args, w):
         mark("shard", 1)
         F.cp_zigzag_positions(S, C, lay, out=pos)
         F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch, o_dtype=F.CP_F32, workspace=ws,
-                                o=o_sh, lse=lse_sh, events=ev["ring"] if ev is not None else None)
+                                o=o_sh, lse=lse_sh, events=ev["ring"] if ev is not None else None,
+                                fused_merge=fused)
         mark("unshard", 0)
         F.cp_zigzag_unshard(o_sh, lay, out=o_full)
         mark("unshard", 1)
@@ -309,7 +311,7 @@ def run_ours(args, w):
         F.cp_ulysses_relayout(vs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=vh)
         mark("relayout", 1)
 
-    launches_per_step = 3 + 1 + C + (C - 1) + 1 + 3
+    launches_per_step = 3 + 1 + C + (0 if fused else C - 1) + 1 + 3
     # ---- warm-up
     for _ in range(args.warmup):
         step(qd, kd, vd, None)
@@ -357,6 +359,24 @@ def run_ours(args, w):
         shard_ms += e["shard"][0].elapsed_time(e["shard"][1]) / args.steps
         unshard_ms += e["unshard"][0].elapsed_time(e["unshard"][1]) / args.steps
         relayout_ms += e["relayout"][0].elapsed_time(e["relayout"][1]) / args.steps
+    if fused:
+        # the step merges inside the attention epilogue; time the standalone merge
+        # kernel on the same ring (separate-merge mode, traced) for its GB/s
+        ws2 = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32, False)),
+                          dtype=torch.uint8, device=dev)
+        o2, l2 = torch.empty_like(o_sh), torch.empty_like(lse_sh)
+        merge_ms = [0.0] * C
+        reps = 2
+        for rep_i in range(reps + 1):
+            ev2 = mk_events(n_ring_ev)
+            F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch, o_dtype=F.CP_F32, workspace=ws2,
+                                    o=o2, lse=l2, events=ev2, fused_merge=False)
+            torch.cuda.synchronize()
+            if rep_i == 0:
+                continue  # warm-up
+            for st in range(1, C):
+                merge_ms[st] += ev2[4 * st + 2].elapsed_time(ev2[4 * st + 3]) / reps
+        del ws2, o2, l2
     attn_flops = [4.0 * B * N * D * p for p in step_pairs]
     attn_total_ms = sum(attn_ms)
     attn_tflops = sum(attn_flops) / (attn_total_ms * 1e-3) / 1e12
@@ -417,7 +437,9 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, prefetch),
+        "config": dict(workload_config(w, prefetch),
+                       merge="fused into the attention epilogue (standalone merge kernel timed separately)"
+                       if fused else "standalone merge kernel per ring step"),
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak_tc, "traffic": traffic,
                      "kernel": "attn_fwd_kernel<%d>" % D,
@@ -431,6 +453,7 @@ def run_ours(args, w):
         "kernels": {
             "attn_ms_per_ring_step": attn_ms, "attn_tflops_per_ring_step": per_step_tflops,
             "merge_ms_per_ring_step": merge_ms[1:], "merge_gbs": merge_gbs,
+            "merge_measured_in": "separate-merge ring calls after the timed region" if fused else "the timed step",
             "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "relayout_gbs": relayout_gbs,
             "hbm_peak_gbs": peaks["hbm_gbs"],
             "merge_frac_hbm": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
@@ -578,6 +601,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="s32k")
     ap.add_argument("--no-prefetch", dest="prefetch", action="store_false")
+    ap.add_argument("--fused-merge", dest="fused_merge", action="store_true",
+                    help="merge each ring step in the attention epilogue instead of with the standalone merge kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="run the contiguous-vs-zigzag sweep instead")

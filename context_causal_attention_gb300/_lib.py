@@ -22,6 +22,7 @@ CP_BF16, CP_F32 = 0, 1
 CP_ZIGZAG, CP_CONTIGUOUS = 0, 1
 CP_SEQ_TO_HEAD, CP_HEAD_TO_SEQ = 0, 1
 CP_RANK_ORDER, CP_GLOBAL_ORDER = 0, 1
+CP_RING_PREFETCH, CP_RING_FUSED_MERGE = 1, 2
 
 
 class CpError(RuntimeError):

@@ -109,6 +109,7 @@ struct AttnArgs {
     int kv_shift, kpos_shift;
     int kv_shared;  // all ranks read the same K/V (rank index 0)
     int kpr;        // key-position ranks with tables: 1 if shared, else C
+    int merge_into; // LSE-merge the partial into the (o, lse) accumulator
     float scale_log2;
     unsigned long long timeout_ns;
     FastDiv div_bn, div_nqb, div_n;  // by B*N, nqb, N (work-item decoding)
@@ -636,12 +637,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long orow = static_cast<long long>(itm.r * a.B + itm.b) * a.Sq + row;
             float *o_row = a.o + (orow * a.N + itm.h) * D;
             float *lse_out = a.lse + (static_cast<long long>(itm.r * a.B + itm.b) * a.N + itm.h) * a.Sq + row;
+            const int n_item = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
             float m_run = -INFINITY, l_run = 0.f;
             int j = 0;
             for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
                  kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt), ++j) {
                 if (!mbar_wait(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
+                if (a.merge_into && row_valid && j == n_item - 1) {
+                    // the epilogue will read this row of the accumulator: start it towards L2
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) prefetch_l2(o_row + c);
+                }
                 uint32_t sa[64], sb[64];
                 const int2 kmm = kt_o[kt];
                 const bool need_mask = (kmm.y > qmin_t) || (kt * 128 + 128 > a.Sk);
@@ -726,8 +733,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if (j == 0) {
-                // nothing visible for this whole block: o = 0, lse = -inf
-                if (row_valid) {
+                // nothing visible for this whole block: o = 0, lse = -inf (a merge
+                // leaves the accumulator as it is)
+                if (row_valid && !a.merge_into) {
 #pragma unroll
                     for (int c = 0; c < D; c += 8) st_global_v8(o_row + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
                     *lse_out = -INFINITY;
@@ -737,20 +745,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
             tc_fence_after();
             const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32(tO + c0, ov);
-                if (row_valid) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 8)
-                        st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l,
-                                     __uint_as_float(ov[c + 2]) * inv_l, __uint_as_float(ov[c + 3]) * inv_l,
-                                     __uint_as_float(ov[c + 4]) * inv_l, __uint_as_float(ov[c + 5]) * inv_l,
-                                     __uint_as_float(ov[c + 6]) * inv_l, __uint_as_float(ov[c + 7]) * inv_l);
+            const float lse_t = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+            // o_row <- wa * o_row + wt * O (O unnormalised in TMEM); plain write: wa = 0
+            bool write = row_valid;
+            float wa = 0.f, wt = inv_l, lse_new = lse_t;
+            if (a.merge_into && row_valid) {
+                // "On Context Parallelism", Peer-to-peer / Forward, the tile merge
+                const float la = *lse_out;
+                if (lse_t == -INFINITY) {
+                    write = false;
+                } else if (la != -INFINITY) {
+                    const float mx = fmaxf(la, lse_t), mn = fminf(la, lse_t);
+                    lse_new = mx + log1pf(expf(mn - mx));
+                    wa = expf(la - lse_new);
+                    wt = expf(lse_t - lse_new) * inv_l;
                 }
             }
-            if (row_valid) *lse_out = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+            if (!a.merge_into) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c0, ov);
+                    if (write) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8)
+                            st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * wt, __uint_as_float(ov[c + 1]) * wt,
+                                         __uint_as_float(ov[c + 2]) * wt, __uint_as_float(ov[c + 3]) * wt,
+                                         __uint_as_float(ov[c + 4]) * wt, __uint_as_float(ov[c + 5]) * wt,
+                                         __uint_as_float(ov[c + 6]) * wt, __uint_as_float(ov[c + 7]) * wt);
+                    }
+                }
+            } else {
+                const bool read_acc = write && wa != 0.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float acc[16];
+                    if (read_acc) {
+                        // issued before the TMEM load so both latencies overlap (the row
+                        // was sent towards L2 when the item's last tile started)
+                        float t8[8];
+                        ld_global_v8(o_row + c0, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = t8[e];
+                        ld_global_v8(o_row + c0 + 8, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[8 + e] = t8[e];
+                    }
+                    uint32_t ov[16];
+                    tmem_ld16(tO + c0, ov);
+                    if (write) {
+#pragma unroll
+                        for (int c = 0; c < 16; c += 8) {
+                            float r8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                r8[e] = read_acc ? fmaf(wa, acc[c + e], wt * __uint_as_float(ov[c + e]))
+                                                 : wt * __uint_as_float(ov[c + e]);
+                            st_global_v8(o_row + c0 + c, r8[0], r8[1], r8[2], r8[3], r8[4], r8[5], r8[6], r8[7]);
+                        }
+                    }
+                }
+            }
+            if (write) *lse_out = lse_new;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.o_empty + wg);
@@ -825,6 +881,7 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.nqb = (a.nqt + 1) / 2;
     a.kv_shift = p.kv_shift;
     a.kv_shared = p.kv_shared ? 1 : 0;
+    a.merge_into = p.merge_into ? 1 : 0;
     a.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
     a.kpos_shift = p.kpos_shift;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);

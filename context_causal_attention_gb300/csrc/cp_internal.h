@@ -50,6 +50,10 @@ struct AttnProblem {
     int64_t B, N, Nkv, D, Sq, Sk;
     int kv_shift, kpos_shift;
     bool kv_shared;
+    // merge_into: o/lse hold an accumulator (o [C][B][Sq][N][D], lse
+    // [C][B][N][Sq]); the partial is LSE-merged into it instead of written
+    // (rows the partial cannot see are left untouched)
+    bool merge_into;
     float scale;
 };
 

@@ -226,6 +226,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr)
         : "memory");
 }
+// Load 16 consecutive 32-bit TMEM columns of this thread's lane and wait.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : CP_R8(r, 0), CP_R8(r, 8)
+        : "r"(taddr)
+        : "memory");
+}
 // Two 32-column loads in flight before one wait (64 columns).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
     asm volatile(
@@ -369,6 +379,17 @@ __device__ __forceinline__ void st_global_v8(float *p, float a, float b, float c
     asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a), "f"(b), "f"(c),
                  "f"(d), "f"(e), "f"(f), "f"(g), "f"(h)
                  : "memory");
+}
+
+// 32-byte global load (8 fp32); the address must be 32-byte aligned.
+__device__ __forceinline__ void ld_global_v8(const float *p, float (&r)[8]) {
+    asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
+                 : "l"(p)
+                 : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
 // ---------------------------------------------------------------- misc

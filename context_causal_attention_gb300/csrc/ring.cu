@@ -8,9 +8,11 @@
 // Attention", "The zigzag fix"), then one merge launch folds the step's
 // partials into the running (o, lse); step 0 writes the accumulator directly.
 //
+// flags (bit set): CP_RING_FUSED_MERGE folds each step's merge into the
+// attention epilogue (the partial is merged straight into the accumulator).
 // The inter-GPU exchange of the pages has two stand-ins here:
-//   prefetch = 0  zero copy: the kernel reads the owner's resident block;
-//   prefetch = 1  the exchange is emulated: the K/V rotation needed by step
+//   no CP_RING_PREFETCH  zero copy: the kernel reads the owner's resident block;
+//   CP_RING_PREFETCH     the exchange is emulated: the K/V rotation needed by step
 //                 st+1 is copied device-to-device on a second stream into a
 //                 double buffer while step st computes ("start the next
 //                 async send/recv before computing", Peer-to-peer / Forward),
@@ -34,18 +36,19 @@ struct Layout {
     size_t o_tile_bytes = 0, lse_bytes = 0, o_acc_bytes = 0, kv_bytes = 0;  // kv: one K (or V) rotation
 };
 
-Layout ws_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, int prefetch, cp_dtype o_dtype) {
+Layout ws_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, int flags, cp_dtype o_dtype) {
     Layout L;
     const int64_t s = S / C;
+    const bool prefetch = (flags & CP_RING_PREFETCH) != 0, fused = (flags & CP_RING_FUSED_MERGE) != 0;
     L.o_tile_bytes = static_cast<size_t>(C) * B * s * N * D * 4;
     L.lse_bytes = static_cast<size_t>(C) * B * N * s * 4;
     L.o_acc_bytes = (o_dtype == CP_BF16) ? L.o_tile_bytes : 0;
     L.kv_bytes = (prefetch && C > 1) ? static_cast<size_t>(C) * B * s * Nkv * D * 2 : 0;
     size_t off = 0;
     L.o_tile = off;
-    off += round_up(C > 1 ? L.o_tile_bytes : 0);
+    off += round_up(C > 1 && !fused ? L.o_tile_bytes : 0);
     L.lse_tile = off;
-    off += round_up(C > 1 ? L.lse_bytes : 0);
+    off += round_up(C > 1 && !fused ? L.lse_bytes : 0);
     L.o_acc = off;
     off += round_up(L.o_acc_bytes);
     L.kv = off;
@@ -112,18 +115,20 @@ cp_status rotate_copy(void *dst, const void *src, size_t rank_bytes, int C, int 
 }
 
 cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos, int64_t B, int64_t S,
-                    int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout, int prefetch,
+                    int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout, int flags,
                     void *o_sh, cp_dtype o_dtype, float *lse_sh, void *workspace, size_t ws_bytes,
                     cudaStream_t stream, const cudaEvent_t *events, int n_events) {
     if (!q_sh || !k_sh || !v_sh || !pos || !o_sh || !lse_sh) return CP_ERR_NULL;
     if (o_dtype != CP_F32 && o_dtype != CP_BF16) return CP_ERR_DTYPE;
     if (layout != CP_ZIGZAG && layout != CP_CONTIGUOUS) return CP_ERR_ARGUMENT;
-    if (prefetch != 0 && prefetch != 1) return CP_ERR_ARGUMENT;
+    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;
+    const int prefetch = (flags & CP_RING_PREFETCH) ? 1 : 0;
+    const bool fused = (flags & CP_RING_FUSED_MERGE) != 0;
     if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
     if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
     if (events && n_events < 4 * C) return CP_ERR_ARGUMENT;
     const int64_t s = S / C;
-    const Layout L = ws_layout(B, S, N, Nkv, D, C, prefetch, o_dtype);
+    const Layout L = ws_layout(B, S, N, Nkv, D, C, flags, o_dtype);
     if (L.total > 0 && (!workspace || ws_bytes < L.total)) return CP_ERR_WORKSPACE;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return CP_ERR_ALIGNMENT;
 
@@ -157,7 +162,7 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         chk.lse = lse_sh;
         cp_status st = validate_attn(chk);
         if (st != CP_OK) return st;
-        if (C > 1 && (!aligned16(o_tile) || !aligned16(lse_tile))) return CP_ERR_ALIGNMENT;
+        if (C > 1 && !fused && (!aligned16(o_tile) || !aligned16(lse_tile))) return CP_ERR_ALIGNMENT;
     }
     const bool use_prefetch = prefetch && C > 1;
     SideRes *res = nullptr;
@@ -202,8 +207,11 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
             ps.v = vbuf[step % 2];
             ps.kv_shift = 0;
         }
-        ps.o = step == 0 ? o_acc : o_tile;
-        ps.lse = step == 0 ? lse_sh : lse_tile;
+        // fused: steps >= 1 merge their partial into the accumulator in the
+        // attention epilogue; otherwise they write the partial and a merge follows
+        ps.merge_into = fused && step > 0;
+        ps.o = (step == 0 || fused) ? o_acc : o_tile;
+        ps.lse = (step == 0 || fused) ? lse_sh : lse_tile;
         rec(4 * step + 0);
         if (st == CP_OK) st = launch_attn(ps, stream);
         rec(4 * step + 1);
@@ -215,7 +223,8 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
             issue_copy(step + 2);
         }
         rec(4 * step + 2);
-        if (step > 0 && st == CP_OK) st = launch_merge(o_acc, lse_sh, o_tile, lse_tile, C * B, s, N, D, stream);
+        if (step > 0 && !fused && st == CP_OK)
+            st = launch_merge(o_acc, lse_sh, o_tile, lse_tile, C * B, s, N, D, stream);
         rec(4 * step + 3);
     }
     if (use_prefetch) {
@@ -235,31 +244,32 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
 using namespace cpattn;
 
 extern "C" cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
-                                            int prefetch, cp_dtype o_dtype, size_t *bytes) {
+                                            int flags, cp_dtype o_dtype, size_t *bytes) {
     if (!bytes) return CP_ERR_NULL;
     if (o_dtype != CP_F32 && o_dtype != CP_BF16) return CP_ERR_DTYPE;
     if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
     if (S % C != 0) return CP_ERR_DIVISIBILITY;
-    *bytes = ws_layout(B, S, N, Nkv, D, C, prefetch ? 1 : 0, o_dtype).total;
+    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;
+    *bytes = ws_layout(B, S, N, Nkv, D, C, flags, o_dtype).total;
     return CP_OK;
 }
 
 extern "C" cp_status cp_ring_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos,
                                            int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
-                                           float scale, cp_layout layout, int prefetch, void *o_sh,
+                                           float scale, cp_layout layout, int flags, void *o_sh,
                                            cp_dtype o_dtype, float *lse_sh, void *workspace, size_t ws_bytes,
                                            cudaStream_t stream) {
-    return ring_impl(q_sh, k_sh, v_sh, pos, B, S, N, Nkv, D, C, scale, layout, prefetch, o_sh, o_dtype, lse_sh,
+    return ring_impl(q_sh, k_sh, v_sh, pos, B, S, N, Nkv, D, C, scale, layout, flags, o_sh, o_dtype, lse_sh,
                      workspace, ws_bytes, stream, nullptr, 0);
 }
 
 extern "C" cp_status cp_ring_attention_fwd_traced(const void *q_sh, const void *k_sh, const void *v_sh,
                                                   const int32_t *pos, int64_t B, int64_t S, int64_t N,
                                                   int64_t Nkv, int64_t D, int C, float scale, cp_layout layout,
-                                                  int prefetch, void *o_sh, cp_dtype o_dtype, float *lse_sh,
+                                                  int flags, void *o_sh, cp_dtype o_dtype, float *lse_sh,
                                                   void *workspace, size_t ws_bytes, cudaStream_t stream,
                                                   cudaEvent_t const *events, int n_events) {
     if (!events) return CP_ERR_NULL;
-    return ring_impl(q_sh, k_sh, v_sh, pos, B, S, N, Nkv, D, C, scale, layout, prefetch, o_sh, o_dtype, lse_sh,
+    return ring_impl(q_sh, k_sh, v_sh, pos, B, S, N, Nkv, D, C, scale, layout, flags, o_sh, o_dtype, lse_sh,
                      workspace, ws_bytes, stream, events, n_events);
 }

@@ -11,7 +11,7 @@ import torch
 
 from . import _lib
 from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_F32, CP_GLOBAL_ORDER, CP_HEAD_TO_SEQ, CP_RANK_ORDER,
-                   CP_SEQ_TO_HEAD, CP_ZIGZAG, CpError)
+                   CP_RING_FUSED_MERGE, CP_RING_PREFETCH, CP_SEQ_TO_HEAD, CP_ZIGZAG, CpError)
 
 __all__ = [
     "cp_zigzag_shard", "cp_zigzag_unshard", "cp_zigzag_positions", "cp_ulysses_relayout", "cp_attn_partial",
@@ -19,7 +19,7 @@ __all__ = [
     "cp_allgather_attention_fwd", "cp_ulysses_attention_fwd",
     "cp_device_status", "cp_version",
     "CP_BF16", "CP_F32", "CP_ZIGZAG", "CP_CONTIGUOUS", "CP_SEQ_TO_HEAD", "CP_HEAD_TO_SEQ", "CP_RANK_ORDER",
-    "CP_GLOBAL_ORDER", "CpError",
+    "CP_GLOBAL_ORDER", "CP_RING_PREFETCH", "CP_RING_FUSED_MERGE", "CpError",
 ]
 
 _DT = {torch.bfloat16: CP_BF16, torch.float32: CP_F32}
@@ -127,15 +127,20 @@ def cp_lse_merge(o_acc, lse_acc, o_tile, lse_tile, stream=None):
     return o_acc, lse_acc
 
 
-def cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch=0, o_dtype=CP_F32):
+def _ring_flags(prefetch, fused_merge):
+    return (CP_RING_PREFETCH if prefetch else 0) | (CP_RING_FUSED_MERGE if fused_merge else 0)
+
+
+def cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch=0, o_dtype=CP_F32, fused_merge=False):
     n = ctypes.c_size_t(0)
-    st = _lib.lib().cp_ring_workspace_size(B, S, N, Nkv, D, C, int(prefetch), o_dtype, ctypes.byref(n))
+    st = _lib.lib().cp_ring_workspace_size(B, S, N, Nkv, D, C, _ring_flags(prefetch, fused_merge), o_dtype,
+                                           ctypes.byref(n))
     _lib.check("cp_ring_workspace_size", st)
     return n.value
 
 
 def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, prefetch=0, o_dtype=CP_F32,
-                          workspace=None, o=None, lse=None, events=None, stream=None):
+                          workspace=None, o=None, lse=None, events=None, stream=None, fused_merge=False):
     """Ring attention forward over C resident virtual ranks.
 
     Returns (o_sh [C,B,s,N,D] of o_dtype, lse_sh fp32 [C,B,N,s]).  `events`, if
@@ -151,11 +156,12 @@ def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, p
         o = torch.empty((C, B, s, N, D), dtype=torch.float32 if o_dtype == CP_F32 else torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
-    need = cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, o_dtype)
+    need = cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, o_dtype, fused_merge)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     L = _lib.lib()
-    args = [_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, S, N, Nkv, D, C, float(scale), layout, int(prefetch),
+    args = [_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, S, N, Nkv, D, C, float(scale), layout,
+            _ring_flags(prefetch, fused_merge),
             _ptr(o), o_dtype, _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _stream(stream)]
     if events is None:

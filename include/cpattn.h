@@ -163,14 +163,19 @@ cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int
 cp_status cp_lse_merge(float *o_acc, float *lse_acc, const float *o_tile, const float *lse_tile,
                        int64_t B, int64_t Sq, int64_t N, int64_t D, cudaStream_t stream);
 
+/* Ring options (bit set, argument `flags` of the ring calls). */
+#define CP_RING_PREFETCH 1    /* emulate the ring exchange by side-stream K/V copies */
+#define CP_RING_FUSED_MERGE 2 /* merge each step's partial in the attention epilogue */
+
 /*
  * cp_ring_workspace_size -- bytes of device workspace cp_ring_attention_fwd
- * needs for these sizes: the per-step partial (fp32 o and lse for all C
- * ranks), an fp32 accumulator when o_dtype is CP_BF16, and with prefetch two
- * K/V rotation buffers.  Host only; *bytes is written on success.
+ * needs for these sizes and flags: the per-step partial (fp32 o and lse for
+ * all C ranks; not with CP_RING_FUSED_MERGE), an fp32 accumulator when o_dtype
+ * is CP_BF16, and with CP_RING_PREFETCH two K/V rotation buffers.  Host only;
+ * *bytes is written on success.
  */
 cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
-                                 int prefetch, cp_dtype o_dtype, size_t *bytes);
+                                 int flags, cp_dtype o_dtype, size_t *bytes);
 
 /*
  * cp_ring_attention_fwd -- ring (P2P) context-parallel attention forward for
@@ -185,10 +190,15 @@ cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, i
  *   pos           : device int32 [C][S/C] global positions (cp_zigzag_positions)
  *   layout        : selects the divisibility rule only (S % 2C for zigzag,
  *                   S % C for contiguous); masks come from `pos`
- *   prefetch      : 0 = zero-copy (each step reads the owner's resident
- *                   block); 1 = the ring exchange is emulated by device
- *                   copies of the next step's K/V on a second stream,
- *                   overlapped with the current step and ordered by events
+ *   flags         : bit set of
+ *                   CP_RING_PREFETCH -- the ring exchange is emulated by
+ *                     device copies of the next step's K/V on a second
+ *                     stream, overlapped with the current step and ordered
+ *                     by events (without it: zero copy, each step reads the
+ *                     owner's resident block);
+ *                   CP_RING_FUSED_MERGE -- steps >= 1 merge their partial
+ *                     into (o, lse) inside the attention epilogue instead of
+ *                     writing it and launching cp_lse_merge's kernel
  *   o_sh          : device [C][B][S/C][N][D] of o_dtype (CP_F32 or CP_BF16);
  *                   32-byte aligned when o_dtype is CP_F32
  *   lse_sh        : device fp32 [C][B][N][S/C]
@@ -198,7 +208,7 @@ cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, i
  */
 cp_status cp_ring_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh,
                                 const int32_t *pos, int64_t B, int64_t S, int64_t N, int64_t Nkv,
-                                int64_t D, int C, float scale, cp_layout layout, int prefetch,
+                                int64_t D, int C, float scale, cp_layout layout, int flags,
                                 void *o_sh, cp_dtype o_dtype, float *lse_sh, void *workspace,
                                 size_t ws_bytes, cudaStream_t stream);
 
@@ -208,15 +218,15 @@ cp_status cp_ring_attention_fwd(const void *q_sh, const void *k_sh, const void *
  *   events[4*step + 0], events[4*step + 1] : before / after the attention
  *                                            launch of `step`
  *   events[4*step + 2], events[4*step + 3] : before / after the merge launch
- *                                            of `step` (step >= 1; for
- *                                            step 0 both are recorded
- *                                            back to back)
+ *                                            of `step` (recorded back to
+ *                                            back for step 0 and with
+ *                                            CP_RING_FUSED_MERGE)
  * n_events must be >= 4*C; events are caller-created (cudaEventCreate).
  */
 cp_status cp_ring_attention_fwd_traced(const void *q_sh, const void *k_sh, const void *v_sh,
                                        const int32_t *pos, int64_t B, int64_t S, int64_t N,
                                        int64_t Nkv, int64_t D, int C, float scale,
-                                       cp_layout layout, int prefetch, void *o_sh,
+                                       cp_layout layout, int flags, void *o_sh,
                                        cp_dtype o_dtype, float *lse_sh, void *workspace,
                                        size_t ws_bytes, cudaStream_t stream,
                                        cudaEvent_t const *events, int n_events);

@@ -231,21 +231,25 @@ def ring_inputs(w, cuda_dev, layout):
 
 @pytest.mark.parametrize("wname,layout", [("tiny", "zigzag"), ("s4k", "zigzag"), ("s4k_contig", "contiguous"),
                                           ("c8", "zigzag")])
-@pytest.mark.parametrize("prefetch", [0, 1])
-def test_ring_vs_oracle(cuda_dev, wname, layout, prefetch):
+def test_ring_vs_oracle(cuda_dev, wname, layout):
+    """Every ring mode (zero copy / prefetched K/V rotation x separate / fused
+    merge) against the fp64 oracle ring."""
     extra = {
         "s4k_contig": SY.Workload("s4k_contig", B=1, S=1024, N=4, Nkv=4, D=64, C=4, layout="contiguous"),
         "c8": SY.Workload("c8", B=1, S=2048, N=2, Nkv=2, D=128, C=8),
     }
     w = extra.get(wname) or SY.WORKLOADS[wname]
     (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, layout)
-    o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch)
     pos_np = pos.cpu().numpy()
     o_ref, l_ref = O.ring_fwd(*(O.shard(f64(t), w.C, 0 if layout == "zigzag" else 1) for t in (q, k, v)),
                               pos_np, nthreads=NTH)
-    assert np.isfinite(f64(lse_sh)).all()
-    assert np.max(np.abs(f64(o_sh) - o_ref)) <= ATOL_O
-    assert np.max(np.abs(f64(lse_sh) - l_ref)) <= ATOL_LSE
+    for prefetch in (0, 1):
+        for fused in (False, True):
+            o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch,
+                                                   fused_merge=fused)
+            assert np.isfinite(f64(lse_sh)).all()
+            assert np.max(np.abs(f64(o_sh) - o_ref)) <= ATOL_O, (prefetch, fused)
+            assert np.max(np.abs(f64(lse_sh) - l_ref)) <= ATOL_LSE, (prefetch, fused)
 
 
 def test_ring_vs_monolithic_gpu_and_bf16_output(cuda_dev):
@@ -256,6 +260,9 @@ def test_ring_vs_monolithic_gpu_and_bf16_output(cuda_dev):
     o_m, l_m = F.cp_attn_partial(q.to(cuda_dev), k.to(cuda_dev), v.to(cuda_dev), gp, gp)
     o_ring = F.cp_zigzag_unshard(o_sh, lay)
     assert torch.max(torch.abs(o_ring - o_m)).item() <= RING_VS_MONO
+    o_fu, l_fu = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1, fused_merge=True)
+    assert torch.max(torch.abs(F.cp_zigzag_unshard(o_fu, lay) - o_m)).item() <= RING_VS_MONO
+    assert torch.max(torch.abs(l_fu - lse_sh)).item() <= RING_VS_MONO
     # lse: rank-major [C,B,N,s] -> [B,N,S] via positions
     l_ring = torch.empty_like(l_m)
     for r in range(w.C):
@@ -280,7 +287,8 @@ def _inverse_positions(pos_np):
 @pytest.mark.parametrize("wname", ["s32k", "s128k"])
 def test_ring_full_size_sampled_rows(cuda_dev, wname):
     """Full-size workloads in the benchmark's launch configuration (prefetch on,
-    fp32 output); sampled query rows of two heads checked against the oracle."""
+    separate merge, fp32 output); sampled query rows of two heads checked
+    against the oracle."""
     w = SY.WORKLOADS[wname]
     (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, "zigzag")
     o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1)
