@@ -593,6 +593,56 @@ def run_sweep(args):
     return 0
 
 
+def run_strategies(args):
+    """One JSON line per (workload, strategy): the forward of the ring, the
+    all-gather, the all-to-all (Ulysses) and the A2A x P2P mesh on the same
+    zigzag shards, timed with CUDA events (3 warm-up calls, then the mean of
+    `--steps` calls), TFLOP/s on the algorithmic causal FLOPs."""
+    import torch
+
+    import cp_synth as SY
+    from context_causal_attention_gb300 import build as cuda_build
+    from context_causal_attention_gb300 import ops as F
+
+    cuda_build.build()
+    dev = torch.device("cuda", 0)
+    names = args.strategies.split(",")
+    for wname in names:
+        w = SY.WORKLOADS[wname]
+        q, k, v, _ = SY.make_qkv(w)
+        qs, ks, vs = (F.cp_zigzag_shard(t.to(dev), w.C) for t in (q, k, v))
+        del q, k, v
+        pos = F.cp_zigzag_positions(w.S, w.C, device=dev)
+        runs = [("ring", lambda: F.cp_ring_attention_fwd(qs, ks, vs, pos, prefetch=1)),
+                ("allgather", lambda: F.cp_allgather_attention_fwd(qs, ks, vs, pos))]
+        if w.N % w.C == 0 and w.Nkv % w.C == 0:
+            runs.append(("ulysses", lambda: F.cp_ulysses_attention_fwd(qs, ks, vs)))
+        for A in range(2, w.C):
+            if w.C % A == 0 and w.N % A == 0 and w.Nkv % A == 0:
+                runs.append(("mesh_a%d_r%d" % (A, w.C // A),
+                             lambda A=A: F.cp_mesh_attention_fwd(qs, ks, vs, pos, A, w.C // A, prefetch=1)))
+        for name, fn in runs:
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(3, args.steps)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            print(json.dumps({"strategy": name, "workload": w.name, "S": w.S, "C": w.C, "N": w.N, "D": w.D,
+                              "ms": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
+                              "note": "forward only, inputs already sharded on the device; includes the "
+                                      "strategy's own relayouts / gathers"}), flush=True)
+            torch.cuda.empty_cache()
+        del qs, ks, vs, pos
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -606,10 +656,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="run the contiguous-vs-zigzag sweep instead")
+    ap.add_argument("--strategies", default="",
+                    help="comma-separated workloads: time ring / all-gather / Ulysses / mesh forwards instead")
     ap.add_argument("--sweep-only", default="", help="comma-separated sweep workload names")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
+    if args.strategies:
+        return run_strategies(args)
     import cp_synth as SY
     w = SY.WORKLOADS.get(args.workload)
     if w is None:

@@ -75,6 +75,9 @@ def lib():
                                              vp]
     L.cp_ulysses_workspace_size.argtypes = [i64, i64, i64, i64, i64, i32, ctypes.POINTER(sz)]
     L.cp_ulysses_attention_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, vp, vp, sz, vp]
+    L.cp_mesh_workspace_size.argtypes = [i64, i64, i64, i64, i64, i32, i32, i32, ctypes.POINTER(sz)]
+    L.cp_mesh_attention_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, f32, i32, i32, vp, vp, vp,
+                                        sz, vp]
     L.cp_ring_attention_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, i32, vp,
                                                 vp]
     for name in header_symbols():

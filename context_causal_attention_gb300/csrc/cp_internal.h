@@ -68,6 +68,10 @@ cp_status launch_merge(float *o_acc, float *lse_acc, const float *o_tile, const 
                        int64_t Sq, int64_t N, int64_t D, cudaStream_t stream);
 
 // fp32 -> bf16 (round to nearest even), n elements, n % 8 == 0.
+// cp_ulysses_relayout applied to `groups` independent blocks laid out one
+// after another (same byte offset of each block on both sides); one launch.
+cp_status ulysses_relayout_groups(const void *in, void *out, int64_t B, int64_t S, int64_t N, int64_t D, int C,
+                                  int groups, cp_dtype dtype, cp_dir dir, cp_seq_order order, cudaStream_t stream);
 cp_status launch_f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t stream);
 
 }  // namespace cpattn

@@ -32,6 +32,8 @@ struct SegArgs {
     long long seg_rows;    // rows per segment
     long long vec_per_row; // row_bytes / 16
     int vpr_shift;         // log2(vec_per_row) or -1
+    long long seg_per_group;  // Ulysses: segments of one independent group (0 = one group)
+    long long group_bytes;    // Ulysses: byte distance between groups, same on both sides
 };
 
 struct Seg {
@@ -40,6 +42,11 @@ struct Seg {
 
 __device__ __forceinline__ Seg segment(const SegArgs &a, long long y) {
     Seg s;
+    long long grp = 0;
+    if (a.seg_per_group) {
+        grp = y / a.seg_per_group;
+        y -= grp * a.seg_per_group;
+    }
     if (a.kind == kZigzagShard || a.kind == kContigShard) {
         // y -> (r, b, half); one segment is a contiguous run of seg_rows rows of N*D
         const long long halves = (a.kind == kZigzagShard) ? 2 : 1;
@@ -92,6 +99,8 @@ __device__ __forceinline__ Seg segment(const SegArgs &a, long long y) {
             s.src_stride = head_stride;
             s.dst_stride = seq_stride;
         }
+        s.src_off += grp * a.group_bytes;
+        s.dst_off += grp * a.group_bytes;
     }
     return s;
 }
@@ -246,19 +255,22 @@ extern "C" cp_status cp_zigzag_positions(int32_t *pos, int64_t S, int C, cp_layo
     return last_launch_status();
 }
 
-extern "C" cp_status cp_ulysses_relayout(const void *in, void *out, int64_t B, int64_t S, int64_t N, int64_t D, int C,
-                                         cp_dtype dtype, cp_dir dir, cp_seq_order order, cudaStream_t stream) {
+namespace cpattn {
+
+cp_status ulysses_relayout_groups(const void *in, void *out, int64_t B, int64_t S, int64_t N, int64_t D, int C,
+                                  int groups, cp_dtype dtype, cp_dir dir, cp_seq_order order, cudaStream_t stream) {
     if (!in || !out) return CP_ERR_NULL;
     if (dtype != CP_BF16 && dtype != CP_F32) return CP_ERR_DTYPE;
     if ((dir != CP_SEQ_TO_HEAD && dir != CP_HEAD_TO_SEQ) || (order != CP_RANK_ORDER && order != CP_GLOBAL_ORDER))
         return CP_ERR_ARGUMENT;
-    if (B < 1 || S < 1 || N < 1 || D < 1 || C < 1) return CP_ERR_SHAPE;
+    if (B < 1 || S < 1 || N < 1 || D < 1 || C < 1 || groups < 1) return CP_ERR_SHAPE;
     if (S % C != 0 || N % C != 0) return CP_ERR_DIVISIBILITY;
     if (order == CP_GLOBAL_ORDER && S % (2LL * C) != 0) return CP_ERR_DIVISIBILITY;
     const long long es = static_cast<long long>(dtype_size(dtype));
     const long long hb = (N / C) * D * es;
     if (!aligned16(in) || !aligned16(out) || hb % 16 != 0) return CP_ERR_ALIGNMENT;
-    const size_t nbytes = static_cast<size_t>(B * S * N * D * es);
+    const size_t gbytes = static_cast<size_t>(B * S * N * D * es);
+    const size_t nbytes = gbytes * static_cast<size_t>(groups);
     if (ranges_overlap(in, nbytes, out, nbytes)) return CP_ERR_ARGUMENT;
     SegArgs a{};
     a.src = static_cast<const uint8_t *>(in);
@@ -271,6 +283,15 @@ extern "C" cp_status cp_ulysses_relayout(const void *in, void *out, int64_t B, i
     a.C = C;
     a.row_bytes = hb;
     a.seg_rows = a.global_order ? S / (2LL * C) : S / C;
-    const long long nseg = static_cast<long long>(C) * B * C * (a.global_order ? 2 : 1);
-    return launch_segments(a, nseg, stream);
+    const long long per_group = static_cast<long long>(C) * B * C * (a.global_order ? 2 : 1);
+    a.seg_per_group = groups > 1 ? per_group : 0;
+    a.group_bytes = static_cast<long long>(gbytes);
+    return launch_segments(a, per_group * groups, stream);
+}
+
+}  // namespace cpattn
+
+extern "C" cp_status cp_ulysses_relayout(const void *in, void *out, int64_t B, int64_t S, int64_t N, int64_t D, int C,
+                                         cp_dtype dtype, cp_dir dir, cp_seq_order order, cudaStream_t stream) {
+    return ulysses_relayout_groups(in, out, B, S, N, D, C, 1, dtype, dir, order, stream);
 }

@@ -16,6 +16,16 @@
 // over the whole sequence for its N/C heads, and the output is relaid back.
 // The C head-group ranks are independent problems with the same positions,
 // so they run as one launch with the rank folded into the batch.
+//
+// A2A x P2P mesh ("On Context Parallelism", Peer-to-peer + All-to-all): the
+// C = A*R ranks form A2A groups of A consecutive ranks (g*A .. g*A+A-1) and
+// P2P groups of R ranks with stride A (a, A+a, 2A+a, ...).  Inside each A2A
+// group the sequence shards become head shards (rank order, N/A heads each,
+// the group's A*S/C positions concatenated in rank order); each P2P group then
+// runs the ring over its R ranks with those concatenated positions, and the
+// output goes back through the inverse relayout.  In memory the relaid tensors
+// are [R][A][B][S/R][N/A][D]: the A2A index joins the batch, so the A
+// independent P2P rings are one ring of R ranks over batch A*B.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,6 +48,23 @@ AgLayout ag_layout(int64_t B, int64_t S, int64_t Nkv, int64_t D) {
     L.v = round_up(kv);
     L.pos = 2 * round_up(kv);
     L.total = L.pos + round_up(static_cast<size_t>(S) * 4);
+    return L;
+}
+
+struct MeshLayout {
+    size_t q = 0, k = 0, v = 0, o = 0, ring = 0, ring_bytes = 0, total = 0;
+};
+MeshLayout mesh_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int A, int R, int flags,
+                       cp_status *st) {
+    MeshLayout L;
+    const size_t qb = static_cast<size_t>(B) * S * N * D * 2, kvb = static_cast<size_t>(B) * S * Nkv * D * 2;
+    L.q = 0;
+    L.k = round_up(qb);
+    L.v = L.k + round_up(kvb);
+    L.o = L.v + round_up(kvb);
+    L.ring = L.o + round_up(static_cast<size_t>(B) * S * N * D * 4);
+    *st = cp_ring_workspace_size(static_cast<int64_t>(A) * B, S, N / A, Nkv / A, D, R, flags, CP_F32, &L.ring_bytes);
+    L.total = L.ring + round_up(L.ring_bytes);
     return L;
 }
 
@@ -172,5 +199,74 @@ extern "C" cp_status cp_ulysses_attention_fwd(const void *q_sh, const void *k_sh
     if (st == CP_OK) st = cp_zigzag_positions(gpos, S, 1, CP_CONTIGUOUS, 1, stream);
     if (st == CP_OK) st = launch_attn(p, stream);
     if (st == CP_OK) st = cp_ulysses_relayout(o_h, o_sh, B, S, N, D, C, CP_F32, CP_HEAD_TO_SEQ, order, stream);
+    return st;
+}
+
+extern "C" cp_status cp_mesh_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int A, int R,
+                                            int flags, size_t *bytes) {
+    if (!bytes) return CP_ERR_NULL;
+    if (A < 1 || R < 1 || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
+    if (N % A != 0 || Nkv % A != 0 || S % (static_cast<int64_t>(A) * R) != 0) return CP_ERR_DIVISIBILITY;
+    cp_status st = CP_OK;
+    const MeshLayout L = mesh_layout(B, S, N, Nkv, D, A, R, flags, &st);
+    if (st != CP_OK) return st;
+    *bytes = L.total;
+    return CP_OK;
+}
+
+extern "C" cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos,
+                                           int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int A, int R,
+                                           float scale, cp_layout layout, int flags, float *o_sh, float *lse_h,
+                                           void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!q_sh || !k_sh || !v_sh || !pos || !o_sh || !lse_h) return CP_ERR_NULL;
+    if (A < 1 || R < 1 || static_cast<int64_t>(A) * R > kMaxC) return CP_ERR_SHAPE;
+    const int C = A * R;
+    cp_status st = check_common(B, S, N, Nkv, D, C, layout);
+    if (st != CP_OK) return st;
+    if (N % A != 0 || Nkv % A != 0) return CP_ERR_DIVISIBILITY;
+    const MeshLayout L = mesh_layout(B, S, N, Nkv, D, A, R, flags, &st);
+    if (st != CP_OK) return st;
+    if (!workspace || ws_bytes < L.total) return CP_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return CP_ERR_ALIGNMENT;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *q_h = ws + L.q, *k_h = ws + L.k, *v_h = ws + L.v;
+    float *o_h = reinterpret_cast<float *>(ws + L.o);
+    const int64_t sg = S / R;  // positions of one A2A group (A shards, rank order)
+    // the relayouts are enqueued before the ring validates its own launch, so
+    // check here, before anything is enqueued, the problem the ring will run
+    {
+        AttnProblem p{};
+        p.q = q_h;
+        p.k = k_h;
+        p.v = v_h;
+        p.q_pos = pos;
+        p.k_pos = pos;
+        p.q_pos_stride = sg;
+        p.k_pos_stride = sg;
+        p.o = o_h;
+        p.lse = lse_h;
+        p.C = R;
+        p.B = static_cast<int64_t>(A) * B;
+        p.N = N / A;
+        p.Nkv = Nkv / A;
+        p.D = D;
+        p.Sq = sg;
+        p.Sk = sg;
+        p.scale = scale;
+        st = validate_attn(p);
+        if (st != CP_OK) return st;
+        if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;
+    }
+    // pos [C][S/C] read as [R][S/R] is each A2A group's concatenation in rank order
+    st = ulysses_relayout_groups(q_sh, q_h, B, sg, N, D, A, R, CP_BF16, CP_SEQ_TO_HEAD, CP_RANK_ORDER, stream);
+    if (st == CP_OK)
+        st = ulysses_relayout_groups(k_sh, k_h, B, sg, Nkv, D, A, R, CP_BF16, CP_SEQ_TO_HEAD, CP_RANK_ORDER, stream);
+    if (st == CP_OK)
+        st = ulysses_relayout_groups(v_sh, v_h, B, sg, Nkv, D, A, R, CP_BF16, CP_SEQ_TO_HEAD, CP_RANK_ORDER, stream);
+    if (st == CP_OK)
+        st = cp_ring_attention_fwd(q_h, k_h, v_h, pos, static_cast<int64_t>(A) * B, S, N / A, Nkv / A, D, R, scale,
+                                   CP_CONTIGUOUS, flags, o_h, CP_F32, lse_h, ws + L.ring, L.ring_bytes, stream);
+    if (st == CP_OK)
+        st = ulysses_relayout_groups(o_h, o_sh, B, sg, N, D, A, R, CP_F32, CP_HEAD_TO_SEQ, CP_RANK_ORDER, stream);
     return st;
 }

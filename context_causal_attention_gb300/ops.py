@@ -224,6 +224,41 @@ def cp_ulysses_attention_fwd(q_sh, k_sh, v_sh, scale=None, layout=CP_ZIGZAG, wor
     return o, lse
 
 
+def cp_mesh_workspace_size(B, S, N, Nkv, D, A, R, prefetch=0, fused_merge=False):
+    n = ctypes.c_size_t(0)
+    st = _lib.lib().cp_mesh_workspace_size(B, S, N, Nkv, D, A, R, _ring_flags(prefetch, fused_merge), ctypes.byref(n))
+    _lib.check("cp_mesh_workspace_size", st)
+    return n.value
+
+
+def cp_mesh_attention_fwd(q_sh, k_sh, v_sh, pos, A, R, scale=None, layout=CP_ZIGZAG, prefetch=0, fused_merge=False,
+                          workspace=None, o=None, lse=None, stream=None):
+    """A2A x P2P mesh CP forward over C = A*R resident virtual ranks.
+
+    Returns (o_sh fp32 [C,B,s,N,D], lse_h fp32 [R,A,B,N/A,S/R])."""
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    if A * R != C:
+        raise ValueError("cp_mesh_attention_fwd: A*R must equal the number of shards")
+    S = C * s
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q_sh.device
+    if o is None:
+        o = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((R, A, B, N // A, S // R), dtype=torch.float32, device=dev)
+    need = cp_mesh_workspace_size(B, S, N, Nkv, D, A, R, prefetch, fused_merge)
+    if workspace is None:
+        workspace = torch.empty(max(256, need), dtype=torch.uint8, device=dev)
+    st = _lib.lib().cp_mesh_attention_fwd(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, S, N, Nkv, D, A, R,
+                                          float(scale), layout, _ring_flags(prefetch, fused_merge), _ptr(o),
+                                          _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    _lib.check("cp_mesh_attention_fwd", st)
+    return o, lse
+
+
 def cp_ring_attention_fwd_noalloc(q_sh, k_sh, v_sh, pos, o, lse, scale=None, layout=CP_ZIGZAG, o_dtype=CP_F32,
                                   stream=None):
     """Ring forward that allocates nothing: for callers that may not call

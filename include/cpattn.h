@@ -278,6 +278,37 @@ cp_status cp_ulysses_attention_fwd(const void *q_sh, const void *k_sh, const voi
                                    size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * cp_mesh_workspace_size / cp_mesh_attention_fwd -- A2A x P2P context-parallel
+ * attention forward on a two-dimensional mesh of C = A * R virtual ranks.
+ * [OCP] "Peer-to-peer + All-to-all": rank c belongs to A2A group c / A (ranks
+ * g*A .. g*A+A-1) and to P2P group c % A (ranks a, A+a, 2A+a, ...).  Inside
+ * each A2A group q, k, v go from sequence sharding to head sharding (N/A
+ * heads; the group's A shards concatenated in rank order, S/R positions), each
+ * P2P group runs the ring (as cp_ring_attention_fwd) over its R ranks with
+ * those concatenated positions, and the output returns to sequence sharding.
+ * A = 1 is the ring; R = 1 is Ulysses in rank order.
+ *   q_sh : device bf16 [C][B][S/C][N][D]; k_sh, v_sh : [C][B][S/C][Nkv][D]
+ *   pos  : device int32 [C][S/C], the global positions of each shard (for
+ *          example cp_zigzag_positions with C and `layout`)
+ *   A, R : A2A and P2P group sizes, 1 <= A*R <= 64; N % A == 0, Nkv % A == 0;
+ *          S % (2C) == 0 for CP_ZIGZAG, S % C == 0 for CP_CONTIGUOUS
+ *   flags: ring options (CP_RING_PREFETCH, CP_RING_FUSED_MERGE)
+ *   o_sh : device fp32 [C][B][S/C][N][D], written
+ *   lse_h: device fp32 [R][A][B][N/A][S/R], written: P2P rank g, A2A index a,
+ *          head a*N/A + h', row a'*S/C + u = query u of shard g*A + a'
+ *   workspace : device, >= cp_mesh_workspace_size bytes, 256-byte aligned
+ *          (relaid q, k, v, the fp32 head-sharded output and the ring's own
+ *          workspace)
+ * Everything is validated before anything is enqueued.
+ */
+cp_status cp_mesh_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int A, int R,
+                                 int flags, size_t *bytes);
+cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos,
+                                int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int A, int R,
+                                float scale, cp_layout layout, int flags, float *o_sh, float *lse_h,
+                                void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * cp_ring_attention_fwd_noalloc -- cp_ring_attention_fwd for callers that
  * cannot allocate device memory.  The source pages have no counterpart: this
  * entry point exists for callers that may not call cudaMalloc or cannot hand

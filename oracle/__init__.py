@@ -242,6 +242,58 @@ def ring_fwd(q_sh, k_sh, v_sh, pos, scale=None, nthreads=1):
     return o, lse
 
 
+def mesh_groups(C, A):
+    """A2A and P2P groups of the two-dimensional mesh of C = A*R ranks.
+
+    "On Context Parallelism", Peer-to-peer + All-to-all: A2A groups are runs of
+    A consecutive ranks, P2P groups take one rank of each A2A group (stride
+    A); P2P group a handles heads [a*N/A, (a+1)*N/A).
+    Returns (a2a_groups, p2p_groups), lists of rank lists.
+    """
+    if A < 1 or C % A:
+        raise ValueError("mesh_groups: A must divide C")
+    R = C // A
+    a2a = [[g * A + a for a in range(A)] for g in range(R)]
+    p2p = [[g * A + a for g in range(R)] for a in range(A)]
+    return a2a, p2p
+
+
+def mesh_fwd(q_sh, k_sh, v_sh, pos, A, scale=None, nthreads=1):
+    """A2A x P2P forward over C = A*R ranks -> (o_sh [C,B,s,N,D], lse_h [R,A,B,N/A,S/R]).
+
+    "On Context Parallelism", Peer-to-peer + All-to-all, in the order the page
+    composes it: (1) inside each A2A group, sequence-to-heads all-to-all of q,
+    k and v (rank order, N/A heads per rank, S/R positions); (2) the positions
+    of the group's shards concatenated in rank order; (3) the peer-to-peer
+    ring forward of each P2P group on those tensors and positions; (4) the
+    heads-to-sequence all-to-all of the output inside each A2A group.  The
+    lse stays in the head-sharded layout of step (3).
+    """
+    q_sh, k_sh, v_sh = _f64(q_sh), _f64(k_sh), _f64(v_sh)
+    pos = _i32(pos)
+    C, B, s, N, D = q_sh.shape
+    a2a, p2p = mesh_groups(C, A)
+    R = C // A
+    # (1) per A2A group g: [A][B][A*s][N/A][D]
+    heads = [[ulysses(x[grp[0]:grp[-1] + 1], A, SEQ_TO_HEAD, RANK_ORDER) for grp in a2a] for x in (q_sh, k_sh, v_sh)]
+    # (2) positions of each A2A group's shards, concatenated in rank order
+    pos_long = np.stack([np.concatenate([pos[c] for c in grp]) for grp in a2a])
+    o_h = [None] * R
+    lse_h = np.empty((R, A, B, N // A, A * s))
+    for a in range(A):
+        # (3) ring over P2P group a: ring rank g holds A2A index a of group g
+        qr, kr, vr = (np.stack([heads[t][g][a] for g in range(R)]) for t in range(3))
+        o_r, l_r = ring_fwd(qr, kr, vr, pos_long, scale=scale, nthreads=nthreads)
+        for g in range(R):
+            if o_h[g] is None:
+                o_h[g] = np.empty((A,) + o_r.shape[1:])
+            o_h[g][a] = o_r[g]
+            lse_h[g, a] = l_r[g]
+    # (4) back to sequence sharding inside each A2A group
+    o_sh = np.concatenate([ulysses(o_h[g], A, HEAD_TO_SEQ, RANK_ORDER) for g in range(R)])
+    return o_sh, lse_h
+
+
 def pair_counts(pos):
     """Visible (query, key) pairs per (rank, K/V owner): int64 [C, C]."""
     pos = _i32(pos)

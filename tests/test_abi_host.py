@@ -128,3 +128,39 @@ def test_allgather_and_ulysses_validation(cplib):
     bad = list(uargs)
     bad[6] = 1                                          # Nkv % C
     assert ul(*bad, FAKE, 1 << 40, None) == 3
+
+
+def test_mesh_validation(cplib):
+    n = ctypes.c_size_t(0)
+    # B, S, N, Nkv, D, A, R, flags
+    assert cplib.cp_mesh_workspace_size(1, 1024, 8, 8, 64, 2, 2, 1, ctypes.byref(n)) == 0 and n.value > 0
+    need = n.value
+    assert cplib.cp_mesh_workspace_size(1, 1024, 7, 7, 64, 2, 2, 0, ctypes.byref(n)) == 3   # N % A
+    assert cplib.cp_mesh_workspace_size(1, 1024, 8, 8, 64, 2, 2, 4, ctypes.byref(n)) == 10  # unknown flag
+    mesh = cplib.cp_mesh_attention_fwd
+    # q, k, v, pos, B, S, N, Nkv, D, A, R, scale, layout, flags, o, lse
+    args = [FAKE, FAKE, FAKE, FAKE, 1, 1024, 8, 8, 64, 2, 2, 0.125, 0, 1, FAKE, FAKE]
+    assert mesh(*args, NULL, 0, None) == 6
+    assert mesh(*args, FAKE, need - 1, None) == 6
+    assert mesh(*args, MISALIGNED, need, None) == 5
+    bad = list(args)
+    bad[6], bad[7] = 5, 5                               # N % A
+    assert mesh(*bad, FAKE, 1 << 40, None) == 3
+    bad = list(args)
+    bad[7] = 3                                          # Nkv % A
+    assert mesh(*bad, FAKE, 1 << 40, None) == 3
+    bad = list(args)
+    bad[5] = 1004                                       # S % 2C
+    assert mesh(*bad, FAKE, 1 << 40, None) == 3
+    bad = list(args)
+    bad[9], bad[10] = 8, 16                             # A*R > 64
+    assert mesh(*bad, FAKE, 1 << 40, None) == 2
+    bad = list(args)
+    bad[8] = 96                                         # D
+    assert mesh(*bad, FAKE, 1 << 40, None) == 7
+    bad = list(args)
+    bad[13] = 8                                         # flags
+    assert mesh(*bad, FAKE, 1 << 40, None) == 10
+    bad = list(args)
+    bad[3] = NULL
+    assert mesh(*bad, FAKE, need, None) == 1

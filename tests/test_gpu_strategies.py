@@ -69,3 +69,34 @@ def test_ulysses_vs_oracle_and_ring(cuda_dev, name, w, layout):
     l_glob = f64(l_h).transpose(1, 0, 2, 3).reshape(B, C * nh, S)
     assert np.max(np.abs(l_glob - l_ref)) <= ATOL_LSE
     assert torch.max(torch.abs(o_ul - o_rg)).item() <= CROSS
+
+
+MESH_CASES = [
+    ("c4_a2r2_zigzag", SY.Workload("m1", B=2, S=1024, N=8, Nkv=8, D=64, C=4), 2, "zigzag"),
+    ("c8_a2r4_zigzag", SY.Workload("m2", B=1, S=2048, N=4, Nkv=4, D=128, C=8), 2, "zigzag"),
+    ("c8_a4r2_contig", SY.Workload("m3", B=1, S=2048, N=8, Nkv=8, D=64, C=8, layout="contiguous"), 4,
+     "contiguous"),
+    ("c4_a4r1_zigzag", SY.Workload("m4", B=1, S=1024, N=4, Nkv=4, D=64, C=4), 4, "zigzag"),
+    ("c4_a1r4_gqa", SY.Workload("m5", B=1, S=1024, N=8, Nkv=4, D=64, C=4), 1, "zigzag"),
+]
+
+
+@pytest.mark.parametrize("name,w,A,layout", MESH_CASES, ids=[c[0] for c in MESH_CASES])
+def test_mesh_vs_oracle_and_ring(cuda_dev, name, w, A, layout):
+    """A2A x P2P mesh against the oracle's mesh composition (o and the
+    head-sharded lse, element by element) and against the plain ring."""
+    R = w.C // A
+    q, k, v, _ = SY.make_qkv(w)
+    lay = F.CP_ZIGZAG if layout == "zigzag" else F.CP_CONTIGUOUS
+    lay_o = O.ZIGZAG if layout == "zigzag" else O.CONTIGUOUS
+    qs, ks, vs = (F.cp_zigzag_shard(t.to(cuda_dev), w.C, lay) for t in (q, k, v))
+    pos = F.cp_zigzag_positions(w.S, w.C, lay, device=cuda_dev)
+    o_ref, l_ref = O.mesh_fwd(*(O.shard(f64(t), w.C, lay_o) for t in (q, k, v)), pos.cpu().numpy(), A,
+                              nthreads=NTH)
+    for prefetch in (0, 1):
+        o_m, l_m = F.cp_mesh_attention_fwd(qs, ks, vs, pos, A, R, layout=lay, prefetch=prefetch)
+        torch.cuda.synchronize()
+        assert np.max(np.abs(f64(o_m) - o_ref)) <= ATOL_O, prefetch
+        assert np.max(np.abs(f64(l_m) - l_ref)) <= ATOL_LSE, prefetch
+    o_rg, _ = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay)
+    assert torch.max(torch.abs(o_m - o_rg)).item() <= CROSS

@@ -452,3 +452,81 @@ def test_ring_equals_direct(C, layout):
     for r in range(C):
         l_glob[:, :, pos[r]] = l_sh[r]
     np.testing.assert_allclose(l_glob, l_ref, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# A2A x P2P mesh
+# --------------------------------------------------------------------------
+def test_mesh_groups_c8_a2_from_the_page():
+    g = read("mesh_groups_c8.txt")
+    C, A, R = int(g["C"]), int(g["A"]), int(g["R"])
+    a2a, p2p = O.mesh_groups(C, A)
+    assert len(a2a) == R and len(p2p) == A
+    for i in range(R):
+        assert a2a[i] == ints(g["a2a_group_%d" % i])
+    for a in range(A):
+        assert p2p[a] == ints(g["p2p_group_%d" % a])
+
+
+def test_mesh_head_groups_and_shapes_from_the_page():
+    """P2P group a of the C=8, A=2, R=4 example handles heads [a N/2, (a+1) N/2):
+    with q carrying its head index and k = 1, every visible score of head h is
+    scale*h, so lse - log(#visible) reads the head back out of lse_h."""
+    g = read("mesh_groups_c8.txt")
+    C, A = int(g["C"]), int(g["A"])
+    R = C // A
+    B, N, D, t = 1, 4, 4, 1
+    S = 2 * C * t
+    s = S // C
+    q = np.zeros((B, S, N, D))
+    q[:, :, :, 0] = np.arange(N)[None, None, :]
+    k = np.zeros((B, S, N, D))
+    k[..., 0] = 1.0
+    v = randn(B, S, N, D)
+    pos = O.positions(S, C, O.ZIGZAG)
+    _, lse_h = O.mesh_fwd(O.shard(q, C), O.shard(k, C), O.shard(v, C), pos, A)
+    assert lse_h.shape == (R, A, B, N // A, S // R)  # each rank: S/R positions, N/A heads, as printed
+    scale = 1.0 / np.sqrt(D)
+    for a in range(A):
+        lo, hi = (int(x) * N // 2 for x in ints(g["p2p_group_%d_heads_halves" % a]))
+        for gg in range(R):
+            for ap in range(A):
+                count = pos[gg * A + ap] + 1.0  # keys at positions 0..p
+                got = lse_h[gg, a, 0, :, ap * s:(ap + 1) * s] - np.log(count)[None, :]
+                want = scale * np.arange(lo, hi, dtype=np.float64)[:, None] * np.ones((1, s))
+                np.testing.assert_allclose(got, want, atol=1e-12)
+
+
+@pytest.mark.parametrize("C,A", [(4, 1), (4, 2), (4, 4), (8, 2), (8, 4)])
+@pytest.mark.parametrize("layout", [O.ZIGZAG, O.CONTIGUOUS])
+def test_mesh_equals_direct(C, A, layout):
+    """Whatever the mesh shape, the result is causal attention over the whole
+    sequence: o by global position, lse mapped from the head-sharded layout."""
+    R = C // A
+    B, N, D, t = 2, 8, 8, 3
+    S = 2 * C * t
+    s = S // C
+    q, k, v = randn(B, S, N, D), randn(B, S, N, D), randn(B, S, N, D)
+    gp = _arange_pos(S)
+    o_ref, l_ref = O.attn_direct(q, k, v, gp, gp)
+    pos = O.positions(S, C, layout)
+    o_sh, lse_h = O.mesh_fwd(O.shard(q, C, layout), O.shard(k, C, layout), O.shard(v, C, layout), pos, A)
+    np.testing.assert_allclose(O.unshard(o_sh, layout), o_ref, atol=1e-13)
+    nh = N // A
+    for g in range(R):
+        for a in range(A):
+            for ap in range(A):
+                rows = pos[g * A + ap]
+                got = lse_h[g, a, :, :, ap * s:(ap + 1) * s]
+                np.testing.assert_allclose(got, l_ref[:, a * nh:(a + 1) * nh, rows], atol=1e-13)
+
+
+def test_mesh_with_a1_is_the_ring():
+    C, B, N, D, t = 4, 1, 2, 8, 4
+    S = 2 * C * t
+    q, k, v = (O.shard(randn(B, S, N, D), C) for _ in range(3))
+    pos = O.positions(S, C)
+    o_m, l_m = O.mesh_fwd(q, k, v, pos, 1)
+    o_r, l_r = O.ring_fwd(q, k, v, pos)
+    np.testing.assert_array_equal(o_m, o_r)
+    np.testing.assert_array_equal(l_m[:, 0], l_r)
