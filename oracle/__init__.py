@@ -43,6 +43,8 @@ def _load():
         lib.orc_ulysses.argtypes = [vp, vp, L, L, L, L, I, L, I, I]
         lib.orc_ring_fwd.argtypes = [dp, dp, dp, ip, L, L, L, L, L, I, Dd, dp, dp, I]
         lib.orc_pair_counts.argtypes = [ip, L, I, vp]
+        lib.orc_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ip, ip, L, L, L, L, L, L, Dd, dp, dp, dp, I]
+        lib.orc_ring_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ip, L, L, L, L, L, I, Dd, dp, dp, dp, I]
         _lib = lib
     return _lib
 
@@ -292,6 +294,48 @@ def mesh_fwd(q_sh, k_sh, v_sh, pos, A, scale=None, nthreads=1):
     # (4) back to sequence sharding inside each A2A group
     o_sh = np.concatenate([ulysses(o_h[g], A, HEAD_TO_SEQ, RANK_ORDER) for g in range(R)])
     return o_sh, lse_h
+
+
+def attn_bwd(q, k, v, o, dout, lse, q_pos, k_pos, scale=None, nthreads=1):
+    """Backward of one attention tile -> (dq [B,Sq,N,D], dk, dv [B,Sk,Nkv,D]).
+
+    "On Context Parallelism", Peer-to-peer / Backward (attention_tile_backward
+    with the final output and lse); the chain rule of the forward definition.
+    """
+    q, k, v, o, dout, lse = (_f64(x) for x in (q, k, v, o, dout, lse))
+    q_pos, k_pos = _i32(q_pos), _i32(k_pos)
+    B, Sq, N, D = q.shape
+    Sk, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    if _load().orc_attn_bwd(_p(q), _p(k), _p(v), _p(o), _p(dout), _p(lse), _p(q_pos), _p(k_pos), B, Sq, Sk, N, Nkv,
+                            D, float(scale), _p(dq), _p(dk), _p(dv), int(nthreads)):
+        raise ValueError("attn_bwd: N must be a multiple of Nkv")
+    return dq, dk, dv
+
+
+def ring_bwd(q_sh, k_sh, v_sh, o_sh, do_sh, lse_sh, pos, scale=None, nthreads=1):
+    """Ring backward over C virtual ranks -> (dq_sh, dk_sh, dv_sh), rank-major shards.
+
+    "On Context Parallelism", Peer-to-peer / Backward.
+    """
+    q_sh, k_sh, v_sh, o_sh, do_sh, lse_sh = (_f64(x) for x in (q_sh, k_sh, v_sh, o_sh, do_sh, lse_sh))
+    pos = _i32(pos)
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    dq = np.empty_like(q_sh)
+    dk = np.empty_like(k_sh)
+    dv = np.empty_like(v_sh)
+    rc = _load().orc_ring_bwd(_p(q_sh), _p(k_sh), _p(v_sh), _p(o_sh), _p(do_sh), _p(lse_sh), _p(pos), B, C * s, N,
+                              Nkv, D, C, float(scale), _p(dq), _p(dk), _p(dv), int(nthreads))
+    if rc:
+        raise ValueError("ring_bwd: bad arguments (%d)" % rc)
+    return dq, dk, dv
 
 
 def pair_counts(pos):

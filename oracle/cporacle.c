@@ -10,8 +10,9 @@
  *
  * Every function below follows a passage of the source pages; the passage is
  * named in the comment above it.  Page titles used:
- *   [OCP]  "On Context Parallelism"  (sections: All-gather, All-to-all,
- *          Peer-to-peer / Forward, Results and Conclusion)
+ *   [OCP]  "On Context Parallelism"  (sections: All-gather (Forward,
+ *          Backward), All-to-all, Peer-to-peer (Forward, Backward),
+ *          Results and Conclusion)
  *   [DAY74] "Context parallelism -- splitting the sequence across GPUs"
  *          (sections: Why long contexts stress training memory, What exactly
  *          gets sharded?, How do partial softmax results combine?)
@@ -487,6 +488,141 @@ int orc_ring_fwd(const double *q_sh, const double *k_sh, const double *v_sh, con
     free(o_t);
     free(l_t);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward of one attention tile.                                          */
+/*                                                                          */
+/* [OCP] Peer-to-peer / Backward: attention_tile_backward(q, k, v, output,  */
+/* grad_output, lse, q_positions, kv_positions, scale) returns the tile's   */
+/* (dq, dk, dv); the call receives the FINAL output and lse of the whole    */
+/* attention, so within a tile the probability of a visible pair is the     */
+/* global one, p_ij = e^{s_ij - lse_i}.  The pages print no formula for it; */
+/* it is the derivative of o_i = sum_j p_ij v_j with s_ij = scale <q_i,k_j> */
+/* written out by the chain rule (READING: the plain definition):           */
+/*   dv_j += p_ij dO_i                                                      */
+/*   dp_ij = <dO_i, v_j>                                                    */
+/*   ds_ij = p_ij (dp_ij - delta_i),  delta_i = sum_j' p_ij' dp_ij'         */
+/*                                          = <dO_i, o_i>                   */
+/*   dq_i += scale ds_ij k_j,   dk_j += scale ds_ij q_i                     */
+/* (delta_i is taken as <dO_i, o_i> with the given output; over the whole   */
+/* key set it equals the sum over j, which a pin checks.)                   */
+/* Rows with lse = -inf see no key and contribute nothing.  With            */
+/* N > Nkv the gradients of a KV head sum over its query heads.             */
+/* Inputs as orc_attn_direct plus o, dO [B][Sq][N][D], lse [B][N][Sq];      */
+/* outputs dq [B][Sq][N][D], dk, dv [B][Sk][Nkv][D] (overwritten).          */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const double *q, *k, *v, *o, *dout, *lse;
+    const int32_t *qpos, *kpos;
+    long B, Sq, Sk, N, Nkv, D;
+    double scale;
+    double *dq, *dk, *dv;
+} orc_bwd_job;
+
+static void orc_bwd_unit(void *arg, long unit) {
+    /* one unit = one (b, kv head) with all its query heads: no two units
+       write the same dq, dk or dv element */
+    const orc_bwd_job *J = (const orc_bwd_job *)arg;
+    const long D = J->D, N = J->N, Nkv = J->Nkv, g = N / Nkv;
+    const long b = unit / Nkv, hk = unit % Nkv;
+    for (long j = 0; j < J->Sk; ++j)
+        for (long d = 0; d < D; ++d) {
+            J->dk[((b * J->Sk + j) * Nkv + hk) * D + d] = 0.0;
+            J->dv[((b * J->Sk + j) * Nkv + hk) * D + d] = 0.0;
+        }
+    for (long h = hk * g; h < (hk + 1) * g; ++h)
+        for (long i = 0; i < J->Sq; ++i) {
+            const double *qi = J->q + ((b * J->Sq + i) * N + h) * D;
+            const double *oi = J->o + ((b * J->Sq + i) * N + h) * D;
+            const double *doi = J->dout + ((b * J->Sq + i) * N + h) * D;
+            double *dqi = J->dq + ((b * J->Sq + i) * N + h) * D;
+            for (long d = 0; d < D; ++d) dqi[d] = 0.0;
+            const double lse = J->lse[(b * N + h) * J->Sq + i];
+            if (lse == ORC_NEG_INF) continue;
+            double delta = 0.0;
+            for (long d = 0; d < D; ++d) delta += doi[d] * oi[d];
+            for (long j = 0; j < J->Sk; ++j) {
+                if (J->kpos[j] > J->qpos[i]) continue;
+                const double *kj = J->k + ((b * J->Sk + j) * Nkv + hk) * D;
+                const double *vj = J->v + ((b * J->Sk + j) * Nkv + hk) * D;
+                double *dkj = J->dk + ((b * J->Sk + j) * Nkv + hk) * D;
+                double *dvj = J->dv + ((b * J->Sk + j) * Nkv + hk) * D;
+                double dot = 0.0, dp = 0.0;
+                for (long d = 0; d < D; ++d) {
+                    dot += qi[d] * kj[d];
+                    dp += doi[d] * vj[d];
+                }
+                const double p = exp(J->scale * dot - lse);
+                const double ds = p * (dp - delta);
+                for (long d = 0; d < D; ++d) {
+                    dvj[d] += p * doi[d];
+                    dqi[d] += J->scale * ds * kj[d];
+                    dkj[d] += J->scale * ds * qi[d];
+                }
+            }
+        }
+}
+
+int orc_attn_bwd(const double *q, const double *k, const double *v, const double *o, const double *dout,
+                 const double *lse, const int32_t *qpos, const int32_t *kpos, long B, long Sq, long Sk, long N,
+                 long Nkv, long D, double scale, double *dq, double *dk, double *dv, int nthreads) {
+    if (N <= 0 || Nkv <= 0 || N % Nkv != 0) return 1;
+    orc_bwd_job J = {q, k, v, o, dout, lse, qpos, kpos, B, Sq, Sk, N, Nkv, D, scale, dq, dk, dv};
+    orc_parallel(orc_bwd_unit, &J, B * Nkv, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Ring backward over C virtual ranks.                                      */
+/*                                                                          */
+/* [OCP] Peer-to-peer / Backward: rank r keeps its queries and accumulates  */
+/* dq locally; at step `step` it holds the K/V block of                     */
+/* kv_owner = (r - step) mod C together with that block's travelling dk/dv  */
+/* accumulators, adds the tile's (dk, dv) to them, and passes all four on;  */
+/* after the full rotation each block's accumulated dk/dv is back on its    */
+/* owner.  Without transport the travelling accumulator of block j is the   */
+/* owner's own dk_sh[j] / dv_sh[j].  The tile backward gets the final       */
+/* output and lse of rank r (saved by the forward).                         */
+/* Shards as orc_ring_fwd; o_sh, do_sh [C][B][s][N][D], lse_sh [C][B][N][s]; */
+/* outputs dq_sh [C][B][s][N][D], dk_sh, dv_sh [C][B][s][Nkv][D].           */
+/* ------------------------------------------------------------------------ */
+int orc_ring_bwd(const double *q_sh, const double *k_sh, const double *v_sh, const double *o_sh,
+                 const double *do_sh, const double *lse_sh, const int32_t *pos, long B, long S, long N, long Nkv,
+                 long D, int C, double scale, double *dq_sh, double *dk_sh, double *dv_sh, int nthreads) {
+    if (C <= 0 || S % C != 0) return 1;
+    const long s = S / C;
+    const long qn = B * s * N * D, kn = B * s * Nkv * D, ln = B * N * s;
+    double *tq = (double *)malloc(sizeof(double) * (size_t)qn);
+    double *tk = (double *)malloc(sizeof(double) * (size_t)kn);
+    double *tv = (double *)malloc(sizeof(double) * (size_t)kn);
+    if (!tq || !tk || !tv) {
+        free(tq);
+        free(tk);
+        free(tv);
+        return 3;
+    }
+    memset(dq_sh, 0, sizeof(double) * (size_t)(C * qn));
+    memset(dk_sh, 0, sizeof(double) * (size_t)(C * kn));
+    memset(dv_sh, 0, sizeof(double) * (size_t)(C * kn));
+    int rc = 0;
+    for (int r = 0; r < C && !rc; ++r)
+        for (int step = 0; step < C && !rc; ++step) {
+            const int owner = ((r - step) % C + C) % C;
+            rc = orc_attn_bwd(q_sh + (long)r * qn, k_sh + (long)owner * kn, v_sh + (long)owner * kn,
+                              o_sh + (long)r * qn, do_sh + (long)r * qn, lse_sh + (long)r * ln, pos + (long)r * s,
+                              pos + (long)owner * s, B, s, s, N, Nkv, D, scale, tq, tk, tv, nthreads);
+            if (rc) break;
+            for (long x = 0; x < qn; ++x) dq_sh[(long)r * qn + x] += tq[x];
+            for (long x = 0; x < kn; ++x) {
+                dk_sh[(long)owner * kn + x] += tk[x];
+                dv_sh[(long)owner * kn + x] += tv[x];
+            }
+        }
+    free(tq);
+    free(tk);
+    free(tv);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */

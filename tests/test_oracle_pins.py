@@ -530,3 +530,102 @@ def test_mesh_with_a1_is_the_ring():
     o_r, l_r = O.ring_fwd(q, k, v, pos)
     np.testing.assert_array_equal(o_m, o_r)
     np.testing.assert_array_equal(l_m[:, 0], l_r)
+
+
+# --------------------------------------------------------------------------
+# backward
+# --------------------------------------------------------------------------
+def _loss_and_grads(q, k, v, dout, qp, kp, scale):
+    """sum(dO * o) and the oracle's gradients of it (o, lse from the forward)."""
+    o, lse = O.attn_direct(q, k, v, qp, kp, scale=scale)
+    dq, dk, dv = O.attn_bwd(q, k, v, o, dout, lse, qp, kp, scale=scale)
+    return float(np.sum(dout * o)), (dq, dk, dv)
+
+
+@pytest.mark.parametrize("Nkv", [2, 1])
+def test_bwd_matches_central_differences_of_the_forward(Nkv):
+    """Every gradient entry against a central difference of the oracle's
+    FORWARD (sum(dO * o)): independent of the backward's chain rule."""
+    B, Sq, Sk, N, D = 1, 5, 6, 2, 3
+    q, k, v = randn(B, Sq, N, D), randn(B, Sk, Nkv, D), randn(B, Sk, Nkv, D)
+    dout = randn(B, Sq, N, D)
+    qp = np.array([3, 0, 5, 2, 7], dtype=np.int32)    # unsorted, one row sees every key
+    kp = np.array([1, 0, 4, 2, 6, 3], dtype=np.int32)
+    scale = 0.7
+    _, grads = _loss_and_grads(q, k, v, dout, qp, kp, scale)
+    h = 1e-5
+    for x, g in zip((q, k, v), grads):
+        num = np.empty_like(x)
+        for idx in np.ndindex(*x.shape):
+            keep = x[idx]
+            x[idx] = keep + h
+            lp = float(np.sum(dout * O.attn_direct(q, k, v, qp, kp, scale=scale)[0]))
+            x[idx] = keep - h
+            lm = float(np.sum(dout * O.attn_direct(q, k, v, qp, kp, scale=scale)[0]))
+            x[idx] = keep
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, num, atol=1e-8, rtol=1e-7)
+
+
+def test_bwd_matches_torch_autograd_fp64():
+    B, S, N, D = 2, 9, 2, 4
+    q, k, v, dout = randn(B, S, N, D), randn(B, S, N, D), randn(B, S, N, D), randn(B, S, N, D)
+    gp = _arange_pos(S)
+    o, lse = O.attn_direct(q, k, v, gp, gp)
+    dq, dk, dv = O.attn_bwd(q, k, v, o, dout, lse, gp, gp)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    sc = torch.einsum("bind,bjnd->bnij", tq, tk) / np.sqrt(D)
+    sc = sc.masked_fill(torch.triu(torch.ones(S, S, dtype=torch.bool), 1), float("-inf"))
+    out = torch.einsum("bnij,bjnd->bind", torch.softmax(sc, -1), tv)
+    out.backward(torch.tensor(dout))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
+def test_bwd_single_visible_key_and_empty_rows():
+    """A row that sees one key has p = 1: dv of that key gets dO, dq = dk = 0
+    (ds = dp - delta = 0).  A row that sees nothing contributes nothing."""
+    B, N, D = 1, 1, 3
+    q, k, v = randn(B, 2, N, D), randn(B, 1, N, D), randn(B, 1, N, D)
+    dout = randn(B, 2, N, D)
+    qp, kp = np.array([5, 1], dtype=np.int32), np.array([4], dtype=np.int32)
+    o, lse = O.attn_direct(q, k, v, qp, kp)
+    assert lse[0, 0, 1] == -np.inf
+    dq, dk, dv = O.attn_bwd(q, k, v, o, dout, lse, qp, kp)
+    np.testing.assert_allclose(dv[0, 0], dout[0, 0], atol=1e-15)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-15)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-15)
+
+
+def test_bwd_delta_identity_and_split_over_key_partials():
+    """Gradients split over disjoint key sets add up (the tile backward uses
+    the final o and lse), which is what lets the ring sum tile gradients."""
+    B, S, N, D = 1, 12, 2, 4
+    q, k, v, dout = randn(B, S, N, D), randn(B, S, N, D), randn(B, S, N, D), randn(B, S, N, D)
+    gp = _arange_pos(S)
+    o, lse = O.attn_direct(q, k, v, gp, gp)
+    full = O.attn_bwd(q, k, v, o, dout, lse, gp, gp)
+    idx = [np.array([0, 3, 4, 9]), np.array([1, 2, 5, 6, 7, 8, 10, 11])]
+    parts = [O.attn_bwd(q, k[:, ix], v[:, ix], o, dout, lse, gp, gp[ix]) for ix in idx]
+    np.testing.assert_allclose(parts[0][0] + parts[1][0], full[0], atol=1e-13)
+    for p, ix in zip(parts, idx):
+        np.testing.assert_allclose(p[1], full[1][:, ix], atol=1e-13)
+        np.testing.assert_allclose(p[2], full[2][:, ix], atol=1e-13)
+
+
+@pytest.mark.parametrize("C", [1, 2, 4])
+@pytest.mark.parametrize("layout", [O.ZIGZAG, O.CONTIGUOUS])
+def test_ring_bwd_equals_direct(C, layout):
+    B, N, Nkv, D, t = 1, 4, 2, 4, 3
+    S = 2 * C * t
+    q, k, v = randn(B, S, N, D), randn(B, S, Nkv, D), randn(B, S, Nkv, D)
+    dout = randn(B, S, N, D)
+    gp = _arange_pos(S)
+    o, lse = O.attn_direct(q, k, v, gp, gp)
+    dq, dk, dv = O.attn_bwd(q, k, v, o, dout, lse, gp, gp)
+    pos = O.positions(S, C, layout)
+    o_sh, l_sh = O.ring_fwd(*(O.shard(x, C, layout) for x in (q, k, v)), pos)
+    g = O.ring_bwd(*(O.shard(x, C, layout) for x in (q, k, v)), o_sh, O.shard(dout, C, layout), l_sh, pos)
+    for got, want in zip(g, (dq, dk, dv)):
+        np.testing.assert_allclose(O.unshard(got, layout), want, atol=1e-12)
