@@ -78,6 +78,12 @@ def lib():
     L.cp_mesh_workspace_size.argtypes = [i64, i64, i64, i64, i64, i32, i32, i32, ctypes.POINTER(sz)]
     L.cp_mesh_attention_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, f32, i32, i32, vp, vp, vp,
                                         sz, vp]
+    L.cp_attn_bwd_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
+    L.cp_attn_bwd_partial.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp,
+                                      i32, vp, sz, vp]
+    L.cp_ring_bwd_workspace_size.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
+    L.cp_ring_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, vp, vp,
+                                        vp, sz, vp]
     L.cp_ring_attention_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, i32, vp,
                                                 vp]
     for name in header_symbols():

@@ -43,6 +43,7 @@
 
 #include "cp_internal.h"
 #include "cp_ptx.cuh"
+#include "cp_sched.cuh"
 
 namespace cpattn {
 
@@ -78,26 +79,6 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
-
-// Division by a runtime-invariant divisor 1 <= d < 2^31 for numerators
-// 0 <= n < 2^31 via a multiply-high: q = (n * m) >> (31 + l) with
-// l = ceil(log2 d) and m = ceil(2^(31+l) / d) < 2^32 (round-up method; the
-// error m*d - 2^(31+l) < d keeps the quotient exact for n < 2^31).
-struct FastDiv {
-    uint32_t d, m, sh;
-};
-inline FastDiv make_fastdiv(uint32_t d) {
-    FastDiv f;
-    f.d = d;
-    uint32_t l = 0;
-    while ((1ull << l) < d) ++l;
-    f.sh = 31 + l;
-    f.m = static_cast<uint32_t>(((1ull << f.sh) + d - 1) / d);
-    return f;
-}
-__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
-    return static_cast<uint32_t>((static_cast<uint64_t>(n) * f.m) >> f.sh);
-}
 
 struct AttnArgs {
     const int32_t *q_pos;
@@ -164,17 +145,6 @@ __device__ __forceinline__ Item decode_item(int idx, const AttnArgs &a, const in
     if (qt1 < a.nqt) qmax = max(qmax, qtab[it.r * a.nqt + qt1].y);
     it.qmax = qmax;
     return it;
-}
-
-// Work item of this CTA in round k of the persistent schedule: items are
-// sorted longest first and dealt out boustrophedon (even rounds CTA 0..G-1,
-// odd rounds G-1..0), so one CTA's long and short items pair up.  Returns -1
-// past the end.
-__device__ __forceinline__ int item_of_round(int k, int n_items) {
-    const int G = gridDim.x;
-    const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x))
-                                                                     : static_cast<int>(blockIdx.x));
-    return idx < n_items ? static_cast<int>(idx) : -1;
 }
 
 // Next key tile >= kt that this block must process (nkt if none).
@@ -642,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int j = 0;
             for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
                  kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt), ++j) {
-                if (!mbar_wait(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                if (!mbar_wait_warp(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
                 if (a.merge_into && row_valid && j == n_item - 1) {
                     // the epilogue will read this row of the accumulator: start it towards L2
@@ -742,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            if (!mbar_wait(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+            if (!mbar_wait_warp(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
             tc_fence_after();
             const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
             const float lse_t = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
@@ -824,7 +794,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && *abort_flag) atomicExch(&g_cp_device_status, static_cast<int>(CP_ERR_DEVICE_TIMEOUT));
 }
 
+}  // namespace
+
 // ------------------------------------------------------------ host side
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -838,16 +811,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     });
     return fn;
 }
+}  // namespace
 
-// 4-D bf16 map over [outer][rows][heads][D], box = 64 columns x 1 head x 128 rows x 1.
-bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int64_t rows, int64_t outer) {
+bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int64_t rows, int64_t outer,
+              int box_rows) {
     auto enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(outer)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(heads * D * 2),
                              static_cast<cuuint64_t>(rows * heads * D * 2)};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -855,13 +829,28 @@ bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int6
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_f32_rows(CUtensorMap *map, const float *base, int64_t cols, int64_t rows, int box_cols) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 4)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
 template <int D>
 cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     using K = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const int64_t kv_outer = p.kv_shared ? p.B : p.C * p.B;
-    if (!make_map(&mq, p.q, D, p.N, p.Sq, p.C * p.B) || !make_map(&mk, p.k, D, p.Nkv, p.Sk, kv_outer) ||
-        !make_map(&mv, p.v, D, p.Nkv, p.Sk, kv_outer))
+    if (!make_map(&mq, p.q, D, p.N, p.Sq, p.C * p.B, 128) || !make_map(&mk, p.k, D, p.Nkv, p.Sk, kv_outer, 128) ||
+        !make_map(&mv, p.v, D, p.Nkv, p.Sk, kv_outer, 128))
         return CP_ERR_CUDA;
     AttnArgs a;
     a.q_pos = p.q_pos;
@@ -977,12 +966,15 @@ extern "C" cp_status cp_attn_partial(const void *q, const void *k, const void *v
 extern "C" cp_status cp_device_status(int *code, int clear, cudaStream_t stream) {
     if (!code) return CP_ERR_NULL;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return CP_ERR_CUDA;
-    int v = 0;
+    int v = 0, vb = 0;
     if (cudaMemcpyFromSymbol(&v, cpattn::g_cp_device_status, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
-    *code = v;
     if (clear) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(cpattn::g_cp_device_status, &zero, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
     }
+    // the backward kernels keep their own word (another translation unit)
+    const cp_status st = cpattn::read_bwd_device_status(&vb, clear != 0);
+    if (st != CP_OK) return st;
+    *code = v != 0 ? v : vb;
     return CP_OK;
 }

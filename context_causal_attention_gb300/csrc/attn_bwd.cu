@@ -1,0 +1,1206 @@
+// attn_bwd.cu -- backward of the partial causal attention with explicit
+// positions on the sm_103a tensor cores (tcgen05 + TMEM + TMA), and the ring
+// backward over C virtual ranks built from it.
+//
+// What it computes ("On Context Parallelism", Peer-to-peer / Backward: the
+// tile backward attention_tile_backward(q, k, v, output, grad_output, lse,
+// q_positions, kv_positions, scale) -> (dq, dk, dv), which receives the FINAL
+// output and lse of the whole attention): over the visible pairs
+// (k_pos[j] <= q_pos[i]) with p_ij = e^{scale <q_i, k_j> - lse_i},
+//   dv_j = sum_i p_ij dO_i,   dp_ij = <dO_i, v_j>,
+//   ds_ij = p_ij (dp_ij - delta_i),   delta_i = <dO_i, o_i>,
+//   dq_i = scale sum_j ds_ij k_j,     dk_j = scale sum_i ds_ij q_i
+// (the chain rule of the forward; with N > Nkv a KV head's gradients sum over
+// its query heads).
+//
+// Three kernels:
+//   bwd_stats_kernel  per query row: nl2 = -lse log2(e) (-inf for rows that see
+//                     nothing and for padding) and nd = -delta; HBM-bound.
+//   bwd_dkdv_kernel   K/V-stationary.  Work item = (rank, b, KV head, 128-key
+//                     tile); it streams the 64-row Q / dO tiles (of every query
+//                     head of the group) that can see the keys and keeps
+//                     dV += P^T dO and dK += dS^T Q in TMEM.
+//   bwd_dq_kernel     Q-stationary.  Work item = (rank, b, head, 128-query tile);
+//                     it streams the 64-key K / V tiles the queries can see and
+//                     keeps dQ += dS K in TMEM.
+// S and dP are formed in both (seven 128x64xD-class products per tile pair
+// instead of five), in exchange for no atomics and deterministic sums.
+//
+// Both kernels: one persistent CTA per SM, 192 threads.
+//   warp 0      TMA producer (stationary tiles once per item, a 3-stage ring
+//               of streamed tiles);
+//   warp 1      TMEM allocator (512 columns) and the single MMA-issuing thread;
+//   warps 2-5   compute: one thread per TMEM lane (row of the stationary
+//               tile); TMEM lane quarter = warp % 4.
+// TMEM: two buffers b = 0, 1 of 128 columns (scores 64 | dP 64, each a
+// 128 x 64 fp32 block; P / dS are written back over them as packed bf16) and
+// the fp32 accumulators from column 256 (dV | dK, or dQ).  The MMA for
+// streamed tile t + 1 runs while the compute warps work on tile t.
+// Every mbarrier wait is bounded (2 s); a CTA that times out unwinds, lets its
+// copies and MMAs land, frees TMEM and records CP_ERR_DEVICE_TIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "cp_internal.h"
+#include "cp_ptx.cuh"
+#include "cp_sched.cuh"
+
+namespace cpattn {
+namespace {
+
+__device__ int g_cp_bwd_status = 0;
+
+constexpr int kBThreads = 192;
+constexpr int kBStages = 3;
+constexpr uint32_t kBTmemCols = 512;
+constexpr uint32_t kNegInfBits = 0xff800000u;
+
+template <int D>
+struct Tiles {
+    static constexpr int kAtoms = D / 64;
+    static constexpr int kBig = 128 * D * 2;    // 128-row bf16 tile
+    static constexpr int kSmall = 64 * D * 2;   // 64-row bf16 tile
+    static constexpr int kAtomBig = 128 * 128;  // one 64-column swizzle atom of a 128-row tile
+    static constexpr int kAtomSmall = 64 * 128; // ... of a 64-row tile
+};
+
+// K/V-stationary kernel: K, V (128 rows) | Q, dO stages (64 rows) | nl2/nd
+// strips per stage | tables | order | cost | barriers | misc.
+template <int D>
+struct CfgKV : Tiles<D> {
+    using T = Tiles<D>;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = T::kBig;
+    static constexpr int kOffQ = 2 * T::kBig;
+    static constexpr int kOffDO = kOffQ + kBStages * T::kSmall;
+    static constexpr int kOffStat = kOffDO + kBStages * T::kSmall;  // per stage: nl2[64] | nd[64]
+    static constexpr int kOffTab = kOffStat + kBStages * 512;
+    static constexpr int kOffOrder = kOffTab + kBwdMaxTables * 8;
+    static constexpr int kOffCost = kOffOrder + kBwdMaxPairs * 4;
+    static constexpr int kOffBar = kOffCost + kBwdMaxPairs * 4;
+    // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full[2], p_full[2], o_full, o_empty, drain
+    static constexpr int kNumBars = 2 + 2 * kBStages + 7;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kMiscBytes = 16 + kMaxC * 4 + kBwdMaxTables / 8;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Q-stationary kernel: Q, dO (128 rows) | K, V stages (64 rows) | tables | ...
+template <int D>
+struct CfgQ : Tiles<D> {
+    using T = Tiles<D>;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffDO = T::kBig;
+    static constexpr int kOffK = 2 * T::kBig;
+    static constexpr int kOffV = kOffK + kBStages * T::kSmall;
+    static constexpr int kOffTab = kOffV + kBStages * T::kSmall;
+    static constexpr int kOffOrder = kOffTab + kBwdMaxTables * 8;
+    static constexpr int kOffCost = kOffOrder + kBwdMaxPairs * 4;
+    static constexpr int kOffBar = kOffCost + kBwdMaxPairs * 4;
+    // qd_full, qd_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full, o_empty, drain
+    static constexpr int kNumBars = 2 + 2 * kBStages + 7;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kMiscBytes = 16 + kMaxC * 4 + kBwdMaxTables / 8;
+    static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct BwdArgs {
+    const int32_t *q_pos, *k_pos;
+    long long q_pos_stride, k_pos_stride;
+    const float *nl2, *nd;  // [C*B*N][sq_pad]
+    long long sq_pad;
+    float *dq, *dk, *dv;
+    int C, B, N, Nkv, Sq, Sk;
+    int nq, nk;  // query / key tiles in the kernel's own tile heights
+    int kv_shift, kpos_shift, kpr;
+    int accumulate;
+    float scale, scale_log2;
+    unsigned long long timeout_ns;
+    FastDiv div_bh, div_nt, div_h;  // by B * (heads per item), stationary tiles per rank, heads per item
+};
+
+// (min, max) of the positions of one tile of T rows (one warp per tile); when
+// `arith` is given, bit g is set if the positions are p, p+1, p+2, ...
+template <int T>
+__device__ __forceinline__ void tile_table(const int32_t *p, int row0, int lim, int lane, int2 *out, uint32_t *arith,
+                                           int g) {
+    constexpr int kPer = T / 32;
+    int mn = INT_MAX, mx = INT_MIN, vals[kPer];
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+        const int row = row0 + lane + 32 * m;
+        vals[m] = (row < lim) ? __ldg(p + row) : 0;
+        if (row < lim) {
+            mn = min(mn, vals[m]);
+            mx = max(mx, vals[m]);
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) *out = make_int2(mn, mx);
+    if (arith) {
+        const int first = __shfl_sync(0xffffffffu, vals[0], 0);
+        bool ok = true;
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+            const int row = row0 + lane + 32 * m;
+            if (row < lim) ok &= (static_cast<long long>(vals[m]) == static_cast<long long>(first) + lane + 32 * m);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0 && ok) atomicOr(arith + (g >> 5), 1u << (g & 31));
+    }
+}
+
+// ---- visibility of streamed tiles
+// K/V-stationary: query tile qt (of rank r) can see key tile (kmin = its
+// smallest key position) iff its largest query position >= kmin.  With the
+// tiles' largest positions non-decreasing (`sorted`) the visible tiles are a
+// suffix found by bisection.
+__device__ __forceinline__ int first_q(const int2 *qt_r, int nq, int kmin, bool sorted) {
+    if (sorted) {
+        int lo = 0, hi = nq;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (qt_r[mid].y >= kmin) hi = mid; else lo = mid + 1;
+        }
+        return lo;
+    }
+    int qt = 0;
+    while (qt < nq && qt_r[qt].y < kmin) ++qt;
+    return qt;
+}
+__device__ __forceinline__ int next_q(int qt, const int2 *qt_r, int nq, int kmin) {
+    while (qt < nq && qt_r[qt].y < kmin) ++qt;
+    return qt;
+}
+__device__ __forceinline__ int count_q(const int2 *qt_r, int nq, int kmin, bool sorted) {
+    if (sorted) return nq - first_q(qt_r, nq, kmin, true);
+    int c = 0;
+    for (int qt = 0; qt < nq; ++qt) c += (qt_r[qt].y >= kmin);
+    return c;
+}
+// Q-stationary: key tile kt can be seen iff its smallest position <= qmax;
+// with the smallest positions non-decreasing the visible tiles are a prefix.
+__device__ __forceinline__ int next_k(int kt, const int2 *kt_o, int nk, int qmax, bool sorted) {
+    for (; kt < nk; ++kt) {
+        if (kt_o[kt].x <= qmax) return kt;
+        if (sorted) return nk;
+    }
+    return nk;
+}
+__device__ __forceinline__ int count_k(const int2 *kt_o, int nk, int qmax, bool sorted) {
+    if (sorted) {
+        int lo = 0, hi = nk;  // first tile with kmin > qmax
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (kt_o[mid].x <= qmax) lo = mid + 1; else hi = mid;
+        }
+        return lo;
+    }
+    int c = 0;
+    for (int kt = 0; kt < nk; ++kt) c += (kt_o[kt].x <= qmax);
+    return c;
+}
+
+// Longest-first order of the np (rank, stationary tile) pairs by cost; ties
+// keep index order.
+__device__ __forceinline__ void sort_pairs(const int *cost, int *order, int np, int tid) {
+    for (int p = tid; p < np; p += kBThreads) {
+        const int c = cost[p];
+        int rank = 0;
+        for (int q = 0; q < np; ++q) {
+            const int cq = cost[q];
+            rank += (cq > c) || (cq == c && q < p);
+        }
+        order[rank] = p;
+    }
+}
+
+// Row of D fp32 values from TMEM columns [col, col + D) of this thread's lane,
+// times `mul`, written to (or added to) dst (32-byte aligned).  Warp-collective.
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float *dst, float mul, bool write, bool add) {
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c0, v);
+        if (write) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+                float r8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r8[e] = __uint_as_float(v[c + e]) * mul;
+                if (add) {
+                    float o8[8];
+                    ld_global_v8(dst + c0 + c, o8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r8[e] += o8[e];
+                }
+                st_global_v8(dst + c0 + c, r8[0], r8[1], r8[2], r8[3], r8[4], r8[5], r8[6], r8[7]);
+            }
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void zero_row(float *dst) {
+#pragma unroll
+    for (int c = 0; c < D; c += 8) st_global_v8(dst + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// ======================================================================
+// dK / dV: K/V-stationary
+// ======================================================================
+template <int D>
+__global__ void __launch_bounds__(kBThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmNL2, const __grid_constant__ CUtensorMap tmND,
+                    const BwdArgs a) {
+    using K = CfgKV<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
+    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
+    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, key tile): visible query tiles
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
+    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per rank
+    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per query tile
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
+    uint64_t *kv_full = bar, *kv_empty = bar + 1, *qd_full = bar + 2, *qd_empty = bar + 2 + kBStages;
+    uint64_t *s_full = bar + 2 + 2 * kBStages, *p_full = s_full + 2, *o_full = s_full + 4, *o_empty = s_full + 5,
+             *drain = s_full + 6;
+    const int2 *ktab = tab;                 // [kpr][nk] 128-key tiles
+    const int2 *qtab = tab + a.kpr * a.nk;  // [C][nq] 64-query tiles
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int w = 0; w < kBwdMaxTables / 32; ++w) arith_bits[w] = 0u;
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(qd_full + s, 1);
+            mbar_init(qd_empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(p_full + i, 4);
+        }
+        mbar_init(o_full, 1);
+        mbar_init(o_empty, 4);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmNL2);
+        tma_prefetch_desc(&tmND);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kBTmemCols);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    {
+        const int nkk = a.kpr * a.nk, total = nkk + a.C * a.nq;
+        for (int g = warp; g < total; g += kBThreads / 32) {
+            if (g < nkk) {
+                const int j = g / a.nk, kt = g - (g / a.nk) * a.nk;
+                tile_table<128>(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab + g, nullptr, 0);
+            } else {
+                const int gq = g - nkk, r = gq / a.nq, qt = gq - (gq / a.nq) * a.nq;
+                tile_table<64>(a.q_pos + r * a.q_pos_stride, qt * 64, a.Sq, lane, tab + g, arith_bits, gq);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < a.C) {
+        int ok = 1;
+        for (int qt = 1; qt < a.nq; ++qt) ok &= (qtab[tid * a.nq + qt].y >= qtab[tid * a.nq + qt - 1].y);
+        sorted_flag[tid] = ok;
+    }
+    __syncthreads();
+    const int np = a.C * a.nk;
+    for (int p = tid; p < np; p += kBThreads) {
+        const int r = p / a.nk, kt = p - (p / a.nk) * a.nk;
+        const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+        cost[p] = count_q(qtab + r * a.nq, a.nq, ktab[owner * a.nk + kt].x, sorted_flag[r] != 0);
+    }
+    __syncthreads();
+    sort_pairs(cost, order, np, tid);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_items = np * a.B * a.Nkv;
+    const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    const int g_heads = a.N / a.Nkv;
+    uint8_t *sK = smem + K::kOffK, *sV = smem + K::kOffV, *sQ = smem + K::kOffQ, *sDO = smem + K::kOffDO;
+    float *sStat = reinterpret_cast<float *>(smem + K::kOffStat);
+
+    // item idx -> (pair, b, KV head)
+    auto decode = [&](int idx, int &r, int &kt, int &b, int &hk, int &owner, int &kvr, int &pr) {
+        const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bh);
+        const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bh.d;
+        pr = order[pi];
+        r = static_cast<int>(fdiv(static_cast<uint32_t>(pr), a.div_nt));
+        kt = pr - r * a.nk;
+        b = static_cast<int>(fdiv(bh, a.div_h));
+        hk = static_cast<int>(bh) - b * a.Nkv;
+        owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+        kvr = (r + a.kv_shift) % a.C;
+    };
+
+    if (warp == 0) {
+        // -------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t it = 0, t = 0;
+            bool ok = true;
+            int kv_par = -1;
+            uint32_t qd_issued = 0, qd_par = 0;
+            for (int rk = 0; rk < n_rounds && ok; ++rk) {
+                const int idx = item_of_round(rk, n_items);
+                if (idx < 0) continue;
+                int r, kt, b, hk, owner, kvr, pr;
+                decode(idx, r, kt, b, hk, owner, kvr, pr);
+                if (cost[pr] == 0) continue;
+                if (!mbar_wait(kv_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                mbar_arrive_expect_tx(kv_full, 2 * K::kBig);
+                kv_par = static_cast<int>(it & 1u);
+                const int kvrow = kvr * a.B + b;
+                for (int at = 0; at < K::kAtoms; ++at) {
+                    tma_load_4d(sK + at * K::kAtomBig, &tmK, kv_full, 64 * at, hk, kt * 128, kvrow);
+                    tma_load_4d(sV + at * K::kAtomBig, &tmV, kv_full, 64 * at, hk, kt * 128, kvrow);
+                }
+                ++it;
+                const int2 *qt_r = qtab + r * a.nq;
+                const int kmin = ktab[owner * a.nk + kt].x;
+                const bool srt = sorted_flag[r] != 0;
+                const int qrow = r * a.B + b;
+                for (int hh = 0; hh < g_heads && ok; ++hh) {
+                    const int h = hk * g_heads + hh;
+                    const int srow = qrow * a.N + h;
+                    for (int qt = first_q(qt_r, a.nq, kmin, srt); qt < a.nq; qt = next_q(qt + 1, qt_r, a.nq, kmin)) {
+                        const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
+                        if (!mbar_wait(qd_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        mbar_arrive_expect_tx(qd_full + st, 2 * K::kSmall + 512);
+                        for (int at = 0; at < K::kAtoms; ++at) {
+                            tma_load_4d(sQ + st * K::kSmall + at * K::kAtomSmall, &tmQ, qd_full + st, 64 * at, h,
+                                        qt * 64, qrow);
+                            tma_load_4d(sDO + st * K::kSmall + at * K::kAtomSmall, &tmDO, qd_full + st, 64 * at, h,
+                                        qt * 64, qrow);
+                        }
+                        tma_load_2d(sStat + st * 128, &tmNL2, qd_full + st, qt * 64, srow);
+                        tma_load_2d(sStat + st * 128 + 64, &tmND, qd_full + st, qt * 64, srow);
+                        qd_issued |= 1u << st;
+                        qd_par = (qd_par & ~(1u << st)) | (ph << st);
+                        ++t;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before shared memory goes away
+                volatile int no_abort = 0;
+                const unsigned long long drain_ns = 100000000ull;
+                if (kv_par >= 0) mbar_wait(kv_full, static_cast<uint32_t>(kv_par), &no_abort, drain_ns);
+                for (int st = 0; st < kBStages; ++st)
+                    if ((qd_issued >> st) & 1u) mbar_wait(qd_full + st, (qd_par >> st) & 1u, &no_abort, drain_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: 128 keys x 64 queries
+            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B operand MN-major
+            constexpr uint64_t kStU = K::kSmall >> 4;                 // one stage, descriptor units
+            const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024), dV = smem_desc_sw128(smem_u32(sV), 16, 1024);
+            const uint64_t dQk = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dOk = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+            const uint64_t dQm = smem_desc_sw128(smem_u32(sQ), K::kAtomSmall, 1024);
+            const uint64_t dOm = smem_desc_sw128(smem_u32(sDO), K::kAtomSmall, 1024);
+            uint32_t it = 0, t = 0;
+            bool ok = true;
+            // dV += P^T dO and dK += dS^T Q for streamed tile pt (P^T / dS^T in
+            // TMEM buffer pt & 1); `first` overwrites the accumulators
+            auto grads = [&](uint32_t pt, bool first) -> bool {
+                const uint32_t pb = pt & 1u, pst = pt % kBStages;
+                if (!mbar_wait(p_full + pb, (pt >> 1) & 1u, abort_flag, a.timeout_ns)) return false;
+                if (first && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) return false;
+                tc_fence_after();
+                umma_ts_k64(tmem + 256, tmem + pb * 128, dOm + pst * kStU, kIdG, first ? 0u : 1u);
+                umma_ts_k64(tmem + 256 + D, tmem + pb * 128 + 64, dQm + pst * kStU, kIdG, first ? 0u : 1u);
+                umma_commit(qd_empty + pst);
+                return true;
+            };
+            for (int rk = 0; rk < n_rounds && ok; ++rk) {
+                const int idx = item_of_round(rk, n_items);
+                if (idx < 0) continue;
+                int r, kt, b, hk, owner, kvr, pr;
+                decode(idx, r, kt, b, hk, owner, kvr, pr);
+                const int n = g_heads * cost[pr];
+                if (n == 0) continue;
+                if (!mbar_wait(kv_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                for (int i = 0; i < n; ++i) {
+                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u, bb = t & 1u;
+                    if (!mbar_wait(qd_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128, dK, dQk + st * kStU, kIdS);
+                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128 + 64, dV, dOk + st * kStU, kIdS);
+                    umma_commit(s_full + bb);
+                    if (i == n - 1) umma_commit(kv_empty);  // K and V are read by S^T / dP^T only
+                    if (i > 0 && !grads(t - 1, i == 1)) { ok = false; break; }
+                    ++t;
+                }
+                if (!ok) break;
+                if (!grads(t - 1, n == 1)) { ok = false; break; }
+                umma_commit(o_full);
+                ++it;
+            }
+            // no MMA may still be running when TMEM is released
+            umma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait(drain, 0, &no_abort, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- compute (one key row per thread)
+        const int quarter = warp & 3;
+        const int row_in = quarter * 32 + lane;
+        const uint32_t tA = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const float sl2 = a.scale_log2;
+        const uint64_t sl2x2 = f2_packf(sl2, sl2);
+        uint32_t it = 0, t = 0;
+        bool ok = true;
+        for (int rk = 0; rk < n_rounds && ok; ++rk) {
+            const int idx = item_of_round(rk, n_items);
+            if (idx < 0) continue;
+            int r, kt, b, hk, owner, kvr, pr;
+            decode(idx, r, kt, b, hk, owner, kvr, pr);
+            const int key = kt * 128 + row_in;
+            const bool key_valid = key < a.Sk;
+            const int kpos = key_valid ? __ldg(a.k_pos + owner * a.k_pos_stride + key) : INT_MAX;
+            const long long krow = (static_cast<long long>(kvr * a.B + b) * a.Sk + key) * a.Nkv + hk;
+            float *dk_row = a.dk + krow * D;
+            float *dv_row = a.dv + krow * D;
+            if (cost[pr] == 0) {
+                // no query sees these keys: their gradients are zero
+                if (key_valid && !a.accumulate) {
+                    zero_row<D>(dk_row);
+                    zero_row<D>(dv_row);
+                }
+                continue;
+            }
+            const int2 kmm = ktab[owner * a.nk + kt];
+            const int2 *qt_r = qtab + r * a.nq;
+            const bool srt = sorted_flag[r] != 0;
+            const int32_t *qpos_r = a.q_pos + r * a.q_pos_stride;
+            for (int hh = 0; hh < g_heads && ok; ++hh) {
+                for (int qt = first_q(qt_r, a.nq, kmm.x, srt); qt < a.nq; qt = next_q(qt + 1, qt_r, a.nq, kmm.x)) {
+                    const uint32_t bb = t & 1u, st = t % kBStages;
+                    if (!mbar_wait_warp(s_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t s[64], dp[64];
+                    tmem_ld64_nowait(tA + bb * 128, s);
+                    tmem_ld64_nowait(tA + bb * 128 + 64, dp);
+                    tmem_wait_ld(s);
+                    tmem_wait_ld(dp);
+                    const int2 qmm = qt_r[qt];
+                    const int q0 = qt * 64;
+                    const int nvalid = min(64, a.Sq - q0);
+                    if (kmm.y > qmm.x || nvalid < 64) {
+                        const int gq = r * a.nq + qt;
+                        if ((arith_bits[gq >> 5] >> (gq & 31)) & 1u) {
+                            // query positions qmin + c: column c visible iff c >= kpos - qmin
+                            const long long dlo = static_cast<long long>(kpos) - qmm.x;
+                            const int lo = dlo <= 0 ? 0 : (dlo > 64 ? 64 : static_cast<int>(dlo));
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                if (c < lo || c >= nvalid) s[c] = kNegInfBits;
+                        } else {
+#pragma unroll
+                            for (int c0 = 0; c0 < 64; c0 += 16) {
+#pragma unroll
+                                for (int c = c0; c < c0 + 16; ++c) {
+                                    const int qp = (c < nvalid) ? __ldg(qpos_r + q0 + c) : INT_MIN;
+                                    if (kpos > qp) s[c] = kNegInfBits;
+                                }
+                                asm volatile("" ::: "memory");
+                            }
+                        }
+                    }
+                    // P^T = 2^(s sl2 + nl2_c), dS^T = P^T (dP^T + nd_c), column stats from the stage
+                    const float *nl = sStat + st * 128, *nd = nl + 64;
+                    uint32_t pk_p[32], pk_d[32];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(nl + c);
+                        const float4 d4 = *reinterpret_cast<const float4 *>(nd + c);
+                        float x0, x1, x2, x3, g0, g1, g2, g3;
+                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, f2_packf(l4.x, l4.y)), x0, x1);
+                        f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, f2_packf(l4.z, l4.w)), x2, x3);
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+                        f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), f2_packf(d4.x, d4.y)),
+                                         0ull),
+                                  g0, g1);
+                        f2_unpack(f2_fma(f2_packf(p2, p3),
+                                         f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_packf(d4.z, d4.w)), 0ull),
+                                  g2, g3);
+                        pk_p[c >> 1] = pack_bf16x2(p0, p1);
+                        pk_p[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+                        pk_d[c >> 1] = pack_bf16x2(g0, g1);
+                        pk_d[(c >> 1) + 1] = pack_bf16x2(g2, g3);
+                    }
+                    tmem_st32_nowait(tA + bb * 128, pk_p);
+                    tmem_st32_nowait(tA + bb * 128 + 64, pk_d);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full + bb);
+                    ++t;
+                }
+            }
+            if (!ok) break;
+            if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            store_acc_row<D>(tA + 256, dv_row, 1.f, key_valid, a.accumulate != 0);
+            store_acc_row<D>(tA + 256 + D, dk_row, a.scale, key_valid, a.accumulate != 0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_empty);
+            ++it;
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kBTmemCols);
+    }
+    if (tid == 0 && *abort_flag) atomicExch(&g_cp_bwd_status, static_cast<int>(CP_ERR_DEVICE_TIMEOUT));
+}
+
+// ======================================================================
+// dQ: Q-stationary
+// ======================================================================
+template <int D>
+__global__ void __launch_bounds__(kBThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdArgs a) {
+    using K = CfgQ<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
+    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
+    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, query tile): visible key tiles
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
+    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per key-position rank
+    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per key tile
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
+    uint64_t *qd_full = bar, *qd_empty = bar + 1, *kv_full = bar + 2, *kv_empty = bar + 2 + kBStages;
+    uint64_t *s_full = bar + 2 + 2 * kBStages, *p_full = s_full + 2, *o_full = s_full + 4, *o_empty = s_full + 5,
+             *drain = s_full + 6;
+    const int2 *qtab = tab;                // [C][nq] 128-query tiles
+    const int2 *ktab = tab + a.C * a.nq;   // [kpr][nk] 64-key tiles
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int w = 0; w < kBwdMaxTables / 32; ++w) arith_bits[w] = 0u;
+        mbar_init(qd_full, 1);
+        mbar_init(qd_empty, 1);
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(kv_full + s, 1);
+            mbar_init(kv_empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(p_full + i, 4);
+        }
+        mbar_init(o_full, 1);
+        mbar_init(o_empty, 4);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kBTmemCols);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    {
+        const int nqq = a.C * a.nq, total = nqq + a.kpr * a.nk;
+        for (int g = warp; g < total; g += kBThreads / 32) {
+            if (g < nqq) {
+                const int r = g / a.nq, qt = g - (g / a.nq) * a.nq;
+                tile_table<128>(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab + g, nullptr, 0);
+            } else {
+                const int gk = g - nqq, j = gk / a.nk, kt = gk - (gk / a.nk) * a.nk;
+                tile_table<64>(a.k_pos + j * a.k_pos_stride, kt * 64, a.Sk, lane, tab + g, arith_bits, gk);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < a.kpr) {
+        int ok = 1;
+        for (int kt = 1; kt < a.nk; ++kt) ok &= (ktab[tid * a.nk + kt].x >= ktab[tid * a.nk + kt - 1].x);
+        sorted_flag[tid] = ok;
+    }
+    __syncthreads();
+    const int np = a.C * a.nq;
+    for (int p = tid; p < np; p += kBThreads) {
+        const int r = p / a.nq, qt = p - (p / a.nq) * a.nq;
+        const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+        cost[p] = count_k(ktab + owner * a.nk, a.nk, qtab[r * a.nq + qt].y, sorted_flag[owner] != 0);
+    }
+    __syncthreads();
+    sort_pairs(cost, order, np, tid);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_items = np * a.B * a.N;
+    const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+    const int g_heads = a.N / a.Nkv;
+    uint8_t *sQ = smem + K::kOffQ, *sDO = smem + K::kOffDO, *sK = smem + K::kOffK, *sV = smem + K::kOffV;
+
+    auto decode = [&](int idx, int &r, int &qt, int &b, int &h, int &owner, int &kvr, int &pr) {
+        const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bh);
+        const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bh.d;
+        pr = order[pi];
+        r = static_cast<int>(fdiv(static_cast<uint32_t>(pr), a.div_nt));
+        qt = pr - r * a.nq;
+        b = static_cast<int>(fdiv(bh, a.div_h));
+        h = static_cast<int>(bh) - b * a.N;
+        owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+        kvr = (r + a.kv_shift) % a.C;
+    };
+
+    if (warp == 0) {
+        // -------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t it = 0, t = 0;
+            bool ok = true;
+            int qd_par = -1;
+            uint32_t kv_issued = 0, kv_par = 0;
+            for (int rk = 0; rk < n_rounds && ok; ++rk) {
+                const int idx = item_of_round(rk, n_items);
+                if (idx < 0) continue;
+                int r, qt, b, h, owner, kvr, pr;
+                decode(idx, r, qt, b, h, owner, kvr, pr);
+                if (cost[pr] == 0) continue;
+                if (!mbar_wait(qd_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                mbar_arrive_expect_tx(qd_full, 2 * K::kBig);
+                qd_par = static_cast<int>(it & 1u);
+                const int qrow = r * a.B + b;
+                for (int at = 0; at < K::kAtoms; ++at) {
+                    tma_load_4d(sQ + at * K::kAtomBig, &tmQ, qd_full, 64 * at, h, qt * 128, qrow);
+                    tma_load_4d(sDO + at * K::kAtomBig, &tmDO, qd_full, 64 * at, h, qt * 128, qrow);
+                }
+                ++it;
+                const int2 *kt_o = ktab + owner * a.nk;
+                const int qmax = qtab[r * a.nq + qt].y;
+                const bool srt = sorted_flag[owner] != 0;
+                const int hk = h / g_heads;
+                const int kvrow = kvr * a.B + b;
+                for (int kt = next_k(0, kt_o, a.nk, qmax, srt); kt < a.nk; kt = next_k(kt + 1, kt_o, a.nk, qmax, srt)) {
+                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
+                    if (!mbar_wait(kv_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(kv_full + st, 2 * K::kSmall);
+                    for (int at = 0; at < K::kAtoms; ++at) {
+                        tma_load_4d(sK + st * K::kSmall + at * K::kAtomSmall, &tmK, kv_full + st, 64 * at, hk,
+                                    kt * 64, kvrow);
+                        tma_load_4d(sV + st * K::kSmall + at * K::kAtomSmall, &tmV, kv_full + st, 64 * at, hk,
+                                    kt * 64, kvrow);
+                    }
+                    kv_issued |= 1u << st;
+                    kv_par = (kv_par & ~(1u << st)) | (ph << st);
+                    ++t;
+                }
+            }
+            if (!ok) {
+                volatile int no_abort = 0;
+                const unsigned long long drain_ns = 100000000ull;
+                if (qd_par >= 0) mbar_wait(qd_full, static_cast<uint32_t>(qd_par), &no_abort, drain_ns);
+                for (int st = 0; st < kBStages; ++st)
+                    if ((kv_issued >> st) & 1u) mbar_wait(kv_full + st, (kv_par >> st) & 1u, &no_abort, drain_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, 0, 0);  // S, dP: 128 queries x 64 keys
+            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);   // dQ: B operand MN-major
+            constexpr uint64_t kStU = K::kSmall >> 4;
+            const uint64_t dQa = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dOa = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+            const uint64_t dKb = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dVb = smem_desc_sw128(smem_u32(sV), 16, 1024);
+            const uint64_t dKm = smem_desc_sw128(smem_u32(sK), K::kAtomSmall, 1024);
+            uint32_t it = 0, t = 0;
+            bool ok = true;
+            auto grad = [&](uint32_t pt, bool first) -> bool {
+                const uint32_t pb = pt & 1u, pst = pt % kBStages;
+                if (!mbar_wait(p_full + pb, (pt >> 1) & 1u, abort_flag, a.timeout_ns)) return false;
+                if (first && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) return false;
+                tc_fence_after();
+                umma_ts_k64(tmem + 256, tmem + pb * 128, dKm + pst * kStU, kIdG, first ? 0u : 1u);
+                umma_commit(kv_empty + pst);  // K (S and dQ) and V (dP) of this stage are read
+                return true;
+            };
+            for (int rk = 0; rk < n_rounds && ok; ++rk) {
+                const int idx = item_of_round(rk, n_items);
+                if (idx < 0) continue;
+                int r, qt, b, h, owner, kvr, pr;
+                decode(idx, r, qt, b, h, owner, kvr, pr);
+                const int n = cost[pr];
+                if (n == 0) continue;
+                if (!mbar_wait(qd_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                for (int j = 0; j < n; ++j) {
+                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u, bb = t & 1u;
+                    if (!mbar_wait(kv_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128, dQa, dKb + st * kStU, kIdS);
+                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128 + 64, dOa, dVb + st * kStU, kIdS);
+                    umma_commit(s_full + bb);
+                    if (j == n - 1) umma_commit(qd_empty);  // Q and dO are read by S / dP only
+                    if (j > 0 && !grad(t - 1, j == 1)) { ok = false; break; }
+                    ++t;
+                }
+                if (!ok) break;
+                if (!grad(t - 1, n == 1)) { ok = false; break; }
+                umma_commit(o_full);
+                ++it;
+            }
+            umma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait(drain, 0, &no_abort, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- compute (one query row per thread)
+        const int quarter = warp & 3;
+        const int row_in = quarter * 32 + lane;
+        const uint32_t tA = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint64_t sl2x2 = f2_packf(a.scale_log2, a.scale_log2);
+        uint32_t it = 0, t = 0;
+        bool ok = true;
+        for (int rk = 0; rk < n_rounds && ok; ++rk) {
+            const int idx = item_of_round(rk, n_items);
+            if (idx < 0) continue;
+            int r, qt, b, h, owner, kvr, pr;
+            decode(idx, r, qt, b, h, owner, kvr, pr);
+            const int row = qt * 128 + row_in;
+            const bool row_valid = row < a.Sq;
+            const int qpos = row_valid ? __ldg(a.q_pos + r * a.q_pos_stride + row) : INT_MIN;
+            const long long qrow = static_cast<long long>(r * a.B + b);
+            float *dq_row = a.dq + ((qrow * a.Sq + row) * a.N + h) * D;
+            if (cost[pr] == 0) {
+                if (row_valid && !a.accumulate) zero_row<D>(dq_row);
+                continue;
+            }
+            // rows past Sq read the padding (-inf, 0): they see nothing
+            const long long srow = (qrow * a.N + h) * a.sq_pad + row;
+            const float nl2 = __ldg(a.nl2 + srow), ndv = __ldg(a.nd + srow);
+            const uint64_t nl2x2 = f2_packf(nl2, nl2), ndx2 = f2_packf(ndv, ndv);
+            const int2 *kt_o = ktab + owner * a.nk;
+            const int2 qmm = qtab[r * a.nq + qt];
+            const bool srt = sorted_flag[owner] != 0;
+            const int32_t *kpos_o = a.k_pos + owner * a.k_pos_stride;
+            for (int kt = next_k(0, kt_o, a.nk, qmm.y, srt); kt < a.nk; kt = next_k(kt + 1, kt_o, a.nk, qmm.y, srt)) {
+                const uint32_t bb = t & 1u;
+                if (!mbar_wait_warp(s_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t s[64], dp[64];
+                tmem_ld64_nowait(tA + bb * 128, s);
+                tmem_ld64_nowait(tA + bb * 128 + 64, dp);
+                tmem_wait_ld(s);
+                tmem_wait_ld(dp);
+                const int2 kmm = kt_o[kt];
+                const int k0 = kt * 64;
+                const int nvalid = min(64, a.Sk - k0);
+                if (kmm.y > qmm.x || nvalid < 64) {
+                    const int gk = owner * a.nk + kt;
+                    if ((arith_bits[gk >> 5] >> (gk & 31)) & 1u) {
+                        // key positions kmin + c: column c visible iff c <= qpos - kmin
+                        const long long dhi = static_cast<long long>(qpos) - kmm.x;
+                        const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c > lim) s[c] = kNegInfBits;
+                    } else {
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+#pragma unroll
+                            for (int c = c0; c < c0 + 16; ++c) {
+                                const int kp = (c < nvalid) ? __ldg(kpos_o + k0 + c) : INT_MAX;
+                                if (kp > qpos) s[c] = kNegInfBits;
+                            }
+                            asm volatile("" ::: "memory");
+                        }
+                    }
+                }
+                // dS = 2^(s sl2 + nl2) (dP + nd)
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float x0, x1, g0, g1;
+                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nl2x2), x0, x1);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), ndx2), 0ull), g0, g1);
+                    pk[c >> 1] = pack_bf16x2(g0, g1);
+                }
+                tmem_st32(tA + bb * 128, pk);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full + bb);
+                ++t;
+            }
+            if (!ok) break;
+            if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+            tc_fence_after();
+            store_acc_row<D>(tA + 256, dq_row, a.scale, row_valid, a.accumulate != 0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_empty);
+            ++it;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kBTmemCols);
+    }
+    if (tid == 0 && *abort_flag) atomicExch(&g_cp_bwd_status, static_cast<int>(CP_ERR_DEVICE_TIMEOUT));
+}
+
+// ======================================================================
+// per-row statistics
+// ======================================================================
+__global__ void __launch_bounds__(256) bwd_stats_kernel(const float *__restrict__ o,
+                                                        const __nv_bfloat16 *__restrict__ dout,
+                                                        const float *__restrict__ lse, long long CB, int Sq, int N,
+                                                        int D, long long sq_pad, float *__restrict__ nl2,
+                                                        float *__restrict__ nd) {
+    const long long total = CB * N * sq_pad;
+    for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long i = idx % sq_pad, rh = idx / sq_pad;
+        const long long h = rh % N, rb = rh / N;
+        float v_nl2 = -INFINITY, v_nd = 0.f;
+        if (i < Sq) {
+            const float l = lse[(rb * N + h) * Sq + i];
+            const long long row = ((rb * Sq + i) * N + h) * D;
+            const float4 *o4 = reinterpret_cast<const float4 *>(o + row);
+            const uint4 *d8 = reinterpret_cast<const uint4 *>(dout + row);
+            float acc = 0.f;
+            for (int c = 0; c < D / 8; ++c) {
+                const float4 a0 = __ldg(o4 + 2 * c), a1 = __ldg(o4 + 2 * c + 1);
+                const uint4 w = __ldg(d8 + c);
+                const __nv_bfloat162 *hb = reinterpret_cast<const __nv_bfloat162 *>(&w);
+                const float2 f0 = __bfloat1622float2(hb[0]), f1 = __bfloat1622float2(hb[1]);
+                const float2 f2 = __bfloat1622float2(hb[2]), f3 = __bfloat1622float2(hb[3]);
+                acc = fmaf(a0.x, f0.x, acc);
+                acc = fmaf(a0.y, f0.y, acc);
+                acc = fmaf(a0.z, f1.x, acc);
+                acc = fmaf(a0.w, f1.y, acc);
+                acc = fmaf(a1.x, f2.x, acc);
+                acc = fmaf(a1.y, f2.y, acc);
+                acc = fmaf(a1.z, f3.x, acc);
+                acc = fmaf(a1.w, f3.y, acc);
+            }
+            v_nl2 = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634074f;
+            v_nd = -acc;
+        }
+        nl2[idx] = v_nl2;
+        nd[idx] = v_nd;
+    }
+}
+
+template <int D>
+BwdArgs make_args(const BwdProblem &p, int nq, int nk, int heads_per_item) {
+    BwdArgs a;
+    a.q_pos = p.q_pos;
+    a.k_pos = p.k_pos;
+    a.q_pos_stride = p.q_pos_stride;
+    a.k_pos_stride = p.k_pos_stride;
+    a.nl2 = p.nl2;
+    a.nd = p.nd;
+    a.sq_pad = p.sq_pad;
+    a.dq = p.dq;
+    a.dk = p.dk;
+    a.dv = p.dv;
+    a.C = p.C;
+    a.B = static_cast<int>(p.B);
+    a.N = static_cast<int>(p.N);
+    a.Nkv = static_cast<int>(p.Nkv);
+    a.Sq = static_cast<int>(p.Sq);
+    a.Sk = static_cast<int>(p.Sk);
+    a.nq = nq;
+    a.nk = nk;
+    a.kv_shift = p.kv_shift;
+    a.kpos_shift = p.kpos_shift;
+    a.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
+    a.accumulate = p.accumulate ? 1 : 0;
+    a.scale = p.scale;
+    a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
+    a.timeout_ns = 2000000000ull;
+    a.div_bh = make_fastdiv(static_cast<uint32_t>(a.B * heads_per_item));
+    a.div_h = make_fastdiv(static_cast<uint32_t>(heads_per_item));
+    return a;
+}
+
+template <int D>
+cp_status launch_dkdv_typed(const BwdProblem &p, cudaStream_t stream) {
+    using K = CfgKV<D>;
+    CUtensorMap mq, mdo, mk, mv, mnl, mnd;
+    const int64_t CB = p.C * p.B;
+    if (!make_map(&mq, p.q, D, p.N, p.Sq, CB, 64) || !make_map(&mdo, p.dout, D, p.N, p.Sq, CB, 64) ||
+        !make_map(&mk, p.k, D, p.Nkv, p.Sk, CB, 128) || !make_map(&mv, p.v, D, p.Nkv, p.Sk, CB, 128) ||
+        !make_map_f32_rows(&mnl, p.nl2, p.sq_pad, CB * p.N, 64) || !make_map_f32_rows(&mnd, p.nd, p.sq_pad, CB * p.N, 64))
+        return CP_ERR_CUDA;
+    const int nq = static_cast<int>((p.Sq + 63) / 64), nk = static_cast<int>((p.Sk + 127) / 128);
+    BwdArgs a = make_args<D>(p, nq, nk, static_cast<int>(p.Nkv));
+    a.div_nt = make_fastdiv(static_cast<uint32_t>(nk));
+    const long long n_items = static_cast<long long>(p.C) * nk * p.B * p.Nkv;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return cuda_status(attr_err);
+    const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
+    bwd_dkdv_kernel<D><<<grid, kBThreads, K::kSmemBytes, stream>>>(mq, mdo, mk, mv, mnl, mnd, a);
+    return last_launch_status();
+}
+
+template <int D>
+cp_status launch_dq_typed(const BwdProblem &p, cudaStream_t stream) {
+    using K = CfgQ<D>;
+    CUtensorMap mq, mdo, mk, mv;
+    const int64_t CB = p.C * p.B;
+    if (!make_map(&mq, p.q, D, p.N, p.Sq, CB, 128) || !make_map(&mdo, p.dout, D, p.N, p.Sq, CB, 128) ||
+        !make_map(&mk, p.k, D, p.Nkv, p.Sk, CB, 64) || !make_map(&mv, p.v, D, p.Nkv, p.Sk, CB, 64))
+        return CP_ERR_CUDA;
+    const int nq = static_cast<int>((p.Sq + 127) / 128), nk = static_cast<int>((p.Sk + 63) / 64);
+    BwdArgs a = make_args<D>(p, nq, nk, static_cast<int>(p.N));
+    a.div_nt = make_fastdiv(static_cast<uint32_t>(nq));
+    const long long n_items = static_cast<long long>(p.C) * nq * p.B * p.N;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return cuda_status(attr_err);
+    const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
+    bwd_dq_kernel<D><<<grid, kBThreads, K::kSmemBytes, stream>>>(mq, mdo, mk, mv, a);
+    return last_launch_status();
+}
+
+}  // namespace
+
+cp_status launch_bwd_stats(const float *o, const void *dout, const float *lse, int64_t CB, int64_t Sq, int64_t N,
+                           int64_t D, int64_t sq_pad, float *nl2, float *nd, cudaStream_t stream) {
+    if (!o || !dout || !lse || !nl2 || !nd) return CP_ERR_NULL;
+    if (CB < 1 || Sq < 1 || N < 1 || (D != 64 && D != 128) || sq_pad < Sq) return CP_ERR_SHAPE;
+    if (!aligned16(o) || !aligned16(dout)) return CP_ERR_ALIGNMENT;
+    const long long total = CB * N * sq_pad;
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    bwd_stats_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        o, static_cast<const __nv_bfloat16 *>(dout), lse, CB, static_cast<int>(Sq), static_cast<int>(N),
+        static_cast<int>(D), sq_pad, nl2, nd);
+    return last_launch_status();
+}
+
+cp_status validate_bwd(const BwdProblem &p) {
+    if (!p.q || !p.k || !p.v || !p.dout || !p.q_pos || !p.k_pos || !p.nl2 || !p.nd || !p.dq || !p.dk || !p.dv)
+        return CP_ERR_NULL;
+    if (p.C < 1 || p.C > kMaxC || p.B < 1 || p.N < 1 || p.Nkv < 1 || p.Sq < 1 || p.Sk < 1) return CP_ERR_SHAPE;
+    if (p.D != 64 && p.D != 128) return CP_ERR_UNSUPPORTED;
+    if (p.N % p.Nkv != 0) return CP_ERR_DIVISIBILITY;
+    if (!(std::isfinite(p.scale) && p.scale > 0.f)) return CP_ERR_ARGUMENT;
+    if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.dout) || !aligned16(p.q_pos) ||
+        !aligned16(p.k_pos) || !aligned16(p.nl2) || !aligned16(p.nd))
+        return CP_ERR_ALIGNMENT;
+    // accumulator rows are written with 32-byte stores
+    if ((reinterpret_cast<uintptr_t>(p.dq) | reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) &
+        31u)
+        return CP_ERR_ALIGNMENT;
+    if (p.sq_pad < bwd_sq_pad(p.Sq) || p.sq_pad % 128 != 0) return CP_ERR_SHAPE;
+    const int64_t kpr = (p.k_pos_stride == 0) ? 1 : p.C;
+    const int64_t q64 = (p.Sq + 63) / 64, q128 = (p.Sq + 127) / 128, k64 = (p.Sk + 63) / 64,
+                  k128 = (p.Sk + 127) / 128;
+    if (kpr * k128 + p.C * q64 > kBwdMaxTables || p.C * q128 + kpr * k64 > kBwdMaxTables) return CP_ERR_SHAPE;
+    if (p.C * k128 > kBwdMaxPairs || p.C * q128 > kBwdMaxPairs) return CP_ERR_SHAPE;
+    if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.C * k128 * p.B * p.Nkv > INT32_MAX ||
+        p.C * q128 * p.B * p.N > INT32_MAX)
+        return CP_ERR_SHAPE;
+    if (p.kv_shift < 0 || p.kv_shift >= p.C || p.kpos_shift < 0 || p.kpos_shift >= p.C) return CP_ERR_ARGUMENT;
+    return CP_OK;
+}
+
+cp_status launch_bwd(const BwdProblem &p, cudaStream_t stream) {
+    cp_status st = validate_bwd(p);
+    if (st != CP_OK) return st;
+    st = (p.D == 128) ? launch_dkdv_typed<128>(p, stream) : launch_dkdv_typed<64>(p, stream);
+    if (st == CP_OK) st = (p.D == 128) ? launch_dq_typed<128>(p, stream) : launch_dq_typed<64>(p, stream);
+    return st;
+}
+
+cp_status read_bwd_device_status(int *code, bool clear) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_cp_bwd_status, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+    *code = v;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_cp_bwd_status, &zero, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
+    }
+    return CP_OK;
+}
+
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t N, size_t *bytes) {
+    if (!bytes) return CP_ERR_NULL;
+    if (B < 1 || Sq < 1 || N < 1) return CP_ERR_SHAPE;
+    *bytes = 2 * static_cast<size_t>(B) * N * bwd_sq_pad(Sq) * sizeof(float);
+    return CP_OK;
+}
+
+extern "C" cp_status cp_attn_bwd_partial(const void *q, const void *k, const void *v, const float *o,
+                                         const void *dout, const float *lse, const int32_t *q_pos,
+                                         const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,
+                                         int64_t Nkv, int64_t D, float scale, float *dq, float *dk, float *dv,
+                                         int accumulate, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!o || !lse) return CP_ERR_NULL;
+    if (B < 1 || Sq < 1 || N < 1) return CP_ERR_SHAPE;
+    const int64_t pad = bwd_sq_pad(Sq);
+    const size_t need = 2 * static_cast<size_t>(B) * N * pad * sizeof(float);
+    if (!workspace || ws_bytes < need) return CP_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return CP_ERR_ALIGNMENT;
+    BwdProblem p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.dout = dout;
+    p.q_pos = q_pos;
+    p.k_pos = k_pos;
+    p.q_pos_stride = 0;
+    p.k_pos_stride = 0;
+    p.nl2 = static_cast<float *>(workspace);
+    p.nd = static_cast<float *>(workspace) + B * N * pad;
+    p.sq_pad = pad;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.C = 1;
+    p.B = B;
+    p.N = N;
+    p.Nkv = Nkv;
+    p.D = D;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.accumulate = accumulate != 0;
+    p.scale = scale;
+    cp_status st = validate_bwd(p);
+    if (st != CP_OK) return st;
+    st = launch_bwd_stats(o, dout, lse, B, Sq, N, D, pad, const_cast<float *>(p.nl2), const_cast<float *>(p.nd),
+                          stream);
+    if (st == CP_OK) st = launch_bwd(p, stream);
+    return st;
+}
+
+extern "C" cp_status cp_ring_bwd_workspace_size(int64_t B, int64_t S, int64_t N, int C, size_t *bytes) {
+    if (!bytes) return CP_ERR_NULL;
+    if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1) return CP_ERR_SHAPE;
+    if (S % C != 0) return CP_ERR_DIVISIBILITY;
+    *bytes = 2 * static_cast<size_t>(C) * B * N * bwd_sq_pad(S / C) * sizeof(float);
+    return CP_OK;
+}
+
+extern "C" cp_status cp_ring_attention_bwd(const void *q_sh, const void *k_sh, const void *v_sh, const float *o_sh,
+                                           const float *lse_sh, const void *do_sh, const int32_t *pos, int64_t B,
+                                           int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, float scale,
+                                           cp_layout layout, float *dq_sh, float *dk_sh, float *dv_sh,
+                                           void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!o_sh || !lse_sh) return CP_ERR_NULL;
+    if (layout != CP_ZIGZAG && layout != CP_CONTIGUOUS) return CP_ERR_ARGUMENT;
+    if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
+    if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
+    const int64_t s = S / C, pad = bwd_sq_pad(s);
+    const size_t need = 2 * static_cast<size_t>(C) * B * N * pad * sizeof(float);
+    if (!workspace || ws_bytes < need) return CP_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return CP_ERR_ALIGNMENT;
+    BwdProblem p{};
+    p.q = q_sh;
+    p.k = k_sh;
+    p.v = v_sh;
+    p.dout = do_sh;
+    p.q_pos = pos;
+    p.k_pos = pos;
+    p.q_pos_stride = s;
+    p.k_pos_stride = s;
+    p.nl2 = static_cast<float *>(workspace);
+    p.nd = static_cast<float *>(workspace) + C * B * N * pad;
+    p.sq_pad = pad;
+    p.dq = dq_sh;
+    p.dk = dk_sh;
+    p.dv = dv_sh;
+    p.C = C;
+    p.B = B;
+    p.N = N;
+    p.Nkv = Nkv;
+    p.D = D;
+    p.Sq = s;
+    p.Sk = s;
+    p.scale = scale;
+    cp_status st = validate_bwd(p);  // everything checked before anything is enqueued
+    if (st != CP_OK) return st;
+    st = launch_bwd_stats(o_sh, do_sh, lse_sh, C * B, s, N, D, pad, const_cast<float *>(p.nl2),
+                          const_cast<float *>(p.nd), stream);
+    // step `step`: rank r's queries against the K/V of owner (r - step) mod C;
+    // dq of rank r and dk / dv of the owner accumulate from step 1 on (the
+    // travelling dK / dV of the pages' ring are the owners' own accumulators here)
+    for (int step = 0; step < C && st == CP_OK; ++step) {
+        const int back = (C - step) % C;
+        BwdProblem ps = p;
+        ps.kv_shift = back;
+        ps.kpos_shift = back;
+        ps.accumulate = step > 0;
+        st = launch_bwd(ps, stream);
+    }
+    return st;
+}

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
 #include "../../include/cpattn.h"
@@ -68,10 +69,54 @@ cp_status launch_merge(float *o_acc, float *lse_acc, const float *o_tile, const 
                        int64_t Sq, int64_t N, int64_t D, cudaStream_t stream);
 
 // fp32 -> bf16 (round to nearest even), n elements, n % 8 == 0.
+cp_status launch_f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t stream);
+
 // cp_ulysses_relayout applied to `groups` independent blocks laid out one
 // after another (same byte offset of each block on both sides); one launch.
 cp_status ulysses_relayout_groups(const void *in, void *out, int64_t B, int64_t S, int64_t N, int64_t D, int C,
                                   int groups, cp_dtype dtype, cp_dir dir, cp_seq_order order, cudaStream_t stream);
-cp_status launch_f32_to_bf16(const float *in, void *out, int64_t n, cudaStream_t stream);
+
+// TMA descriptors.  make_map: 4-D bf16 map over [outer][rows][heads][D],
+// box 64 columns x 1 head x box_rows rows x 1, 128-byte swizzle.
+// make_map_f32_rows: 2-D fp32 map over [rows][cols], box box_cols x 1.
+bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int64_t rows, int64_t outer,
+              int box_rows);
+bool make_map_f32_rows(CUtensorMap *map, const float *base, int64_t cols, int64_t rows, int box_cols);
+
+// ------------------------------------------------------------ backward
+constexpr int kBwdMaxTables = 4096;  // position tables of one backward launch
+constexpr int kBwdMaxPairs = 2048;   // (rank, stationary tile) pairs of one backward launch
+
+// One batched backward launch over C "rank" problems (the tile backward of
+// each rank's queries against the K/V of rank (r + kv_shift) mod C), with the
+// same rank conventions as AttnProblem.  dout is bf16 like q; o fp32 (the
+// final output, [C][B][Sq][N][D]); lse the final log-sum-exp [C][B][N][Sq].
+// nl2 / nd: per-row statistics from launch_bwd_stats ([C][B][N][sq_pad]).
+// dq [C][B][Sq][N][D]; dk, dv [C][B][Sk][Nkv][D] indexed by the K/V rank;
+// accumulate: add to them instead of overwriting.
+struct BwdProblem {
+    const void *q, *k, *v, *dout;
+    const int32_t *q_pos, *k_pos;
+    int64_t q_pos_stride, k_pos_stride;
+    const float *nl2, *nd;
+    int64_t sq_pad;
+    float *dq, *dk, *dv;
+    int C;
+    int64_t B, N, Nkv, D, Sq, Sk;
+    int kv_shift, kpos_shift;
+    bool accumulate;
+    float scale;
+};
+// Rows of the per-row statistics (a multiple of 128 >= Sq).
+inline int64_t bwd_sq_pad(int64_t Sq) { return (Sq + 127) / 128 * 128; }
+// nl2[r][i] = -lse * log2(e) (-inf where lse = -inf or i >= Sq) and
+// nd[r][i] = -<dO_i, o_i> (0 for i >= Sq), rows r over C*B*N.
+cp_status launch_bwd_stats(const float *o, const void *dout, const float *lse, int64_t CB, int64_t Sq, int64_t N,
+                           int64_t D, int64_t sq_pad, float *nl2, float *nd, cudaStream_t stream);
+cp_status validate_bwd(const BwdProblem &p);
+// dK / dV launch then dQ launch (both validated first).
+cp_status launch_bwd(const BwdProblem &p, cudaStream_t stream);
+// Sticky device status word of the backward kernels (read and optionally cleared).
+cp_status read_bwd_device_status(int *code, bool clear);
 
 }  // namespace cpattn

@@ -65,6 +65,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait by every lane of a warp with one warp-wide answer: a lane that
+// gave up (timeout or abort) makes the whole warp give up, so the warp never
+// splits around the warp-collective tcgen05 instructions that follow.  Lanes
+// still spinning see the raised abort flag and stop as well.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                               uint64_t timeout_ns) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, timeout_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -77,6 +87,15 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// 2-D tiled load (innermost coordinate c0 in elements).
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
         : "memory");
 }
 
@@ -195,6 +214,61 @@ __device__ __forceinline__ void umma_pv_group(uint32_t d_tmem, uint32_t a_tmem, 
         "add.u32 a1, %1, 40;\n\tadd.s64 b1, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
         "add.u32 a1, %1, 48;\n\tadd.s64 b1, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
         "add.u32 a1, %1, 56;\n\tadd.s64 b1, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u)
+        : "memory");
+}
+
+// D = A B^T over NK k-steps of 16 (K = 16 NK) with both operands K-major,
+// 128-byte swizzled: k-step kk starts (kk / 4) swizzle atoms + (kk % 4) * 32 B
+// further in each operand, an atom of A being AU and of B being BU descriptor
+// units (16 B; a 128-row atom is 1024 units, a 64-row atom 512).  The first
+// MMA overwrites D.
+template <int NK, int AU, int BU>
+__device__ __forceinline__ void umma_ss_kgroup(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc) {
+    static_assert(NK == 4 || NK == 8, "head dim 64 or 128");
+    if (NK == 8) {
+        asm volatile(
+            "{\n\t.reg .pred t, f;\n\t.reg .b64 a1, b1;\n\t"
+            "setp.ne.b32 t, %4, 0;\n\tsetp.eq.b32 f, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %9;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, %6;\n\tadd.s64 b1, %2, %10;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, %7;\n\tadd.s64 b1, %2, %11;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, %8;\n\tadd.s64 b1, %2, %12;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(1u), "n"(AU), "n"(AU + 2), "n"(AU + 4), "n"(AU + 6), "n"(BU),
+            "n"(BU + 2), "n"(BU + 4), "n"(BU + 6)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred t, f;\n\t.reg .b64 a1, b1;\n\t"
+            "setp.ne.b32 t, %4, 0;\n\tsetp.eq.b32 f, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "}" ::"r"(d_tmem),
+            "l"(a), "l"(b), "r"(idesc), "r"(1u)
+            : "memory");
+    }
+}
+// D (+)= A B over K = 64 (4 k-steps of 16): A read from TMEM starting at
+// column `a_tmem` (8 columns of packed bf16 pairs per k-step), B from an
+// MN-major swizzled tile whose descriptor for rows 0..15 is `b` (next 16
+// rows: +2048 B = +128 units).  `acc` = 0 overwrites D with the first product.
+__device__ __forceinline__ void umma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred t, p;\n\t.reg .b64 b1;\n\t.reg .b32 a1;\n\t"
+        "setp.ne.b32 t, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.s64 b1, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 16;\n\tadd.s64 b1, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 24;\n\tadd.s64 b1, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
         "}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u)
         : "memory");

@@ -259,6 +259,58 @@ def cp_mesh_attention_fwd(q_sh, k_sh, v_sh, pos, A, R, scale=None, layout=CP_ZIG
     return o, lse
 
 
+def cp_attn_bwd_partial(q, k, v, o, dout, lse, q_pos, k_pos, scale=None, dq=None, dk=None, dv=None, accumulate=False,
+                        workspace=None, stream=None):
+    """Tile backward -> (dq fp32 [B,Sq,N,D], dk, dv fp32 [B,Sk,Nkv,D]) from the
+    final output o (fp32) and lse; q, k, v, dout bf16."""
+    B, Sq, N, D = q.shape
+    Sk, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q.device
+    dq = torch.empty((B, Sq, N, D), dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty((B, Sk, Nkv, D), dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty((B, Sk, Nkv, D), dtype=torch.float32, device=dev) if dv is None else dv
+    L = _lib.lib()
+    n = ctypes.c_size_t(0)
+    _lib.check("cp_attn_bwd_workspace_size", L.cp_attn_bwd_workspace_size(B, Sq, N, ctypes.byref(n)))
+    if workspace is None:
+        workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
+    st = L.cp_attn_bwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(q_pos), _ptr(k_pos), B,
+                               Sq, Sk, N, Nkv, D, float(scale), _ptr(dq), _ptr(dk), _ptr(dv), 1 if accumulate else 0,
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _lib.check("cp_attn_bwd_partial", st)
+    return dq, dk, dv
+
+
+def cp_ring_bwd_workspace_size(B, S, N, C):
+    n = ctypes.c_size_t(0)
+    _lib.check("cp_ring_bwd_workspace_size", _lib.lib().cp_ring_bwd_workspace_size(B, S, N, C, ctypes.byref(n)))
+    return n.value
+
+
+def cp_ring_attention_bwd(q_sh, k_sh, v_sh, o_sh, lse_sh, do_sh, pos, scale=None, layout=CP_ZIGZAG, workspace=None,
+                          dq=None, dk=None, dv=None, stream=None):
+    """Ring backward over C resident virtual ranks -> (dq_sh, dk_sh, dv_sh) fp32, rank-major."""
+    C, B, s, N, D = q_sh.shape
+    Nkv = k_sh.shape[3]
+    S = C * s
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q_sh.device
+    dq = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty((C, B, s, Nkv, D), dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty((C, B, s, Nkv, D), dtype=torch.float32, device=dev) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(256, cp_ring_bwd_workspace_size(B, S, N, C)), dtype=torch.uint8, device=dev)
+    st = _lib.lib().cp_ring_attention_bwd(_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(o_sh), _ptr(lse_sh), _ptr(do_sh),
+                                          _ptr(pos), B, S, N, Nkv, D, C, float(scale), layout, _ptr(dq), _ptr(dk),
+                                          _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    _lib.check("cp_ring_attention_bwd", st)
+    return dq, dk, dv
+
+
 def cp_ring_attention_fwd_noalloc(q_sh, k_sh, v_sh, pos, o, lse, scale=None, layout=CP_ZIGZAG, o_dtype=CP_F32,
                                   stream=None):
     """Ring forward that allocates nothing: for callers that may not call

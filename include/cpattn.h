@@ -309,6 +309,63 @@ cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, const void *
                                 void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * cp_attn_bwd_workspace_size / cp_attn_bwd_partial -- backward of one
+ * partial attention ("tile backward"): [OCP] Peer-to-peer / Backward,
+ * attention_tile_backward(q, k, v, output, grad_output, lse, q_positions,
+ * kv_positions, scale) -> (dq, dk, dv).  It takes the FINAL output and lse of
+ * the attention the tile belongs to, so p_ij = e^{scale <q_i,k_j> - lse_i}
+ * over visible pairs (k_pos[j] <= q_pos[i]), and
+ *   dv_j = sum_i p_ij dO_i,  ds_ij = p_ij (<dO_i, v_j> - <dO_i, o_i>),
+ *   dq_i = scale sum_j ds_ij k_j,  dk_j = scale sum_i ds_ij q_i
+ * (the chain rule of the forward; a KV head's gradients sum over its query
+ * heads).  P and dS enter the tensor cores as bf16; accumulation is fp32.
+ *   q, dout : device bf16 [B][Sq][N][D]; k, v : device bf16 [B][Sk][Nkv][D]
+ *   o       : device fp32 [B][Sq][N][D], the final output
+ *   lse     : device fp32 [B][N][Sq], the final natural-log log-sum-exp
+ *             (-inf: the row sees nothing and contributes nothing)
+ *   q_pos, k_pos : device int32 [Sq], [Sk]
+ *   D in {64, 128}; N % Nkv == 0; scale finite and > 0
+ *   dq : device fp32 [B][Sq][N][D]; dk, dv : device fp32 [B][Sk][Nkv][D];
+ *        32-byte aligned; written, or added to when accumulate != 0
+ *   workspace : device, >= cp_attn_bwd_workspace_size(B, Sq, N) bytes,
+ *        256-byte aligned (per-row statistics)
+ * Other pointers 16-byte aligned.  Limits (else CP_ERR_SHAPE):
+ * ceil(Sk/128) + ceil(Sq/64) <= 4096 and ceil(Sq/128) + ceil(Sk/64) <= 4096.
+ */
+cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t N, size_t *bytes);
+cp_status cp_attn_bwd_partial(const void *q, const void *k, const void *v, const float *o, const void *dout,
+                              const float *lse, const int32_t *q_pos, const int32_t *k_pos, int64_t B,
+                              int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv, int64_t D, float scale, float *dq,
+                              float *dk, float *dv, int accumulate, void *workspace, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
+ * cp_ring_bwd_workspace_size / cp_ring_attention_bwd -- ring (P2P)
+ * context-parallel attention backward for C virtual ranks.
+ * [OCP] Peer-to-peer / Backward: at step = 0 .. C-1 rank r holds the K/V
+ * block of owner (r - step) mod C and its travelling dK/dV accumulators; the
+ * tile backward of rank r's queries against it (with rank r's final output
+ * and lse from the forward) adds to rank r's dq and to the block's dk/dv,
+ * which are back on their owner after the full rotation.  On one GPU the
+ * travelling accumulators are the owners' own dk_sh / dv_sh; every step is one
+ * dK/dV launch and one dQ launch over all C ranks.
+ *   q_sh, do_sh : device bf16 [C][B][S/C][N][D]; k_sh, v_sh : [C][B][S/C][Nkv][D]
+ *   o_sh  : device fp32 [C][B][S/C][N][D], lse_sh : fp32 [C][B][N][S/C]
+ *           (cp_ring_attention_fwd's outputs with o_dtype CP_F32)
+ *   pos   : device int32 [C][S/C]
+ *   dq_sh : device fp32 [C][B][S/C][N][D]; dk_sh, dv_sh : [C][B][S/C][Nkv][D];
+ *           written (32-byte aligned)
+ *   workspace : device, >= cp_ring_bwd_workspace_size bytes, 256-byte aligned
+ * Everything is validated before anything is enqueued.
+ */
+cp_status cp_ring_bwd_workspace_size(int64_t B, int64_t S, int64_t N, int C, size_t *bytes);
+cp_status cp_ring_attention_bwd(const void *q_sh, const void *k_sh, const void *v_sh, const float *o_sh,
+                                const float *lse_sh, const void *do_sh, const int32_t *pos, int64_t B, int64_t S,
+                                int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout,
+                                float *dq_sh, float *dk_sh, float *dv_sh, void *workspace, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/*
  * cp_ring_attention_fwd_noalloc -- cp_ring_attention_fwd for callers that
  * cannot allocate device memory.  The source pages have no counterpart: this
  * entry point exists for callers that may not call cudaMalloc or cannot hand
