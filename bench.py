@@ -643,6 +643,60 @@ def run_strategies(args):
     return 0
 
 
+def run_backward(args):
+    """One JSON line per workload: the ring backward (statistics, then per ring
+    step one dK/dV and one dQ launch) on the full workload, after a ring
+    forward that supplies o and lse.  TFLOP/s on the algorithmic backward
+    FLOPs, 10 D per visible (query, key) pair per head (five products: S, dP,
+    dV, dK, dQ; 2.5x the forward); the kernels also recompute S and dP in the
+    dQ pass (14 D per pair executed), reported as well."""
+    import torch
+
+    import cp_synth as SY
+    from context_causal_attention_gb300 import build as cuda_build
+    from context_causal_attention_gb300 import ops as F
+
+    cuda_build.build()
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    for wname in args.backward.split(","):
+        w = SY.WORKLOADS[wname]
+        q, k, v, _ = SY.make_qkv(w)
+        g = torch.Generator("cpu").manual_seed(1)
+        do = torch.randn(w.B, w.S, w.N, w.D, generator=g).to(torch.bfloat16)
+        qs, ks, vs, dos = (F.cp_zigzag_shard(t.to(dev), w.C) for t in (q, k, v, do))
+        del q, k, v, do
+        pos = F.cp_zigzag_positions(w.S, w.C, device=dev)
+        o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, prefetch=1)
+        ws = torch.empty(max(256, F.cp_ring_bwd_workspace_size(w.B, w.S, w.N, w.C)), dtype=torch.uint8, device=dev)
+        dq, dk, dv = (torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (qs, ks, vs))
+
+        def bwd():
+            F.cp_ring_attention_bwd(qs, ks, vs, o_sh, lse_sh, dos, pos, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+        for _ in range(max(3, args.warmup)):
+            bwd()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps)
+        e0.record()
+        for _ in range(reps):
+            bwd()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        pairs = w.S * (w.S + 1) / 2 * w.B * w.N
+        alg = 10.0 * w.D * pairs
+        print(json.dumps({"backward": w.name, "S": w.S, "C": w.C, "N": w.N, "D": w.D, "ms": ms,
+                          "tflops_algorithmic": alg / (ms * 1e-3) / 1e12,
+                          "tflops_executed": 1.4 * alg / (ms * 1e-3) / 1e12,
+                          "frac_of_sustained_bf16": alg / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                          "status": F.cp_device_status()}), flush=True)
+        del qs, ks, vs, dos, o_sh, lse_sh, ws, dq, dk, dv
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -658,12 +712,16 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="run the contiguous-vs-zigzag sweep instead")
     ap.add_argument("--strategies", default="",
                     help="comma-separated workloads: time ring / all-gather / Ulysses / mesh forwards instead")
+    ap.add_argument("--backward", default="",
+                    help="comma-separated workloads: time the ring backward instead")
     ap.add_argument("--sweep-only", default="", help="comma-separated sweep workload names")
     args = ap.parse_args()
     if args.sweep:
         return run_sweep(args)
     if args.strategies:
         return run_strategies(args)
+    if args.backward:
+        return run_backward(args)
     import cp_synth as SY
     w = SY.WORKLOADS.get(args.workload)
     if w is None:
