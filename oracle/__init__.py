@@ -44,6 +44,8 @@ def _load():
         lib.orc_ring_fwd.argtypes = [dp, dp, dp, ip, L, L, L, L, L, I, Dd, dp, dp, I]
         lib.orc_pair_counts.argtypes = [ip, L, I, vp]
         lib.orc_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ip, ip, L, L, L, L, L, L, Dd, dp, dp, dp, I]
+        lib.orc_attn_bwd_rows.argtypes = [dp, dp, dp, dp, ip, ip, L, L, L, L, L, L, Dd, vp, L, dp, I]
+        lib.orc_attn_bwd_keys.argtypes = [dp, dp, dp, dp, ip, ip, L, L, L, L, L, L, Dd, vp, L, dp, dp, I]
         lib.orc_ring_bwd.argtypes = [dp, dp, dp, dp, dp, dp, ip, L, L, L, L, L, I, Dd, dp, dp, dp, I]
         _lib = lib
     return _lib
@@ -315,6 +317,44 @@ def attn_bwd(q, k, v, o, dout, lse, q_pos, k_pos, scale=None, nthreads=1):
                             D, float(scale), _p(dq), _p(dk), _p(dv), int(nthreads)):
         raise ValueError("attn_bwd: N must be a multiple of Nkv")
     return dq, dk, dv
+
+
+def attn_bwd_rows(q, k, v, dout, q_pos, k_pos, rows, scale=None, nthreads=1):
+    """dq of the chosen query rows -> [B, len(rows), N, D], everything
+    (lse, o, delta of each row) recomputed from q, k, v.
+
+    "On Context Parallelism", Peer-to-peer / Backward (tile backward definitions).
+    """
+    q, k, v, dout = (_f64(x) for x in (q, k, v, dout))
+    q_pos, k_pos = _i32(q_pos), _i32(k_pos)
+    B, Sq, N, D = q.shape
+    Sk, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((B, len(rows), N, D))
+    if _load().orc_attn_bwd_rows(_p(q), _p(k), _p(v), _p(dout), _p(q_pos), _p(k_pos), B, Sq, Sk, N, Nkv, D,
+                                 float(scale), _p(rows), len(rows), _p(out), int(nthreads)):
+        raise ValueError("attn_bwd_rows: bad arguments")
+    return out
+
+
+def attn_bwd_keys(q, k, v, dout, q_pos, k_pos, keys, scale=None, nthreads=1):
+    """(dk, dv) of the chosen keys -> [B, len(keys), Nkv, D] each, with every
+    query row that sees a key recomputed from q, k, v (cheap for late keys)."""
+    q, k, v, dout = (_f64(x) for x in (q, k, v, dout))
+    q_pos, k_pos = _i32(q_pos), _i32(k_pos)
+    B, Sq, N, D = q.shape
+    Sk, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    keys = np.ascontiguousarray(keys, dtype=np.int64)
+    dk = np.empty((B, len(keys), Nkv, D))
+    dv = np.empty((B, len(keys), Nkv, D))
+    if _load().orc_attn_bwd_keys(_p(q), _p(k), _p(v), _p(dout), _p(q_pos), _p(k_pos), B, Sq, Sk, N, Nkv, D,
+                                 float(scale), _p(keys), len(keys), _p(dk), _p(dv), int(nthreads)):
+        raise ValueError("attn_bwd_keys: bad arguments")
+    return dk, dv
 
 
 def ring_bwd(q_sh, k_sh, v_sh, o_sh, do_sh, lse_sh, pos, scale=None, nthreads=1):

@@ -574,6 +574,157 @@ int orc_attn_bwd(const double *q, const double *k, const double *v, const double
 }
 
 /* ------------------------------------------------------------------------ */
+/* Sampled gradients for sequences too long for orc_attn_bwd.               */
+/*                                                                          */
+/* Same definitions as orc_attn_bwd ([OCP] Peer-to-peer / Backward, the     */
+/* chain rule of the forward), but nothing is taken from a forward output:  */
+/* every row involved gets its lse_i, o_i and delta_i = <dO_i, o_i>          */
+/* recomputed here from q, k, v in fp64.                                     */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    const int32_t *qpos, *kpos;
+    long B, Sq, Sk, N, Nkv, D;
+    double scale;
+    const long *sel; /* sampled query rows (dq) or keys (dk, dv) */
+    long nsel;
+    double *out1, *out2;
+} orc_bwd_sample_job;
+
+/* lse, o and delta of query row i of head h (o written to o_i [D]). */
+static double orc_row_stats(const orc_bwd_sample_job *J, long b, long h, long i, double *o_i, double *delta) {
+    const long D = J->D, N = J->N, Nkv = J->Nkv, hk = h / (N / Nkv);
+    const double *qi = J->q + ((b * J->Sq + i) * N + h) * D;
+    double m = ORC_NEG_INF;
+    int any = 0;
+    for (long j = 0; j < J->Sk; ++j) {
+        if (J->kpos[j] > J->qpos[i]) continue;
+        const double *kj = J->k + ((b * J->Sk + j) * Nkv + hk) * D;
+        double dot = 0.0;
+        for (long d = 0; d < D; ++d) dot += qi[d] * kj[d];
+        const double sj = J->scale * dot;
+        if (!any || sj > m) m = sj;
+        any = 1;
+    }
+    for (long d = 0; d < D; ++d) o_i[d] = 0.0;
+    *delta = 0.0;
+    if (!any) return ORC_NEG_INF;
+    double l = 0.0;
+    for (long j = 0; j < J->Sk; ++j) {
+        if (J->kpos[j] > J->qpos[i]) continue;
+        const double *kj = J->k + ((b * J->Sk + j) * Nkv + hk) * D;
+        double dot = 0.0;
+        for (long d = 0; d < D; ++d) dot += qi[d] * kj[d];
+        l += exp(J->scale * dot - m);
+    }
+    const double lse = m + log(l);
+    for (long j = 0; j < J->Sk; ++j) {
+        if (J->kpos[j] > J->qpos[i]) continue;
+        const double *kj = J->k + ((b * J->Sk + j) * Nkv + hk) * D;
+        const double *vj = J->v + ((b * J->Sk + j) * Nkv + hk) * D;
+        double dot = 0.0;
+        for (long d = 0; d < D; ++d) dot += qi[d] * kj[d];
+        const double p = exp(J->scale * dot - lse);
+        for (long d = 0; d < D; ++d) o_i[d] += p * vj[d];
+    }
+    const double *doi = J->dout + ((b * J->Sq + i) * N + h) * D;
+    for (long d = 0; d < D; ++d) *delta += doi[d] * o_i[d];
+    return lse;
+}
+
+static void orc_bwd_rows_unit(void *arg, long unit) {
+    /* unit = (b, h, sampled row) */
+    const orc_bwd_sample_job *J = (const orc_bwd_sample_job *)arg;
+    const long D = J->D, N = J->N, Nkv = J->Nkv, hk_div = N / Nkv;
+    const long r = unit % J->nsel, bh = unit / J->nsel, b = bh / N, h = bh % N, hk = h / hk_div;
+    const long i = J->sel[r];
+    double *dq = J->out1 + ((b * J->nsel + r) * N + h) * D;
+    for (long d = 0; d < D; ++d) dq[d] = 0.0;
+    double *o_i = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!o_i) return;
+    double delta;
+    const double lse = orc_row_stats(J, b, h, i, o_i, &delta);
+    if (lse != ORC_NEG_INF) {
+        const double *qi = J->q + ((b * J->Sq + i) * N + h) * D;
+        const double *doi = J->dout + ((b * J->Sq + i) * N + h) * D;
+        for (long j = 0; j < J->Sk; ++j) {
+            if (J->kpos[j] > J->qpos[i]) continue;
+            const double *kj = J->k + ((b * J->Sk + j) * Nkv + hk) * D;
+            const double *vj = J->v + ((b * J->Sk + j) * Nkv + hk) * D;
+            double dot = 0.0, dp = 0.0;
+            for (long d = 0; d < D; ++d) {
+                dot += qi[d] * kj[d];
+                dp += doi[d] * vj[d];
+            }
+            const double ds = exp(J->scale * dot - lse) * (dp - delta);
+            for (long d = 0; d < D; ++d) dq[d] += J->scale * ds * kj[d];
+        }
+    }
+    free(o_i);
+}
+
+/* dq of the query rows rows[0..nrows): dq [B][nrows][N][D]. */
+int orc_attn_bwd_rows(const double *q, const double *k, const double *v, const double *dout, const int32_t *qpos,
+                      const int32_t *kpos, long B, long Sq, long Sk, long N, long Nkv, long D, double scale,
+                      const long *rows, long nrows, double *dq, int nthreads) {
+    if (N <= 0 || Nkv <= 0 || N % Nkv != 0) return 1;
+    for (long r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= Sq) return 2;
+    orc_bwd_sample_job J = {q, k, v, dout, qpos, kpos, B, Sq, Sk, N, Nkv, D, scale, rows, nrows, dq, NULL};
+    orc_parallel(orc_bwd_rows_unit, &J, B * N * nrows, nthreads);
+    return 0;
+}
+
+static void orc_bwd_keys_unit(void *arg, long unit) {
+    /* unit = (b, kv head, sampled key): sums over the query heads of the group
+       and over every query row that sees the key */
+    const orc_bwd_sample_job *J = (const orc_bwd_sample_job *)arg;
+    const long D = J->D, N = J->N, Nkv = J->Nkv, g = N / Nkv;
+    const long r = unit % J->nsel, bh = unit / J->nsel, b = bh / Nkv, hk = bh % Nkv;
+    const long j = J->sel[r];
+    double *dk = J->out1 + ((b * J->nsel + r) * Nkv + hk) * D;
+    double *dv = J->out2 + ((b * J->nsel + r) * Nkv + hk) * D;
+    for (long d = 0; d < D; ++d) dk[d] = dv[d] = 0.0;
+    double *o_i = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!o_i) return;
+    const double *kj = J->k + ((b * J->Sk + j) * Nkv + hk) * D;
+    const double *vj = J->v + ((b * J->Sk + j) * Nkv + hk) * D;
+    for (long h = hk * g; h < (hk + 1) * g; ++h)
+        for (long i = 0; i < J->Sq; ++i) {
+            if (J->kpos[j] > J->qpos[i]) continue;
+            double delta;
+            const double lse = orc_row_stats(J, b, h, i, o_i, &delta);
+            const double *qi = J->q + ((b * J->Sq + i) * N + h) * D;
+            const double *doi = J->dout + ((b * J->Sq + i) * N + h) * D;
+            double dot = 0.0, dp = 0.0;
+            for (long d = 0; d < D; ++d) {
+                dot += qi[d] * kj[d];
+                dp += doi[d] * vj[d];
+            }
+            const double p = exp(J->scale * dot - lse);
+            const double ds = p * (dp - delta);
+            for (long d = 0; d < D; ++d) {
+                dv[d] += p * doi[d];
+                dk[d] += J->scale * ds * qi[d];
+            }
+        }
+    free(o_i);
+}
+
+/* dk, dv of the keys keys[0..nkeys): dk, dv [B][nkeys][Nkv][D].  Cost grows
+ * with the number of query rows that see each key (use late keys). */
+int orc_attn_bwd_keys(const double *q, const double *k, const double *v, const double *dout, const int32_t *qpos,
+                      const int32_t *kpos, long B, long Sq, long Sk, long N, long Nkv, long D, double scale,
+                      const long *keys, long nkeys, double *dk, double *dv, int nthreads) {
+    if (N <= 0 || Nkv <= 0 || N % Nkv != 0) return 1;
+    for (long r = 0; r < nkeys; ++r)
+        if (keys[r] < 0 || keys[r] >= Sk) return 2;
+    orc_bwd_sample_job J = {q, k, v, dout, qpos, kpos, B, Sq, Sk, N, Nkv, D, scale, keys, nkeys, dk, dv};
+    orc_parallel(orc_bwd_keys_unit, &J, B * Nkv * nkeys, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Ring backward over C virtual ranks.                                      */
 /*                                                                          */
 /* [OCP] Peer-to-peer / Backward: rank r keeps its queries and accumulates  */

@@ -173,3 +173,46 @@ def test_ring_fwd_then_bwd_end_to_end_vs_direct(cuda_dev):
     for nm, g_, r_ in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
         assert_grad_close("e2e:" + nm, O.unshard(f64(g_), lay_o), r_)
     assert F.cp_device_status() == 0
+
+
+def test_ring_bwd_full_size_sampled(cuda_dev):
+    """S=32768 workload in the benchmark's configuration (ring forward with
+    prefetch, then the ring backward): dq of sampled rows and dk / dv of late
+    keys against the oracle (which recomputes every row it needs from q, k, v),
+    for two heads; and two identities over every key of every head:
+    sum_j dv_j = sum_i dO_i (each row's p sums to 1) and sum_j dk_j = 0 (each
+    row's ds sums to 0)."""
+    w = SY.WORKLOADS["s32k"]
+    (q, k, v, do), (qs, ks, vs, dos), pos, lay, lay_o = ring_setup(w, "zigzag", cuda_dev)
+    o_sh, l_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1)
+    dq, dk, dv = F.cp_ring_attention_bwd(qs, ks, vs, o_sh, l_sh, dos, pos, layout=lay)
+    torch.cuda.synchronize()
+    assert F.cp_device_status() == 0
+    C, s = w.C, w.S // w.C
+    pos_np = pos.cpu().numpy()
+    where = np.empty((w.S, 2), dtype=np.int64)  # global position -> (rank, local row)
+    for r in range(C):
+        where[pos_np[r], 0] = r
+        where[pos_np[r], 1] = np.arange(s)
+    heads = [0, 17]
+    gp = np.arange(w.S, dtype=np.int32)
+    sub = [f64(t[:, :, heads]) for t in (q, k, v, do)]
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, 127, 128, 4095, 4096, w.S - 1], rng.integers(0, w.S, 58)]))
+    ref_dq = O.attn_bwd_rows(*sub, gp, gp, rows, nthreads=NTH)
+    got_dq = np.stack([f64(dq[where[i, 0], :, where[i, 1]][:, heads]) for i in rows], axis=1)
+    assert_grad_close("dq rows", got_dq, ref_dq)
+    keys = np.arange(w.S - 96, w.S, 3)
+    ref_dk, ref_dv = O.attn_bwd_keys(*sub, gp, gp, keys, nthreads=NTH)
+    got_dk = np.stack([f64(dk[where[j, 0], :, where[j, 1]][:, heads]) for j in keys], axis=1)
+    got_dv = np.stack([f64(dv[where[j, 0], :, where[j, 1]][:, heads]) for j in keys], axis=1)
+    assert_grad_close("dk keys", got_dk, ref_dk)
+    assert_grad_close("dv keys", got_dv, ref_dv)
+    # identities over all keys (N == Nkv here): per (b, head, d)
+    sum_dv = dv.double().sum(dim=(0, 2)).cpu().numpy()             # [B, Nkv, D]
+    sum_do = dos.double().sum(dim=(0, 2)).cpu().numpy()
+    norm_do = np.sqrt((dos.double() ** 2).sum(dim=(0, 2)).cpu().numpy())
+    assert np.max(np.abs(sum_dv - sum_do) / norm_do) <= 1e-2
+    sum_dk = dk.double().sum(dim=(0, 2)).cpu().numpy()
+    norm_dk = np.sqrt((dk.double() ** 2).sum(dim=(0, 2)).cpu().numpy())
+    assert np.max(np.abs(sum_dk) / norm_dk) <= 1e-2

@@ -629,3 +629,20 @@ def test_ring_bwd_equals_direct(C, layout):
     g = O.ring_bwd(*(O.shard(x, C, layout) for x in (q, k, v)), o_sh, O.shard(dout, C, layout), l_sh, pos)
     for got, want in zip(g, (dq, dk, dv)):
         np.testing.assert_allclose(O.unshard(got, layout), want, atol=1e-12)
+
+
+def test_bwd_sampled_rows_and_keys_equal_full():
+    """The sampled-gradient functions (which recompute lse, o and delta per
+    row) agree with the full backward on every chosen row and key."""
+    B, Sq, Sk, N, Nkv, D = 2, 23, 19, 4, 2, 5
+    q, k, v, dout = randn(B, Sq, N, D), randn(B, Sk, Nkv, D), randn(B, Sk, Nkv, D), randn(B, Sq, N, D)
+    qp = np.random.default_rng(3).integers(0, 25, Sq).astype(np.int32)
+    kp = np.random.default_rng(4).integers(0, 25, Sk).astype(np.int32)
+    o, lse = O.attn_direct(q, k, v, qp, kp)
+    dq, dk, dv = O.attn_bwd(q, k, v, o, dout, lse, qp, kp)
+    rows = [0, 5, 22, 7]
+    keys = [18, 0, 3]
+    np.testing.assert_allclose(O.attn_bwd_rows(q, k, v, dout, qp, kp, rows, nthreads=3), dq[:, rows], atol=1e-13)
+    sk, sv = O.attn_bwd_keys(q, k, v, dout, qp, kp, keys, nthreads=3)
+    np.testing.assert_allclose(sk, dk[:, keys], atol=1e-13)
+    np.testing.assert_allclose(sv, dv[:, keys], atol=1e-13)
