@@ -659,8 +659,9 @@ def run_backward(args):
     cuda_build.build()
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
+    sweep = {x.name: x for x in SY.sweep_workloads()}
     for wname in args.backward.split(","):
-        w = SY.WORKLOADS[wname]
+        w = SY.WORKLOADS.get(wname) or sweep[wname]
         q, k, v, _ = SY.make_qkv(w)
         g = torch.Generator("cpu").manual_seed(1)
         do = torch.randn(w.B, w.S, w.N, w.D, generator=g).to(torch.bfloat16)

@@ -17,25 +17,32 @@
 //   bwd_stats_kernel  per query row: nl2 = -lse log2(e) (-inf for rows that see
 //                     nothing and for padding) and nd = -delta; HBM-bound.
 //   bwd_dkdv_kernel   K/V-stationary.  Work item = (rank, b, KV head, 128-key
-//                     tile); it streams the 64-row Q / dO tiles (of every query
+//                     tile); it streams the 128-row Q / dO tiles (of every query
 //                     head of the group) that can see the keys and keeps
 //                     dV += P^T dO and dK += dS^T Q in TMEM.
 //   bwd_dq_kernel     Q-stationary.  Work item = (rank, b, head, 128-query tile);
-//                     it streams the 64-key K / V tiles the queries can see and
+//                     it streams the 128-key K / V tiles the queries can see and
 //                     keeps dQ += dS K in TMEM.
-// S and dP are formed in both (seven 128x64xD-class products per tile pair
+// S and dP are formed in both (seven 128x128xD-class products per tile pair
 // instead of five), in exchange for no atomics and deterministic sums.
 //
-// Both kernels: one persistent CTA per SM, 192 threads.
-//   warp 0      TMA producer (stationary tiles once per item, a 3-stage ring
+// Both kernels: one persistent CTA per SM, 384 threads.
+//   warp 0      TMA producer (stationary tiles once per item, a 2-stage ring
 //               of streamed tiles);
 //   warp 1      TMEM allocator (512 columns) and the single MMA-issuing thread;
-//   warps 2-5   compute: one thread per TMEM lane (row of the stationary
-//               tile); TMEM lane quarter = warp % 4.
-// TMEM: two buffers b = 0, 1 of 128 columns (scores 64 | dP 64, each a
-// 128 x 64 fp32 block; P / dS are written back over them as packed bf16) and
-// the fp32 accumulators from column 256 (dV | dK, or dQ).  The MMA for
-// streamed tile t + 1 runs while the compute warps work on tile t.
+//   warps 2-3   idle;
+//   warps 4-11  compute: two warps per TMEM lane quarter (quarter = warp % 4,
+//               one row of the stationary tile per thread); warps 4-7 take
+//               columns 0..31 of every 64-column half, warps 8-11 columns
+//               32..63, so two warps per SM sub-partition hide each other's
+//               shared-memory and TMEM latencies.
+// TMEM: scores S (or S^T) in columns 0..127, dP in 128..255 (128 x 128 fp32
+// each, all products N = 128), then the fp32 accumulators (dV | dK, or dQ).
+// The compute warps work through a streamed tile in two 64-column halves and
+// write P / dS back over columns they have read, as packed bf16; the
+// gradient MMAs of the first half (K = 64) run while the second half is
+// computed.  The next tile's S and dP are issued after both halves' gradient
+// MMAs (the tensor pipe runs them in order).
 // Every mbarrier wait is bounded (2 s); a CTA that times out unwinds, lets its
 // copies and MMAs land, frees TMEM and records CP_ERR_DEVICE_TIMEOUT.
 #include <cuda.h>
@@ -55,56 +62,56 @@ namespace {
 
 __device__ int g_cp_bwd_status = 0;
 
-constexpr int kBThreads = 192;
-constexpr int kBStages = 3;
+constexpr int kBThreads = 384;  // three warps per SM sub-partition: at most 168 registers
+constexpr int kBStages = 2;
 constexpr uint32_t kBTmemCols = 512;
 constexpr uint32_t kNegInfBits = 0xff800000u;
+constexpr int kComputeWarps = 8;
 
 template <int D>
 struct Tiles {
     static constexpr int kAtoms = D / 64;
-    static constexpr int kBig = 128 * D * 2;    // 128-row bf16 tile
-    static constexpr int kSmall = 64 * D * 2;   // 64-row bf16 tile
-    static constexpr int kAtomBig = 128 * 128;  // one 64-column swizzle atom of a 128-row tile
-    static constexpr int kAtomSmall = 64 * 128; // ... of a 64-row tile
+    static constexpr int kTile = 128 * D * 2;   // 128-row bf16 tile
+    static constexpr int kAtom = 128 * 128;     // one 64-column swizzle atom of it
 };
 
-// K/V-stationary kernel: K, V (128 rows) | Q, dO stages (64 rows) | nl2/nd
-// strips per stage | tables | order | cost | barriers | misc.
+// K/V-stationary kernel: K, V | Q, dO stages | nl2/nd strips per stage |
+// tables | order | cost | barriers | misc.
 template <int D>
 struct CfgKV : Tiles<D> {
     using T = Tiles<D>;
     static constexpr int kOffK = 0;
-    static constexpr int kOffV = T::kBig;
-    static constexpr int kOffQ = 2 * T::kBig;
-    static constexpr int kOffDO = kOffQ + kBStages * T::kSmall;
-    static constexpr int kOffStat = kOffDO + kBStages * T::kSmall;  // per stage: nl2[64] | nd[64]
-    static constexpr int kOffTab = kOffStat + kBStages * 512;
+    static constexpr int kOffV = T::kTile;
+    static constexpr int kOffQ = 2 * T::kTile;
+    static constexpr int kOffDO = kOffQ + kBStages * T::kTile;
+    static constexpr int kOffStat = kOffDO + kBStages * T::kTile;  // per stage: nl2[128] | nd[128]
+    static constexpr int kOffTab = kOffStat + kBStages * 1024;
     static constexpr int kOffOrder = kOffTab + kBwdMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kBwdMaxPairs * 4;
     static constexpr int kOffBar = kOffCost + kBwdMaxPairs * 4;
-    // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full[2], p_full[2], o_full, o_empty, drain
-    static constexpr int kNumBars = 2 + 2 * kBStages + 7;
+    // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full, p_half, p_full, o_full, o_empty, drain
+    // (p_half, p_full, o_empty: one arrival per compute warp)
+    static constexpr int kNumBars = 2 + 2 * kBStages + 6;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMiscBytes = 16 + kMaxC * 4 + kBwdMaxTables / 8;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Q-stationary kernel: Q, dO (128 rows) | K, V stages (64 rows) | tables | ...
+// Q-stationary kernel: Q, dO | K, V stages | tables | order | cost | ...
 template <int D>
 struct CfgQ : Tiles<D> {
     using T = Tiles<D>;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffDO = T::kBig;
-    static constexpr int kOffK = 2 * T::kBig;
-    static constexpr int kOffV = kOffK + kBStages * T::kSmall;
-    static constexpr int kOffTab = kOffV + kBStages * T::kSmall;
+    static constexpr int kOffDO = T::kTile;
+    static constexpr int kOffK = 2 * T::kTile;
+    static constexpr int kOffV = kOffK + kBStages * T::kTile;
+    static constexpr int kOffTab = kOffV + kBStages * T::kTile;
     static constexpr int kOffOrder = kOffTab + kBwdMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kBwdMaxPairs * 4;
     static constexpr int kOffBar = kOffCost + kBwdMaxPairs * 4;
-    // qd_full, qd_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full, o_empty, drain
-    static constexpr int kNumBars = 2 + 2 * kBStages + 7;
+    // qd_full, qd_empty, kv_full[S], kv_empty[S], s_full, p_half, p_full, o_full, o_empty, drain
+    static constexpr int kNumBars = 2 + 2 * kBStages + 6;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMiscBytes = 16 + kMaxC * 4 + kBwdMaxTables / 8;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
@@ -118,7 +125,7 @@ struct BwdArgs {
     long long sq_pad;
     float *dq, *dk, *dv;
     int C, B, N, Nkv, Sq, Sk;
-    int nq, nk;  // query / key tiles in the kernel's own tile heights
+    int nq, nk;  // 128-row query / key tiles
     int kv_shift, kpos_shift, kpr;
     int accumulate;
     float scale, scale_log2;
@@ -126,15 +133,13 @@ struct BwdArgs {
     FastDiv div_bh, div_nt, div_h;  // by B * (heads per item), stationary tiles per rank, heads per item
 };
 
-// (min, max) of the positions of one tile of T rows (one warp per tile); when
+// (min, max) of the positions of one 128-row tile (one warp per tile); when
 // `arith` is given, bit g is set if the positions are p, p+1, p+2, ...
-template <int T>
 __device__ __forceinline__ void tile_table(const int32_t *p, int row0, int lim, int lane, int2 *out, uint32_t *arith,
                                            int g) {
-    constexpr int kPer = T / 32;
-    int mn = INT_MAX, mx = INT_MIN, vals[kPer];
+    int mn = INT_MAX, mx = INT_MIN, vals[4];
 #pragma unroll
-    for (int m = 0; m < kPer; ++m) {
+    for (int m = 0; m < 4; ++m) {
         const int row = row0 + lane + 32 * m;
         vals[m] = (row < lim) ? __ldg(p + row) : 0;
         if (row < lim) {
@@ -149,7 +154,7 @@ __device__ __forceinline__ void tile_table(const int32_t *p, int row0, int lim, 
         const int first = __shfl_sync(0xffffffffu, vals[0], 0);
         bool ok = true;
 #pragma unroll
-        for (int m = 0; m < kPer; ++m) {
+        for (int m = 0; m < 4; ++m) {
             const int row = row0 + lane + 32 * m;
             if (row < lim) ok &= (static_cast<long long>(vals[m]) == static_cast<long long>(first) + lane + 32 * m);
         }
@@ -259,6 +264,14 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Releases one half of a streamed tile to the MMA issuer (warp-collective).
+__device__ __forceinline__ void release_half(uint64_t *bar, int lane) {
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
 // ======================================================================
 // dK / dV: K/V-stationary
 // ======================================================================
@@ -282,10 +295,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per query tile
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
     uint64_t *kv_full = bar, *kv_empty = bar + 1, *qd_full = bar + 2, *qd_empty = bar + 2 + kBStages;
-    uint64_t *s_full = bar + 2 + 2 * kBStages, *p_full = s_full + 2, *o_full = s_full + 4, *o_empty = s_full + 5,
-             *drain = s_full + 6;
-    const int2 *ktab = tab;                 // [kpr][nk] 128-key tiles
-    const int2 *qtab = tab + a.kpr * a.nk;  // [C][nq] 64-query tiles
+    uint64_t *s_full = bar + 2 + 2 * kBStages, *p_half = s_full + 1, *p_full = s_full + 2, *o_full = s_full + 3,
+             *o_empty = s_full + 4, *drain = s_full + 5;
+    const int2 *ktab = tab;                 // [kpr][nk] key tiles
+    const int2 *qtab = tab + a.kpr * a.nk;  // [C][nq] query tiles
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -296,12 +309,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
             mbar_init(qd_full + s, 1);
             mbar_init(qd_empty + s, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full + i, 1);
-            mbar_init(p_full + i, 4);
-        }
+        mbar_init(s_full, 1);
+        mbar_init(p_half, kComputeWarps);
+        mbar_init(p_full, kComputeWarps);
         mbar_init(o_full, 1);
-        mbar_init(o_empty, 4);
+        mbar_init(o_empty, kComputeWarps);
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -321,10 +333,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int g = warp; g < total; g += kBThreads / 32) {
             if (g < nkk) {
                 const int j = g / a.nk, kt = g - (g / a.nk) * a.nk;
-                tile_table<128>(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab + g, nullptr, 0);
+                tile_table(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab + g, nullptr, 0);
             } else {
                 const int gq = g - nkk, r = gq / a.nq, qt = gq - (gq / a.nq) * a.nq;
-                tile_table<64>(a.q_pos + r * a.q_pos_stride, qt * 64, a.Sq, lane, tab + g, arith_bits, gq);
+                tile_table(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab + g, arith_bits, gq);
             }
         }
     }
@@ -381,12 +393,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 decode(idx, r, kt, b, hk, owner, kvr, pr);
                 if (cost[pr] == 0) continue;
                 if (!mbar_wait(kv_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(kv_full, 2 * K::kBig);
+                mbar_arrive_expect_tx(kv_full, 2 * K::kTile);
                 kv_par = static_cast<int>(it & 1u);
                 const int kvrow = kvr * a.B + b;
                 for (int at = 0; at < K::kAtoms; ++at) {
-                    tma_load_4d(sK + at * K::kAtomBig, &tmK, kv_full, 64 * at, hk, kt * 128, kvrow);
-                    tma_load_4d(sV + at * K::kAtomBig, &tmV, kv_full, 64 * at, hk, kt * 128, kvrow);
+                    tma_load_4d(sK + at * K::kAtom, &tmK, kv_full, 64 * at, hk, kt * 128, kvrow);
+                    tma_load_4d(sV + at * K::kAtom, &tmV, kv_full, 64 * at, hk, kt * 128, kvrow);
                 }
                 ++it;
                 const int2 *qt_r = qtab + r * a.nq;
@@ -399,15 +411,15 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     for (int qt = first_q(qt_r, a.nq, kmin, srt); qt < a.nq; qt = next_q(qt + 1, qt_r, a.nq, kmin)) {
                         const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
                         if (!mbar_wait(qd_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                        mbar_arrive_expect_tx(qd_full + st, 2 * K::kSmall + 512);
+                        mbar_arrive_expect_tx(qd_full + st, 2 * K::kTile + 1024);
                         for (int at = 0; at < K::kAtoms; ++at) {
-                            tma_load_4d(sQ + st * K::kSmall + at * K::kAtomSmall, &tmQ, qd_full + st, 64 * at, h,
-                                        qt * 64, qrow);
-                            tma_load_4d(sDO + st * K::kSmall + at * K::kAtomSmall, &tmDO, qd_full + st, 64 * at, h,
-                                        qt * 64, qrow);
+                            tma_load_4d(sQ + st * K::kTile + at * K::kAtom, &tmQ, qd_full + st, 64 * at, h, qt * 128,
+                                        qrow);
+                            tma_load_4d(sDO + st * K::kTile + at * K::kAtom, &tmDO, qd_full + st, 64 * at, h, qt * 128,
+                                        qrow);
                         }
-                        tma_load_2d(sStat + st * 128, &tmNL2, qd_full + st, qt * 64, srow);
-                        tma_load_2d(sStat + st * 128 + 64, &tmND, qd_full + st, qt * 64, srow);
+                        tma_load_2d(sStat + st * 256, &tmNL2, qd_full + st, qt * 128, srow);
+                        tma_load_2d(sStat + st * 256 + 128, &tmND, qd_full + st, qt * 128, srow);
                         qd_issued |= 1u << st;
                         qd_par = (qd_par & ~(1u << st)) | (ph << st);
                         ++t;
@@ -427,28 +439,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, 0, 0);  // S^T, dP^T: 128 keys x 64 queries
-            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B operand MN-major
-            constexpr uint64_t kStU = K::kSmall >> 4;                 // one stage, descriptor units
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: 128 keys x 128 queries
+            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B operand MN-major
+            constexpr uint64_t kStU = K::kTile >> 4;                   // one stage, descriptor units
+            constexpr uint64_t kHalfU = (64 * 128) >> 4;               // 64 rows of a swizzled tile
             const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024), dV = smem_desc_sw128(smem_u32(sV), 16, 1024);
             const uint64_t dQk = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dOk = smem_desc_sw128(smem_u32(sDO), 16, 1024);
-            const uint64_t dQm = smem_desc_sw128(smem_u32(sQ), K::kAtomSmall, 1024);
-            const uint64_t dOm = smem_desc_sw128(smem_u32(sDO), K::kAtomSmall, 1024);
+            const uint64_t dQm = smem_desc_sw128(smem_u32(sQ), K::kAtom, 1024);
+            const uint64_t dOm = smem_desc_sw128(smem_u32(sDO), K::kAtom, 1024);
             uint32_t it = 0, t = 0;
             bool ok = true;
-            // dV += P^T dO and dK += dS^T Q for streamed tile pt (P^T / dS^T in
-            // TMEM buffer pt & 1); `first` overwrites the accumulators
-            auto grads = [&](uint32_t pt, bool first) -> bool {
-                const uint32_t pb = pt & 1u, pst = pt % kBStages;
-                if (!mbar_wait(p_full + pb, (pt >> 1) & 1u, abort_flag, a.timeout_ns)) return false;
-                if (first && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) return false;
-                tc_fence_after();
-                umma_ts_k64(tmem + 256, tmem + pb * 128, dOm + pst * kStU, kIdG, first ? 0u : 1u);
-                umma_ts_k64(tmem + 256 + D, tmem + pb * 128 + 64, dQm + pst * kStU, kIdG, first ? 0u : 1u);
-                umma_commit(qd_empty + pst);
-                return true;
-            };
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
@@ -458,19 +459,30 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 if (n == 0) continue;
                 if (!mbar_wait(kv_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
-                for (int i = 0; i < n; ++i) {
-                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u, bb = t & 1u;
+                for (int i = 0; i < n; ++i, ++t) {
+                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
                     if (!mbar_wait(qd_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128, dK, dQk + st * kStU, kIdS);
-                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128 + 64, dV, dOk + st * kStU, kIdS);
-                    umma_commit(s_full + bb);
+                    // S^T and dP^T overwrite the previous tile's P^T / dS^T: in
+                    // issue order after that tile's gradient MMAs
+                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem, dK, dQk + st * kStU, kIdS);
+                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem + 128, dV, dOk + st * kStU, kIdS);
+                    umma_commit(s_full);
                     if (i == n - 1) umma_commit(kv_empty);  // K and V are read by S^T / dP^T only
-                    if (i > 0 && !grads(t - 1, i == 1)) { ok = false; break; }
-                    ++t;
+                    // dV += P^T dO, dK += dS^T Q over the tile's first 64 queries,
+                    // then over the second 64; `first` overwrites the accumulators
+                    if (!mbar_wait(p_half, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    if (i == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_ts_k64_split(tmem + 256, tmem, dOm + st * kStU, kIdG, i == 0 ? 0u : 1u);
+                    umma_ts_k64_split(tmem + 256 + D, tmem + 128, dQm + st * kStU, kIdG, i == 0 ? 0u : 1u);
+                    if (!mbar_wait(p_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_ts_k64_split(tmem + 256, tmem + 64, dOm + st * kStU + kHalfU, kIdG, 1u);
+                    umma_ts_k64_split(tmem + 256 + D, tmem + 192, dQm + st * kStU + kHalfU, kIdG, 1u);
+                    umma_commit(qd_empty + st);
                 }
                 if (!ok) break;
-                if (!grads(t - 1, n == 1)) { ok = false; break; }
                 umma_commit(o_full);
                 ++it;
             }
@@ -480,13 +492,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
             mbar_wait(drain, 0, &no_abort, 100000000ull);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // -------------------------------------------------------- compute (one key row per thread)
         const int quarter = warp & 3;
+        const int grp = (warp - 4) >> 2;  // columns 32 grp .. 32 grp + 31 of each half
         const int row_in = quarter * 32 + lane;
         const uint32_t tA = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const float sl2 = a.scale_log2;
-        const uint64_t sl2x2 = f2_packf(sl2, sl2);
+        const uint64_t sl2x2 = f2_packf(a.scale_log2, a.scale_log2);
         uint32_t it = 0, t = 0;
         bool ok = true;
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
@@ -498,13 +510,14 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const bool key_valid = key < a.Sk;
             const int kpos = key_valid ? __ldg(a.k_pos + owner * a.k_pos_stride + key) : INT_MAX;
             const long long krow = (static_cast<long long>(kvr * a.B + b) * a.Sk + key) * a.Nkv + hk;
-            float *dk_row = a.dk + krow * D;
-            float *dv_row = a.dv + krow * D;
+            // each group writes half of the row's D columns
+            float *dk_row = a.dk + krow * D + grp * (D / 2);
+            float *dv_row = a.dv + krow * D + grp * (D / 2);
             if (cost[pr] == 0) {
                 // no query sees these keys: their gradients are zero
                 if (key_valid && !a.accumulate) {
-                    zero_row<D>(dk_row);
-                    zero_row<D>(dv_row);
+                    zero_row<D / 2>(dk_row);
+                    zero_row<D / 2>(dv_row);
                 }
                 continue;
             }
@@ -513,75 +526,84 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const bool srt = sorted_flag[r] != 0;
             const int32_t *qpos_r = a.q_pos + r * a.q_pos_stride;
             for (int hh = 0; hh < g_heads && ok; ++hh) {
-                for (int qt = first_q(qt_r, a.nq, kmm.x, srt); qt < a.nq; qt = next_q(qt + 1, qt_r, a.nq, kmm.x)) {
-                    const uint32_t bb = t & 1u, st = t % kBStages;
-                    if (!mbar_wait_warp(s_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                for (int qt = first_q(qt_r, a.nq, kmm.x, srt); qt < a.nq;
+                     qt = next_q(qt + 1, qt_r, a.nq, kmm.x), ++t) {
+                    const uint32_t st = t % kBStages;
+                    if (!mbar_wait_warp(s_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    uint32_t s[64], dp[64];
-                    tmem_ld64_nowait(tA + bb * 128, s);
-                    tmem_ld64_nowait(tA + bb * 128 + 64, dp);
-                    tmem_wait_ld(s);
-                    tmem_wait_ld(dp);
                     const int2 qmm = qt_r[qt];
-                    const int q0 = qt * 64;
-                    const int nvalid = min(64, a.Sq - q0);
-                    if (kmm.y > qmm.x || nvalid < 64) {
-                        const int gq = r * a.nq + qt;
-                        if ((arith_bits[gq >> 5] >> (gq & 31)) & 1u) {
-                            // query positions qmin + c: column c visible iff c >= kpos - qmin
-                            const long long dlo = static_cast<long long>(kpos) - qmm.x;
-                            const int lo = dlo <= 0 ? 0 : (dlo > 64 ? 64 : static_cast<int>(dlo));
+                    const int q0 = qt * 128;
+                    const bool need_mask = kmm.y > qmm.x || q0 + 128 > a.Sq;
+                    const int gq = r * a.nq + qt;
+                    const bool arith = (arith_bits[gq >> 5] >> (gq & 31)) & 1u;
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        // this warp's columns: cb .. cb+31 = queries q0 + cb ..
+                        const int cb = 64 * h + 32 * grp;
+                        uint32_t s[32], dp[32];
+                        tmem_ld32_nowait(tA + cb, s);
+                        tmem_ld32_nowait(tA + 128 + cb, dp);
+                        tmem_wait_ld32(s);
+                        tmem_wait_ld32(dp);
+                        if (need_mask) {
+                            const int qh = q0 + cb;
+                            const int nvalid = min(32, a.Sq - qh);
+                            if (arith) {
+                                // query positions qmin + cb + c: column c visible iff c >= kpos - qmin - cb
+                                const long long dlo = static_cast<long long>(kpos) - qmm.x - cb;
+                                const int lo = dlo <= 0 ? 0 : (dlo > 32 ? 32 : static_cast<int>(dlo));
 #pragma unroll
-                            for (int c = 0; c < 64; ++c)
-                                if (c < lo || c >= nvalid) s[c] = kNegInfBits;
-                        } else {
+                                for (int c = 0; c < 32; ++c)
+                                    if (c < lo || c >= nvalid) s[c] = kNegInfBits;
+                            } else {
 #pragma unroll
-                            for (int c0 = 0; c0 < 64; c0 += 16) {
+                                for (int c0 = 0; c0 < 32; c0 += 16) {
 #pragma unroll
-                                for (int c = c0; c < c0 + 16; ++c) {
-                                    const int qp = (c < nvalid) ? __ldg(qpos_r + q0 + c) : INT_MIN;
-                                    if (kpos > qp) s[c] = kNegInfBits;
+                                    for (int c = c0; c < c0 + 16; ++c) {
+                                        const int qp = (c < nvalid) ? __ldg(qpos_r + qh + c) : INT_MIN;
+                                        if (kpos > qp) s[c] = kNegInfBits;
+                                    }
+                                    asm volatile("" ::: "memory");
                                 }
-                                asm volatile("" ::: "memory");
                             }
                         }
-                    }
-                    // P^T = 2^(s sl2 + nl2_c), dS^T = P^T (dP^T + nd_c), column stats from the stage
-                    const float *nl = sStat + st * 128, *nd = nl + 64;
-                    uint32_t pk_p[32], pk_d[32];
+                        // P^T = 2^(s sl2 + nl2_c), dS^T = P^T (dP^T + nd_c), column stats from the stage
+                        const float *nl = sStat + st * 256 + cb, *nd = nl + 128;
+                        uint32_t pk_p[16], pk_d[16];
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(nl + c);
-                        const float4 d4 = *reinterpret_cast<const float4 *>(nd + c);
-                        float x0, x1, x2, x3, g0, g1, g2, g3;
-                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, f2_packf(l4.x, l4.y)), x0, x1);
-                        f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, f2_packf(l4.z, l4.w)), x2, x3);
-                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2), p3 = fast_exp2(x3);
-                        f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), f2_packf(d4.x, d4.y)),
-                                         0ull),
-                                  g0, g1);
-                        f2_unpack(f2_fma(f2_packf(p2, p3),
-                                         f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_packf(d4.z, d4.w)), 0ull),
-                                  g2, g3);
-                        pk_p[c >> 1] = pack_bf16x2(p0, p1);
-                        pk_p[(c >> 1) + 1] = pack_bf16x2(p2, p3);
-                        pk_d[c >> 1] = pack_bf16x2(g0, g1);
-                        pk_d[(c >> 1) + 1] = pack_bf16x2(g2, g3);
+                        for (int c = 0; c < 32; c += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4 *>(nl + c);
+                            const float4 d4 = *reinterpret_cast<const float4 *>(nd + c);
+                            float x0, x1, x2, x3, g0, g1, g2, g3;
+                            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, f2_packf(l4.x, l4.y)), x0, x1);
+                            f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, f2_packf(l4.z, l4.w)), x2, x3);
+                            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2),
+                                        p3 = fast_exp2(x3);
+                            f2_unpack(f2_fma(f2_packf(p0, p1),
+                                             f2_add(f2_pack(dp[c], dp[c + 1]), f2_packf(d4.x, d4.y)), 0ull),
+                                      g0, g1);
+                            f2_unpack(f2_fma(f2_packf(p2, p3),
+                                             f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_packf(d4.z, d4.w)), 0ull),
+                                      g2, g3);
+                            pk_p[c >> 1] = pack_bf16x2(p0, p1);
+                            pk_p[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+                            pk_d[c >> 1] = pack_bf16x2(g0, g1);
+                            pk_d[(c >> 1) + 1] = pack_bf16x2(g2, g3);
+                        }
+                        // packed over the first 16 of this warp's own 32 columns (already
+                        // read; no other warp reads them): the MMA finds the half's
+                        // 64 packed queries at columns 64h + {0..15, 32..47}
+                        tmem_st16_nowait(tA + cb, pk_p);
+                        tmem_st16_nowait(tA + 128 + cb, pk_d);
+                        release_half(h == 0 ? p_half : p_full, lane);
                     }
-                    tmem_st32_nowait(tA + bb * 128, pk_p);
-                    tmem_st32_nowait(tA + bb * 128 + 64, pk_d);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(p_full + bb);
-                    ++t;
                 }
             }
             if (!ok) break;
             if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
             tc_fence_after();
-            store_acc_row<D>(tA + 256, dv_row, 1.f, key_valid, a.accumulate != 0);
-            store_acc_row<D>(tA + 256 + D, dk_row, a.scale, key_valid, a.accumulate != 0);
+            store_acc_row<D / 2>(tA + 256 + grp * (D / 2), dv_row, 1.f, key_valid, a.accumulate != 0);
+            store_acc_row<D / 2>(tA + 256 + D + grp * (D / 2), dk_row, a.scale, key_valid, a.accumulate != 0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_empty);
@@ -620,10 +642,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per key tile
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
     uint64_t *qd_full = bar, *qd_empty = bar + 1, *kv_full = bar + 2, *kv_empty = bar + 2 + kBStages;
-    uint64_t *s_full = bar + 2 + 2 * kBStages, *p_full = s_full + 2, *o_full = s_full + 4, *o_empty = s_full + 5,
-             *drain = s_full + 6;
-    const int2 *qtab = tab;                // [C][nq] 128-query tiles
-    const int2 *ktab = tab + a.C * a.nq;   // [kpr][nk] 64-key tiles
+    uint64_t *s_full = bar + 2 + 2 * kBStages, *p_half = s_full + 1, *p_full = s_full + 2, *o_full = s_full + 3,
+             *o_empty = s_full + 4, *drain = s_full + 5;
+    const int2 *qtab = tab;               // [C][nq] query tiles
+    const int2 *ktab = tab + a.C * a.nq;  // [kpr][nk] key tiles
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -634,12 +656,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
             mbar_init(kv_full + s, 1);
             mbar_init(kv_empty + s, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full + i, 1);
-            mbar_init(p_full + i, 4);
-        }
+        mbar_init(s_full, 1);
+        mbar_init(p_half, kComputeWarps);
+        mbar_init(p_full, kComputeWarps);
         mbar_init(o_full, 1);
-        mbar_init(o_empty, 4);
+        mbar_init(o_empty, kComputeWarps);
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -657,10 +678,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int g = warp; g < total; g += kBThreads / 32) {
             if (g < nqq) {
                 const int r = g / a.nq, qt = g - (g / a.nq) * a.nq;
-                tile_table<128>(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab + g, nullptr, 0);
+                tile_table(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab + g, nullptr, 0);
             } else {
                 const int gk = g - nqq, j = gk / a.nk, kt = gk - (gk / a.nk) * a.nk;
-                tile_table<64>(a.k_pos + j * a.k_pos_stride, kt * 64, a.Sk, lane, tab + g, arith_bits, gk);
+                tile_table(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab + g, arith_bits, gk);
             }
         }
     }
@@ -715,12 +736,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 decode(idx, r, qt, b, h, owner, kvr, pr);
                 if (cost[pr] == 0) continue;
                 if (!mbar_wait(qd_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(qd_full, 2 * K::kBig);
+                mbar_arrive_expect_tx(qd_full, 2 * K::kTile);
                 qd_par = static_cast<int>(it & 1u);
                 const int qrow = r * a.B + b;
                 for (int at = 0; at < K::kAtoms; ++at) {
-                    tma_load_4d(sQ + at * K::kAtomBig, &tmQ, qd_full, 64 * at, h, qt * 128, qrow);
-                    tma_load_4d(sDO + at * K::kAtomBig, &tmDO, qd_full, 64 * at, h, qt * 128, qrow);
+                    tma_load_4d(sQ + at * K::kAtom, &tmQ, qd_full, 64 * at, h, qt * 128, qrow);
+                    tma_load_4d(sDO + at * K::kAtom, &tmDO, qd_full, 64 * at, h, qt * 128, qrow);
                 }
                 ++it;
                 const int2 *kt_o = ktab + owner * a.nk;
@@ -731,12 +752,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 for (int kt = next_k(0, kt_o, a.nk, qmax, srt); kt < a.nk; kt = next_k(kt + 1, kt_o, a.nk, qmax, srt)) {
                     const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
                     if (!mbar_wait(kv_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    mbar_arrive_expect_tx(kv_full + st, 2 * K::kSmall);
+                    mbar_arrive_expect_tx(kv_full + st, 2 * K::kTile);
                     for (int at = 0; at < K::kAtoms; ++at) {
-                        tma_load_4d(sK + st * K::kSmall + at * K::kAtomSmall, &tmK, kv_full + st, 64 * at, hk,
-                                    kt * 64, kvrow);
-                        tma_load_4d(sV + st * K::kSmall + at * K::kAtomSmall, &tmV, kv_full + st, 64 * at, hk,
-                                    kt * 64, kvrow);
+                        tma_load_4d(sK + st * K::kTile + at * K::kAtom, &tmK, kv_full + st, 64 * at, hk, kt * 128,
+                                    kvrow);
+                        tma_load_4d(sV + st * K::kTile + at * K::kAtom, &tmV, kv_full + st, 64 * at, hk, kt * 128,
+                                    kvrow);
                     }
                     kv_issued |= 1u << st;
                     kv_par = (kv_par & ~(1u << st)) | (ph << st);
@@ -755,25 +776,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, 0, 0);  // S, dP: 128 queries x 64 keys
-            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);   // dQ: B operand MN-major
-            constexpr uint64_t kStU = K::kSmall >> 4;
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: 128 queries x 128 keys
+            constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);    // dQ: B operand MN-major
+            constexpr uint64_t kStU = K::kTile >> 4;
+            constexpr uint64_t kHalfU = (64 * 128) >> 4;
             const uint64_t dQa = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dOa = smem_desc_sw128(smem_u32(sDO), 16, 1024);
             const uint64_t dKb = smem_desc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t dVb = smem_desc_sw128(smem_u32(sV), 16, 1024);
-            const uint64_t dKm = smem_desc_sw128(smem_u32(sK), K::kAtomSmall, 1024);
+            const uint64_t dKm = smem_desc_sw128(smem_u32(sK), K::kAtom, 1024);
             uint32_t it = 0, t = 0;
             bool ok = true;
-            auto grad = [&](uint32_t pt, bool first) -> bool {
-                const uint32_t pb = pt & 1u, pst = pt % kBStages;
-                if (!mbar_wait(p_full + pb, (pt >> 1) & 1u, abort_flag, a.timeout_ns)) return false;
-                if (first && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) return false;
-                tc_fence_after();
-                umma_ts_k64(tmem + 256, tmem + pb * 128, dKm + pst * kStU, kIdG, first ? 0u : 1u);
-                umma_commit(kv_empty + pst);  // K (S and dQ) and V (dP) of this stage are read
-                return true;
-            };
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
@@ -783,19 +796,25 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 if (n == 0) continue;
                 if (!mbar_wait(qd_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
-                for (int j = 0; j < n; ++j) {
-                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u, bb = t & 1u;
+                for (int j = 0; j < n; ++j, ++t) {
+                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
                     if (!mbar_wait(kv_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128, dQa, dKb + st * kStU, kIdS);
-                    umma_ss_kgroup<D / 16, 1024, 512>(tmem + bb * 128 + 64, dOa, dVb + st * kStU, kIdS);
-                    umma_commit(s_full + bb);
+                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem, dQa, dKb + st * kStU, kIdS);
+                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem + 128, dOa, dVb + st * kStU, kIdS);
+                    umma_commit(s_full);
                     if (j == n - 1) umma_commit(qd_empty);  // Q and dO are read by S / dP only
-                    if (j > 0 && !grad(t - 1, j == 1)) { ok = false; break; }
-                    ++t;
+                    // dQ += dS K over the tile's first 64 keys, then the second 64
+                    if (!mbar_wait(p_half, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_ts_k64_split(tmem + 256, tmem, dKm + st * kStU, kIdG, j == 0 ? 0u : 1u);
+                    if (!mbar_wait(p_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    umma_ts_k64_split(tmem + 256, tmem + 64, dKm + st * kStU + kHalfU, kIdG, 1u);
+                    umma_commit(kv_empty + st);  // K (S and dQ) and V (dP) of this stage are read
                 }
                 if (!ok) break;
-                if (!grad(t - 1, n == 1)) { ok = false; break; }
                 umma_commit(o_full);
                 ++it;
             }
@@ -804,9 +823,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
             mbar_wait(drain, 0, &no_abort, 100000000ull);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // -------------------------------------------------------- compute (one query row per thread)
         const int quarter = warp & 3;
+        const int grp = (warp - 4) >> 2;  // columns 32 grp .. 32 grp + 31 of each half
         const int row_in = quarter * 32 + lane;
         const uint32_t tA = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint64_t sl2x2 = f2_packf(a.scale_log2, a.scale_log2);
@@ -821,9 +841,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const bool row_valid = row < a.Sq;
             const int qpos = row_valid ? __ldg(a.q_pos + r * a.q_pos_stride + row) : INT_MIN;
             const long long qrow = static_cast<long long>(r * a.B + b);
-            float *dq_row = a.dq + ((qrow * a.Sq + row) * a.N + h) * D;
+            float *dq_row = a.dq + ((qrow * a.Sq + row) * a.N + h) * D + grp * (D / 2);
             if (cost[pr] == 0) {
-                if (row_valid && !a.accumulate) zero_row<D>(dq_row);
+                if (row_valid && !a.accumulate) zero_row<D / 2>(dq_row);
                 continue;
             }
             // rows past Sq read the padding (-inf, 0): they see nothing
@@ -834,59 +854,65 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const int2 qmm = qtab[r * a.nq + qt];
             const bool srt = sorted_flag[owner] != 0;
             const int32_t *kpos_o = a.k_pos + owner * a.k_pos_stride;
-            for (int kt = next_k(0, kt_o, a.nk, qmm.y, srt); kt < a.nk; kt = next_k(kt + 1, kt_o, a.nk, qmm.y, srt)) {
-                const uint32_t bb = t & 1u;
-                if (!mbar_wait_warp(s_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+            for (int kt = next_k(0, kt_o, a.nk, qmm.y, srt); kt < a.nk;
+                 kt = next_k(kt + 1, kt_o, a.nk, qmm.y, srt), ++t) {
+                if (!mbar_wait_warp(s_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t s[64], dp[64];
-                tmem_ld64_nowait(tA + bb * 128, s);
-                tmem_ld64_nowait(tA + bb * 128 + 64, dp);
-                tmem_wait_ld(s);
-                tmem_wait_ld(dp);
                 const int2 kmm = kt_o[kt];
-                const int k0 = kt * 64;
-                const int nvalid = min(64, a.Sk - k0);
-                if (kmm.y > qmm.x || nvalid < 64) {
-                    const int gk = owner * a.nk + kt;
-                    if ((arith_bits[gk >> 5] >> (gk & 31)) & 1u) {
-                        // key positions kmin + c: column c visible iff c <= qpos - kmin
-                        const long long dhi = static_cast<long long>(qpos) - kmm.x;
-                        const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
+                const int k0 = kt * 128;
+                const bool need_mask = kmm.y > qmm.x || k0 + 128 > a.Sk;
+                const int gk = owner * a.nk + kt;
+                const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+                    // this warp's columns: cb .. cb+31 = keys k0 + cb ..
+                    const int cb = 64 * hf + 32 * grp;
+                    uint32_t s[32], dp[32];
+                    tmem_ld32_nowait(tA + cb, s);
+                    tmem_ld32_nowait(tA + 128 + cb, dp);
+                    tmem_wait_ld32(s);
+                    tmem_wait_ld32(dp);
+                    if (need_mask) {
+                        const int kh = k0 + cb;
+                        const int nvalid = min(32, a.Sk - kh);
+                        if (arith) {
+                            // key positions kmin + cb + c: column c visible iff c <= qpos - kmin - cb
+                            const long long dhi = static_cast<long long>(qpos) - kmm.x - cb;
+                            const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c > lim) s[c] = kNegInfBits;
-                    } else {
+                            for (int c = 0; c < 32; ++c)
+                                if (c > lim) s[c] = kNegInfBits;
+                        } else {
 #pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
+                            for (int c0 = 0; c0 < 32; c0 += 16) {
 #pragma unroll
-                            for (int c = c0; c < c0 + 16; ++c) {
-                                const int kp = (c < nvalid) ? __ldg(kpos_o + k0 + c) : INT_MAX;
-                                if (kp > qpos) s[c] = kNegInfBits;
+                                for (int c = c0; c < c0 + 16; ++c) {
+                                    const int kp = (c < nvalid) ? __ldg(kpos_o + kh + c) : INT_MAX;
+                                    if (kp > qpos) s[c] = kNegInfBits;
+                                }
+                                asm volatile("" ::: "memory");
                             }
-                            asm volatile("" ::: "memory");
                         }
                     }
-                }
-                // dS = 2^(s sl2 + nl2) (dP + nd)
-                uint32_t pk[32];
+                    // dS = 2^(s sl2 + nl2) (dP + nd)
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float x0, x1, g0, g1;
-                    f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nl2x2), x0, x1);
-                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                    f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), ndx2), 0ull), g0, g1);
-                    pk[c >> 1] = pack_bf16x2(g0, g1);
+                    for (int c = 0; c < 32; c += 2) {
+                        float x0, x1, g0, g1;
+                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nl2x2), x0, x1);
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), ndx2), 0ull), g0, g1);
+                        pk[c >> 1] = pack_bf16x2(g0, g1);
+                    }
+                    // packed over the first 16 of this warp's own 32 columns (see dK / dV)
+                    tmem_st16_nowait(tA + cb, pk);
+                    release_half(hf == 0 ? p_half : p_full, lane);
                 }
-                tmem_st32(tA + bb * 128, pk);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + bb);
-                ++t;
             }
             if (!ok) break;
             if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
             tc_fence_after();
-            store_acc_row<D>(tA + 256, dq_row, a.scale, row_valid, a.accumulate != 0);
+            store_acc_row<D / 2>(tA + 256 + grp * (D / 2), dq_row, a.scale, row_valid, a.accumulate != 0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_empty);
@@ -984,11 +1010,12 @@ cp_status launch_dkdv_typed(const BwdProblem &p, cudaStream_t stream) {
     using K = CfgKV<D>;
     CUtensorMap mq, mdo, mk, mv, mnl, mnd;
     const int64_t CB = p.C * p.B;
-    if (!make_map(&mq, p.q, D, p.N, p.Sq, CB, 64) || !make_map(&mdo, p.dout, D, p.N, p.Sq, CB, 64) ||
+    if (!make_map(&mq, p.q, D, p.N, p.Sq, CB, 128) || !make_map(&mdo, p.dout, D, p.N, p.Sq, CB, 128) ||
         !make_map(&mk, p.k, D, p.Nkv, p.Sk, CB, 128) || !make_map(&mv, p.v, D, p.Nkv, p.Sk, CB, 128) ||
-        !make_map_f32_rows(&mnl, p.nl2, p.sq_pad, CB * p.N, 64) || !make_map_f32_rows(&mnd, p.nd, p.sq_pad, CB * p.N, 64))
+        !make_map_f32_rows(&mnl, p.nl2, p.sq_pad, CB * p.N, 128) ||
+        !make_map_f32_rows(&mnd, p.nd, p.sq_pad, CB * p.N, 128))
         return CP_ERR_CUDA;
-    const int nq = static_cast<int>((p.Sq + 63) / 64), nk = static_cast<int>((p.Sk + 127) / 128);
+    const int nq = static_cast<int>((p.Sq + 127) / 128), nk = static_cast<int>((p.Sk + 127) / 128);
     BwdArgs a = make_args<D>(p, nq, nk, static_cast<int>(p.Nkv));
     a.div_nt = make_fastdiv(static_cast<uint32_t>(nk));
     const long long n_items = static_cast<long long>(p.C) * nk * p.B * p.Nkv;
@@ -1009,9 +1036,9 @@ cp_status launch_dq_typed(const BwdProblem &p, cudaStream_t stream) {
     CUtensorMap mq, mdo, mk, mv;
     const int64_t CB = p.C * p.B;
     if (!make_map(&mq, p.q, D, p.N, p.Sq, CB, 128) || !make_map(&mdo, p.dout, D, p.N, p.Sq, CB, 128) ||
-        !make_map(&mk, p.k, D, p.Nkv, p.Sk, CB, 64) || !make_map(&mv, p.v, D, p.Nkv, p.Sk, CB, 64))
+        !make_map(&mk, p.k, D, p.Nkv, p.Sk, CB, 128) || !make_map(&mv, p.v, D, p.Nkv, p.Sk, CB, 128))
         return CP_ERR_CUDA;
-    const int nq = static_cast<int>((p.Sq + 127) / 128), nk = static_cast<int>((p.Sk + 63) / 64);
+    const int nq = static_cast<int>((p.Sq + 127) / 128), nk = static_cast<int>((p.Sk + 127) / 128);
     BwdArgs a = make_args<D>(p, nq, nk, static_cast<int>(p.N));
     a.div_nt = make_fastdiv(static_cast<uint32_t>(nq));
     const long long n_items = static_cast<long long>(p.C) * nq * p.B * p.N;
@@ -1059,9 +1086,8 @@ cp_status validate_bwd(const BwdProblem &p) {
         return CP_ERR_ALIGNMENT;
     if (p.sq_pad < bwd_sq_pad(p.Sq) || p.sq_pad % 128 != 0) return CP_ERR_SHAPE;
     const int64_t kpr = (p.k_pos_stride == 0) ? 1 : p.C;
-    const int64_t q64 = (p.Sq + 63) / 64, q128 = (p.Sq + 127) / 128, k64 = (p.Sk + 63) / 64,
-                  k128 = (p.Sk + 127) / 128;
-    if (kpr * k128 + p.C * q64 > kBwdMaxTables || p.C * q128 + kpr * k64 > kBwdMaxTables) return CP_ERR_SHAPE;
+    const int64_t q128 = (p.Sq + 127) / 128, k128 = (p.Sk + 127) / 128;
+    if (kpr * k128 + p.C * q128 > kBwdMaxTables) return CP_ERR_SHAPE;
     if (p.C * k128 > kBwdMaxPairs || p.C * q128 > kBwdMaxPairs) return CP_ERR_SHAPE;
     if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.C * k128 * p.B * p.Nkv > INT32_MAX ||
         p.C * q128 * p.B * p.N > INT32_MAX)

@@ -84,8 +84,8 @@ bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int6
 bool make_map_f32_rows(CUtensorMap *map, const float *base, int64_t cols, int64_t rows, int box_cols);
 
 // ------------------------------------------------------------ backward
-constexpr int kBwdMaxTables = 4096;  // position tables of one backward launch
-constexpr int kBwdMaxPairs = 2048;   // (rank, stationary tile) pairs of one backward launch
+constexpr int kBwdMaxTables = 2048;  // 128-row position tables of one backward launch
+constexpr int kBwdMaxPairs = 1024;   // (rank, stationary tile) pairs of one backward launch
 
 // One batched backward launch over C "rank" problems (the tile backward of
 // each rank's queries against the K/V of rank (r + kv_shift) mod C), with the

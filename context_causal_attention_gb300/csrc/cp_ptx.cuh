@@ -274,6 +274,22 @@ __device__ __forceinline__ void umma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// umma_ts_k64 with the A operand's four k-steps at TMEM columns a, a+8, a+32,
+// a+40 (two 16-column blocks 32 columns apart).
+__device__ __forceinline__ void umma_ts_k64_split(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                  uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred t, p;\n\t.reg .b64 b1;\n\t.reg .b32 a1;\n\t"
+        "setp.ne.b32 t, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.s64 b1, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 32;\n\tadd.s64 b1, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "add.u32 a1, %1, 40;\n\tadd.s64 b1, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
@@ -386,6 +402,31 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[64]) {
                    CP_RW8(r, 48), CP_RW8(r, 56)
                  :
                  : "memory");
+}
+// Issue a 32-column load WITHOUT waiting; read `r` only after tmem_wait_ld32(r).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : CP_R8(r, 0), CP_R8(r, 8), CP_R8(r, 16), CP_R8(r, 24)
+        : "r"(taddr)
+        : "memory");
+}
+// Wait for every outstanding tcgen05.ld of this thread, declaring `r` produced here.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : CP_RW8(r, 0), CP_RW8(r, 8), CP_RW8(r, 16), CP_RW8(r, 24)
+                 :
+                 : "memory");
+}
+// Issue a 16-column store without waiting (tmem_wait_st completes it).
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        CP_W8(r, 0), CP_W8(r, 8)
+        : "memory");
 }
 // Issue a 32-column store without waiting (tmem_wait_st completes it).
 __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&r)[32]) {

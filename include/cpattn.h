@@ -330,7 +330,7 @@ cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, const void *
  *   workspace : device, >= cp_attn_bwd_workspace_size(B, Sq, N) bytes,
  *        256-byte aligned (per-row statistics)
  * Other pointers 16-byte aligned.  Limits (else CP_ERR_SHAPE):
- * ceil(Sk/128) + ceil(Sq/64) <= 4096 and ceil(Sq/128) + ceil(Sk/64) <= 4096.
+ * ceil(Sk/128) + ceil(Sq/128) <= 2048, ceil(Sq/128) <= 1024, ceil(Sk/128) <= 1024.
  */
 cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t N, size_t *bytes);
 cp_status cp_attn_bwd_partial(const void *q, const void *k, const void *v, const float *o, const void *dout,
