@@ -50,6 +50,9 @@ namespace cpattn {
 // Sticky device status word of the library (CP_ERR_DEVICE_TIMEOUT when a
 // kernel gave up a bounded wait).  Read by cp_device_status().
 __device__ int g_cp_device_status = 0;
+// A flag nothing ever sets: the self-test holds the producer on it until its
+// bounded wait runs out.
+__device__ int g_cp_never_set = 0;
 
 namespace {
 
@@ -93,6 +96,7 @@ struct AttnArgs {
     int merge_into; // LSE-merge the partial into the (o, lse) accumulator
     float scale_log2;
     unsigned long long timeout_ns;
+    const int *hold;  // failure injection (self-test only), else null
     FastDiv div_bn, div_nqb, div_n;  // by B*N, nqb, N (work-item decoding)
 };
 
@@ -442,6 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;  // per stage: issued / phase parity
             int q_parity = -1;
             bool pend = false;  // a V tile waits to be issued
+            if (a.hold) {
+                // self-test: wait (bounded) for a flag nothing sets, then give up
+                // like any other wait does
+                const uint64_t t0 = global_timer_ns();
+                while (*reinterpret_cast<const volatile int *>(a.hold) == 0) {
+                    if (global_timer_ns() - t0 > a.timeout_ns) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(1000);
+                }
+            }
             int pend_kt = 0, pend_hk = 0, pend_row = 0;
             auto issue_v = [&]() -> bool {
                 const uint32_t st = v_it % K::kStages, ph = (v_it / K::kStages) & 1u;
@@ -874,7 +891,8 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
     a.kpos_shift = p.kpos_shift;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
-    a.timeout_ns = 2000000000ull;
+    a.timeout_ns = p.timeout_ns ? p.timeout_ns : 2000000000ull;
+    a.hold = p.hold;
     a.div_bn = make_fastdiv(static_cast<uint32_t>(a.B * a.N));
     a.div_nqb = make_fastdiv(static_cast<uint32_t>(a.nqb));
     a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
@@ -960,6 +978,33 @@ extern "C" cp_status cp_attn_partial(const void *q, const void *k, const void *v
     p.kv_shift = 0;
     p.kpos_shift = 0;
     p.scale = scale;
+    return cpattn::launch_attn(p, stream);
+}
+
+extern "C" cp_status cp_selftest_stalled_producer(const void *q, const void *k, const void *v, const int32_t *pos,
+                                                  float *o, float *lse, uint64_t timeout_ns, cudaStream_t stream) {
+    if (timeout_ns < 1000000ull || timeout_ns > 2000000000ull) return CP_ERR_ARGUMENT;
+    int *flag = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&flag), cpattn::g_cp_never_set) != cudaSuccess)
+        return CP_ERR_CUDA;
+    cpattn::AttnProblem p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.q_pos = pos;
+    p.k_pos = pos;
+    p.o = o;
+    p.lse = lse;
+    p.C = 1;
+    p.B = 1;
+    p.N = 1;
+    p.Nkv = 1;
+    p.D = 64;
+    p.Sq = 128;
+    p.Sk = 128;
+    p.scale = 0.125f;
+    p.hold = flag;
+    p.timeout_ns = timeout_ns;
     return cpattn::launch_attn(p, stream);
 }
 

@@ -56,6 +56,10 @@ struct AttnProblem {
     // (rows the partial cannot see are left untouched)
     bool merge_into;
     float scale;
+    // failure injection (self-test only): the producer first waits for *hold
+    // to become non-zero; every bounded wait uses timeout_ns (0: 2 s)
+    const int *hold = nullptr;
+    unsigned long long timeout_ns = 0;
 };
 
 // Host validation shared by cp_attn_partial and the ring.

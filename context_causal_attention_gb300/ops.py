@@ -328,6 +328,15 @@ def cp_ring_attention_fwd_noalloc(q_sh, k_sh, v_sh, pos, o, lse, scale=None, lay
     return o, lse
 
 
+def cp_selftest_stalled_producer(q, k, v, pos, o, lse, timeout_ns, stream=None):
+    """Failure-detection self-test: the attention kernel with its producer held
+    on a flag nothing sets; its bounded waits give up after timeout_ns and the
+    device status becomes CP_ERR_DEVICE_TIMEOUT (read it with cp_device_status)."""
+    st = _lib.lib().cp_selftest_stalled_producer(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), _ptr(o), _ptr(lse),
+                                                 int(timeout_ns), _stream(stream))
+    _lib.check("cp_selftest_stalled_producer", st)
+
+
 def cp_device_status(clear=True, stream=None):
     """Synchronise the stream and return the library's device status code."""
     code = ctypes.c_int(0)

@@ -366,6 +366,22 @@ cp_status cp_ring_attention_bwd(const void *q_sh, const void *k_sh, const void *
                                 cudaStream_t stream);
 
 /*
+ * cp_selftest_stalled_producer -- failure-detection self-test of the bounded
+ * device-side waits (no counterpart on the pages).  Launches the attention
+ * kernel on a [1][128][1][64] problem (q, k, v device bf16 [128][64], pos
+ * device int32 [128], o fp32 [128][64] 32-byte aligned, lse fp32 [128]) with
+ * its TMA producer held on a device flag that nothing sets and every bounded
+ * wait limited to timeout_ns (1 ms .. 2 s, else CP_ERR_ARGUMENT).  The producer
+ * gives up after timeout_ns, the other roles see the abort and unwind, TMEM
+ * is freed, and the kernel records CP_ERR_DEVICE_TIMEOUT in the device status
+ * word; o and lse are left unwritten.  The call itself returns CP_OK when the
+ * launch succeeded: read the outcome with cp_device_status().  The context
+ * stays usable.
+ */
+cp_status cp_selftest_stalled_producer(const void *q, const void *k, const void *v, const int32_t *pos, float *o,
+                                       float *lse, uint64_t timeout_ns, cudaStream_t stream);
+
+/*
  * cp_ring_attention_fwd_noalloc -- cp_ring_attention_fwd for callers that
  * cannot allocate device memory.  The source pages have no counterpart: this
  * entry point exists for callers that may not call cudaMalloc or cannot hand

@@ -164,3 +164,10 @@ def test_mesh_validation(cplib):
     bad = list(args)
     bad[3] = NULL
     assert mesh(*bad, FAKE, need, None) == 1
+
+
+def test_selftest_timeout_range(cplib):
+    # q, k, v, pos, o, lse, timeout_ns, stream: the limit is checked before any CUDA call
+    assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 10
+    assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 999_999, None) == 10
+    assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3_000_000_000, None) == 10
