@@ -698,6 +698,55 @@ def run_backward(args):
     return 0
 
 
+def run_tf32(args):
+    """One JSON line per workload: the ring forward over fp32 shards with the
+    tensor cores in tf32 (CP_RING_TF32, zero copy), TFLOP/s on the algorithmic
+    causal FLOPs against the tf32 peak (the measured bf16 peak x the nominal
+    tf32 / bf16 ratio 1.1 / 2.25)."""
+    import torch
+
+    import cp_synth as SY
+    from context_causal_attention_gb300 import build as cuda_build
+    from context_causal_attention_gb300 import ops as F
+
+    cuda_build.build()
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    ratio = 1.1 / 2.25
+    for wname in args.tf32.split(","):
+        w = SY.WORKLOADS[wname]
+        g = torch.Generator("cpu").manual_seed(0)
+        qs, ks, vs = (F.cp_zigzag_shard(torch.randn(w.B, w.S, n, w.D, generator=g).to(dev), w.C)
+                      for n in (w.N, w.Nkv, w.Nkv))
+        pos = F.cp_zigzag_positions(w.S, w.C, device=dev)
+        ws = torch.empty(max(256, F.cp_ring_workspace_size(w.B, w.S, w.N, w.Nkv, w.D, w.C, tf32=True)),
+                         dtype=torch.uint8, device=dev)
+
+        def fwd():
+            F.cp_ring_attention_fwd(qs, ks, vs, pos, tf32=True, workspace=ws)
+
+        for _ in range(max(3, args.warmup)):
+            fwd()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps)
+        e0.record()
+        for _ in range(reps):
+            fwd()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tf = w.flops / (ms * 1e-3) / 1e12
+        print(json.dumps({"tf32_ring": w.name, "S": w.S, "C": w.C, "N": w.N, "D": w.D, "ms": ms, "tflops": tf,
+                          "tf32_peak_sustained": peaks["bf16_tflops_sustained"] * ratio,
+                          "frac_of_tf32_sustained": tf / (peaks["bf16_tflops_sustained"] * ratio),
+                          "note": "includes the per-call transpose of v (fp32) for the K-major P V operand",
+                          "status": F.cp_device_status()}), flush=True)
+        del qs, ks, vs, ws
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -715,6 +764,8 @@ def main():
                     help="comma-separated workloads: time ring / all-gather / Ulysses / mesh forwards instead")
     ap.add_argument("--backward", default="",
                     help="comma-separated workloads: time the ring backward instead")
+    ap.add_argument("--tf32", default="",
+                    help="comma-separated workloads: time the ring forward over fp32 shards in tf32 instead")
     ap.add_argument("--sweep-only", default="", help="comma-separated sweep workload names")
     args = ap.parse_args()
     if args.sweep:
@@ -723,6 +774,8 @@ def main():
         return run_strategies(args)
     if args.backward:
         return run_backward(args)
+    if args.tf32:
+        return run_tf32(args)
     import cp_synth as SY
     w = SY.WORKLOADS.get(args.workload)
     if w is None:

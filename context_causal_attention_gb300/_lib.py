@@ -22,7 +22,7 @@ CP_BF16, CP_F32 = 0, 1
 CP_ZIGZAG, CP_CONTIGUOUS = 0, 1
 CP_SEQ_TO_HEAD, CP_HEAD_TO_SEQ = 0, 1
 CP_RANK_ORDER, CP_GLOBAL_ORDER = 0, 1
-CP_RING_PREFETCH, CP_RING_FUSED_MERGE = 1, 2
+CP_RING_PREFETCH, CP_RING_FUSED_MERGE, CP_RING_TF32 = 1, 2, 4
 
 
 class CpError(RuntimeError):
@@ -85,6 +85,8 @@ def lib():
     L.cp_ring_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, vp, vp,
                                         vp, sz, vp]
     L.cp_selftest_stalled_producer.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_uint64, vp]
+    L.cp_attn_f32_workspace_size.argtypes = [i64, i64, i64, i64, ctypes.POINTER(sz)]
+    L.cp_attn_partial_f32.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, sz, vp]
     L.cp_ring_attention_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, i32, vp,
                                                 vp]
     for name in header_symbols():

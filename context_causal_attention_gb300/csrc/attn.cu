@@ -846,6 +846,22 @@ bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int6
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_f32_4d(CUtensorMap *map, const float *base, int64_t d0, int64_t d1, int64_t d2, int64_t d3, int b0,
+                     int b1, int b2) {
+    auto enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1), static_cast<cuuint64_t>(d2),
+                          static_cast<cuuint64_t>(d3)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d0 * 4), static_cast<cuuint64_t>(d0 * d1 * 4),
+                             static_cast<cuuint64_t>(d0 * d1 * d2 * 4)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(b0), static_cast<cuuint32_t>(b1), static_cast<cuuint32_t>(b2), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_map_f32_rows(CUtensorMap *map, const float *base, int64_t cols, int64_t rows, int box_cols) {
     auto enc = get_encode_fn();
     if (!enc) return false;
@@ -1017,9 +1033,11 @@ extern "C" cp_status cp_device_status(int *code, int clear, cudaStream_t stream)
         const int zero = 0;
         if (cudaMemcpyToSymbol(cpattn::g_cp_device_status, &zero, sizeof(int)) != cudaSuccess) return CP_ERR_CUDA;
     }
-    // the backward kernels keep their own word (another translation unit)
-    const cp_status st = cpattn::read_bwd_device_status(&vb, clear != 0);
+    // the backward and tf32 kernels keep their own words (other translation units)
+    int vt = 0;
+    cp_status st = cpattn::read_bwd_device_status(&vb, clear != 0);
+    if (st == CP_OK) st = cpattn::read_tf32_device_status(&vt, clear != 0);
     if (st != CP_OK) return st;
-    *code = v != 0 ? v : vb;
+    *code = v != 0 ? v : (vb != 0 ? vb : vt);
     return CP_OK;
 }

@@ -86,6 +86,21 @@ cp_status ulysses_relayout_groups(const void *in, void *out, int64_t B, int64_t 
 bool make_map(CUtensorMap *map, const void *base, int64_t D, int64_t heads, int64_t rows, int64_t outer,
               int box_rows);
 bool make_map_f32_rows(CUtensorMap *map, const float *base, int64_t cols, int64_t rows, int box_cols);
+// 4-D fp32 map over [d3][d2][d1][d0] (d0 innermost), box b0 x b1 x b2 x 1,
+// 128-byte swizzle.
+bool make_map_f32_4d(CUtensorMap *map, const float *base, int64_t d0, int64_t d1, int64_t d2, int64_t d3, int b0,
+                     int b1, int b2);
+
+// ------------------------------------------------------------ tf32 path
+// The attention of launch_attn for fp32 q, k, v (tensor cores in tf32); vt is
+// v transposed by launch_tf32_transpose ([outer][Nkv][D][tf32_vt_pad(Sk)]).
+cp_status validate_attn_tf32(const AttnProblem &p);
+cp_status launch_attn_tf32(const AttnProblem &p, const float *vt, cudaStream_t stream);
+int64_t tf32_vt_pad(int64_t Sk);
+size_t tf32_vt_bytes(int64_t outer, int64_t Sk, int64_t Nkv, int64_t D);
+cp_status launch_tf32_transpose(const float *v, float *vt, int64_t outer, int64_t Sk, int64_t Nkv, int64_t D,
+                                cudaStream_t stream);
+cp_status read_tf32_device_status(int *code, bool clear);
 
 // ------------------------------------------------------------ backward
 constexpr int kBwdMaxTables = 2048;  // 128-row position tables of one backward launch

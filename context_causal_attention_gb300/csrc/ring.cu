@@ -9,7 +9,9 @@
 // partials into the running (o, lse); step 0 writes the accumulator directly.
 //
 // flags (bit set): CP_RING_FUSED_MERGE folds each step's merge into the
-// attention epilogue (the partial is merged straight into the accumulator).
+// attention epilogue (the partial is merged straight into the accumulator);
+// CP_RING_TF32 takes fp32 q, k, v and runs the tf32 kernel (attn_tf32.cu),
+// zero copy only (v of every rank is transposed once per call).
 // The inter-GPU exchange of the pages has two stand-ins here:
 //   no CP_RING_PREFETCH  zero copy: the kernel reads the owner's resident block;
 //   CP_RING_PREFETCH     the exchange is emulated: the K/V rotation needed by step
@@ -32,7 +34,7 @@ constexpr size_t kAlign = 256;
 inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t o_tile = 0, lse_tile = 0, o_acc = 0, kv = 0, total = 0;
+    size_t o_tile = 0, lse_tile = 0, o_acc = 0, kv = 0, vt = 0, total = 0;
     size_t o_tile_bytes = 0, lse_bytes = 0, o_acc_bytes = 0, kv_bytes = 0;  // kv: one K (or V) rotation
 };
 
@@ -53,6 +55,8 @@ Layout ws_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
     off += round_up(L.o_acc_bytes);
     L.kv = off;
     off += 4 * round_up(L.kv_bytes);  // 2 buffers x (K, V)
+    L.vt = off;
+    if (flags & CP_RING_TF32) off += round_up(tf32_vt_bytes(static_cast<int64_t>(C) * B, s, Nkv, D));
     L.total = off;
     return L;
 }
@@ -121,9 +125,11 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
     if (!q_sh || !k_sh || !v_sh || !pos || !o_sh || !lse_sh) return CP_ERR_NULL;
     if (o_dtype != CP_F32 && o_dtype != CP_BF16) return CP_ERR_DTYPE;
     if (layout != CP_ZIGZAG && layout != CP_CONTIGUOUS) return CP_ERR_ARGUMENT;
-    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;
+    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE | CP_RING_TF32)) return CP_ERR_ARGUMENT;
     const int prefetch = (flags & CP_RING_PREFETCH) ? 1 : 0;
     const bool fused = (flags & CP_RING_FUSED_MERGE) != 0;
+    const bool tf32 = (flags & CP_RING_TF32) != 0;
+    if (tf32 && (prefetch || fused)) return CP_ERR_UNSUPPORTED;
     if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
     if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
     if (events && n_events < 4 * C) return CP_ERR_ARGUMENT;
@@ -160,7 +166,7 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         chk.v = v_sh;
         chk.o = o_acc;
         chk.lse = lse_sh;
-        cp_status st = validate_attn(chk);
+        cp_status st = tf32 ? validate_attn_tf32(chk) : validate_attn(chk);
         if (st != CP_OK) return st;
         if (C > 1 && !fused && (!aligned16(o_tile) || !aligned16(lse_tile))) return CP_ERR_ALIGNMENT;
     }
@@ -184,6 +190,9 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         if (st == CP_OK) st = rotate_copy(vbuf[b], v_sh, rank_kv_bytes, C, step, res->side);
         if (st == CP_OK && cudaEventRecord(res->copy_done[b], res->side) != cudaSuccess) st = CP_ERR_CUDA;
     };
+    float *vt = reinterpret_cast<float *>(ws + L.vt);
+    if (tf32) st = launch_tf32_transpose(static_cast<const float *>(v_sh), vt, static_cast<int64_t>(C) * B, s, Nkv, D,
+                                        stream);
     if (use_prefetch) {
         if (cudaEventRecord(res->start, stream) != cudaSuccess || cudaStreamWaitEvent(res->side, res->start, 0) !=
                                                                         cudaSuccess)
@@ -213,7 +222,7 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         ps.o = (step == 0 || fused) ? o_acc : o_tile;
         ps.lse = (step == 0 || fused) ? lse_sh : lse_tile;
         rec(4 * step + 0);
-        if (st == CP_OK) st = launch_attn(ps, stream);
+        if (st == CP_OK) st = tf32 ? launch_attn_tf32(ps, vt, stream) : launch_attn(ps, stream);
         rec(4 * step + 1);
         if (use_prefetch && st == CP_OK && step + 2 < C) {
             // buffer (step+2)%2 was last read by this step's launch
@@ -249,7 +258,7 @@ extern "C" cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int
     if (o_dtype != CP_F32 && o_dtype != CP_BF16) return CP_ERR_DTYPE;
     if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
     if (S % C != 0) return CP_ERR_DIVISIBILITY;
-    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;
+    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE | CP_RING_TF32)) return CP_ERR_ARGUMENT;
     *bytes = ws_layout(B, S, N, Nkv, D, C, flags, o_dtype).total;
     return CP_OK;
 }

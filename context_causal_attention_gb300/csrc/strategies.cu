@@ -207,6 +207,7 @@ extern "C" cp_status cp_mesh_workspace_size(int64_t B, int64_t S, int64_t N, int
     if (!bytes) return CP_ERR_NULL;
     if (A < 1 || R < 1 || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
     if (N % A != 0 || Nkv % A != 0 || S % (static_cast<int64_t>(A) * R) != 0) return CP_ERR_DIVISIBILITY;
+    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;  // bf16 shards only
     cp_status st = CP_OK;
     const MeshLayout L = mesh_layout(B, S, N, Nkv, D, A, R, flags, &st);
     if (st != CP_OK) return st;
@@ -224,6 +225,7 @@ extern "C" cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, c
     cp_status st = check_common(B, S, N, Nkv, D, C, layout);
     if (st != CP_OK) return st;
     if (N % A != 0 || Nkv % A != 0) return CP_ERR_DIVISIBILITY;
+    if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;  // bf16 shards only
     const MeshLayout L = mesh_layout(B, S, N, Nkv, D, A, R, flags, &st);
     if (st != CP_OK) return st;
     if (!workspace || ws_bytes < L.total) return CP_ERR_WORKSPACE;

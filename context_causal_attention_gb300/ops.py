@@ -11,7 +11,7 @@ import torch
 
 from . import _lib
 from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_F32, CP_GLOBAL_ORDER, CP_HEAD_TO_SEQ, CP_RANK_ORDER,
-                   CP_RING_FUSED_MERGE, CP_RING_PREFETCH, CP_SEQ_TO_HEAD, CP_ZIGZAG, CpError)
+                   CP_RING_FUSED_MERGE, CP_RING_PREFETCH, CP_RING_TF32, CP_SEQ_TO_HEAD, CP_ZIGZAG, CpError)
 
 __all__ = [
     "cp_zigzag_shard", "cp_zigzag_unshard", "cp_zigzag_positions", "cp_ulysses_relayout", "cp_attn_partial",
@@ -19,7 +19,7 @@ __all__ = [
     "cp_allgather_attention_fwd", "cp_ulysses_attention_fwd",
     "cp_device_status", "cp_version",
     "CP_BF16", "CP_F32", "CP_ZIGZAG", "CP_CONTIGUOUS", "CP_SEQ_TO_HEAD", "CP_HEAD_TO_SEQ", "CP_RANK_ORDER",
-    "CP_GLOBAL_ORDER", "CP_RING_PREFETCH", "CP_RING_FUSED_MERGE", "CpError",
+    "CP_GLOBAL_ORDER", "CP_RING_PREFETCH", "CP_RING_FUSED_MERGE", "CP_RING_TF32", "CpError",
 ]
 
 _DT = {torch.bfloat16: CP_BF16, torch.float32: CP_F32}
@@ -118,6 +118,29 @@ def cp_attn_partial(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, stream=
     return o, lse
 
 
+def cp_attn_partial_f32(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, workspace=None, stream=None):
+    """cp_attn_partial for fp32 q, k, v with the tensor cores in tf32 -> (o fp32, lse fp32)."""
+    B, Sq, N, D = q.shape
+    Sk, Nkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, Sq, N, D), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, N, Sq), dtype=torch.float32, device=dev)
+    L = _lib.lib()
+    n = ctypes.c_size_t(0)
+    _lib.check("cp_attn_f32_workspace_size", L.cp_attn_f32_workspace_size(B, Sk, Nkv, D, ctypes.byref(n)))
+    if workspace is None:
+        workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
+    st = L.cp_attn_partial_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D, float(scale),
+                               _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _lib.check("cp_attn_partial_f32", st)
+    return o, lse
+
+
 def cp_lse_merge(o_acc, lse_acc, o_tile, lse_tile, stream=None):
     """In-place merge of (o_tile, lse_tile) into (o_acc, lse_acc)."""
     B, Sq, N, D = o_acc.shape
@@ -127,25 +150,26 @@ def cp_lse_merge(o_acc, lse_acc, o_tile, lse_tile, stream=None):
     return o_acc, lse_acc
 
 
-def _ring_flags(prefetch, fused_merge):
-    return (CP_RING_PREFETCH if prefetch else 0) | (CP_RING_FUSED_MERGE if fused_merge else 0)
+def _ring_flags(prefetch, fused_merge, tf32=False):
+    return ((CP_RING_PREFETCH if prefetch else 0) | (CP_RING_FUSED_MERGE if fused_merge else 0) |
+            (CP_RING_TF32 if tf32 else 0))
 
 
-def cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch=0, o_dtype=CP_F32, fused_merge=False):
+def cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch=0, o_dtype=CP_F32, fused_merge=False, tf32=False):
     n = ctypes.c_size_t(0)
-    st = _lib.lib().cp_ring_workspace_size(B, S, N, Nkv, D, C, _ring_flags(prefetch, fused_merge), o_dtype,
+    st = _lib.lib().cp_ring_workspace_size(B, S, N, Nkv, D, C, _ring_flags(prefetch, fused_merge, tf32), o_dtype,
                                            ctypes.byref(n))
     _lib.check("cp_ring_workspace_size", st)
     return n.value
 
 
 def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, prefetch=0, o_dtype=CP_F32,
-                          workspace=None, o=None, lse=None, events=None, stream=None, fused_merge=False):
+                          workspace=None, o=None, lse=None, events=None, stream=None, fused_merge=False, tf32=False):
     """Ring attention forward over C resident virtual ranks.
 
     Returns (o_sh [C,B,s,N,D] of o_dtype, lse_sh fp32 [C,B,N,s]).  `events`, if
     given, is a list of >= 4*C recorded torch.cuda.Event objects (see the C
-    header for their meaning)."""
+    header for their meaning).  tf32: fp32 shards, tensor cores in tf32."""
     C, B, s, N, D = q_sh.shape
     Nkv = k_sh.shape[3]
     S = C * s
@@ -156,12 +180,12 @@ def cp_ring_attention_fwd(q_sh, k_sh, v_sh, pos, scale=None, layout=CP_ZIGZAG, p
         o = torch.empty((C, B, s, N, D), dtype=torch.float32 if o_dtype == CP_F32 else torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
-    need = cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, o_dtype, fused_merge)
+    need = cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, o_dtype, fused_merge, tf32)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     L = _lib.lib()
     args = [_ptr(q_sh), _ptr(k_sh), _ptr(v_sh), _ptr(pos), B, S, N, Nkv, D, C, float(scale), layout,
-            _ring_flags(prefetch, fused_merge),
+            _ring_flags(prefetch, fused_merge, tf32),
             _ptr(o), o_dtype, _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _stream(stream)]
     if events is None:

@@ -150,6 +150,22 @@ cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int
                           cudaStream_t stream);
 
 /*
+ * cp_attn_f32_workspace_size / cp_attn_partial_f32 -- cp_attn_partial for fp32
+ * inputs with the tensor cores in tf32 (tcgen05.mma kind::tf32: operands
+ * rounded to a 10-bit mantissa, fp32 accumulation; P enters P V as tf32 too).
+ * Same arguments, result and conventions as cp_attn_partial except:
+ *   q : device fp32 [B][Sq][N][D]; k, v : device fp32 [B][Sk][Nkv][D]
+ *   workspace : device, >= cp_attn_f32_workspace_size(B, Sk, Nkv, D) bytes,
+ *               256-byte aligned (holds v transposed for the K-major operand)
+ * Limits: ceil(Sk/64) + ceil(Sq/128) <= 2048 (else CP_ERR_SHAPE).
+ */
+cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sk, int64_t Nkv, int64_t D, size_t *bytes);
+cp_status cp_attn_partial_f32(const float *q, const float *k, const float *v, const int32_t *q_pos,
+                              const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv,
+                              int64_t D, float scale, float *o, float *lse, void *workspace, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
  * cp_lse_merge -- merge a completed partial into an accumulator, in place.
  * [OCP] Peer-to-peer / Forward, the tile merge:
  *   lse = logaddexp(lse_acc, lse_tile)
@@ -166,6 +182,7 @@ cp_status cp_lse_merge(float *o_acc, float *lse_acc, const float *o_tile, const 
 /* Ring options (bit set, argument `flags` of the ring calls). */
 #define CP_RING_PREFETCH 1    /* emulate the ring exchange by side-stream K/V copies */
 #define CP_RING_FUSED_MERGE 2 /* merge each step's partial in the attention epilogue */
+#define CP_RING_TF32 4        /* fp32 q, k, v; tensor cores in tf32 (not with the other two flags) */
 
 /*
  * cp_ring_workspace_size -- bytes of device workspace cp_ring_attention_fwd

@@ -136,7 +136,8 @@ def test_mesh_validation(cplib):
     assert cplib.cp_mesh_workspace_size(1, 1024, 8, 8, 64, 2, 2, 1, ctypes.byref(n)) == 0 and n.value > 0
     need = n.value
     assert cplib.cp_mesh_workspace_size(1, 1024, 7, 7, 64, 2, 2, 0, ctypes.byref(n)) == 3   # N % A
-    assert cplib.cp_mesh_workspace_size(1, 1024, 8, 8, 64, 2, 2, 4, ctypes.byref(n)) == 10  # unknown flag
+    assert cplib.cp_mesh_workspace_size(1, 1024, 8, 8, 64, 2, 2, 4, ctypes.byref(n)) == 10  # tf32: ring only
+    assert cplib.cp_mesh_workspace_size(1, 1024, 8, 8, 64, 2, 2, 8, ctypes.byref(n)) == 10  # unknown flag
     mesh = cplib.cp_mesh_attention_fwd
     # q, k, v, pos, B, S, N, Nkv, D, A, R, scale, layout, flags, o, lse
     args = [FAKE, FAKE, FAKE, FAKE, 1, 1024, 8, 8, 64, 2, 2, 0.125, 0, 1, FAKE, FAKE]

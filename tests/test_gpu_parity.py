@@ -311,3 +311,79 @@ def test_ring_full_size_sampled_rows(cuda_dev, wname):
 
 def test_device_status_clean(cuda_dev):
     assert F.cp_device_status(clear=True) == 0
+
+
+# --------------------------------------------------------------------------
+# tf32 input path
+# --------------------------------------------------------------------------
+# Bars: q and k enter the tensor cores truncated to tf32 (10-bit mantissa), v
+# and P rounded to it.  A CPU emulation with all four truncated gives max|do|
+# <= 4e-3 and max|dlse| <= 3.5e-3 against fp64 of the fp32 inputs on S=256-1024
+# causal problems; the bars are 1e-2 for both.
+TF32_ATOL = 1e-2
+
+TF32_CASES = {
+    "tiny_fp32_causal": dict(B=1, Sq=256, Sk=256, N=2, Nkv=2, D=64, qp=lambda: np.arange(256), kp=lambda: np.arange(256)),
+    "ragged_gqa_d128": dict(B=2, Sq=200, Sk=333, N=4, Nkv=2, D=128, qp=lambda: np.arange(133, 333),
+                            kp=lambda: np.arange(333)),
+    "zigzag_r1_owner3_empty_rows": dict(B=1, Sq=128, Sk=128, N=2, Nkv=2, D=64, qp=lambda: _zz(512, 4)[1],
+                                        kp=lambda: _zz(512, 4)[3]),
+    "unsorted_positions": dict(B=1, Sq=300, Sk=500, N=2, Nkv=1, D=64,
+                               qp=lambda: np.random.default_rng(5).integers(0, 500, 300),
+                               kp=lambda: np.random.default_rng(6).permutation(500)),
+    "multi_tile_1024": dict(B=1, Sq=1024, Sk=1024, N=2, Nkv=2, D=128, qp=lambda: np.arange(1024),
+                            kp=lambda: np.arange(1024)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TF32_CASES))
+def test_attn_partial_f32_vs_oracle(cuda_dev, name):
+    c = TF32_CASES[name]
+    g = torch.Generator().manual_seed(zlib.crc32(name.encode()) % 1000)
+    q = torch.randn(c["B"], c["Sq"], c["N"], c["D"], generator=g)
+    k = torch.randn(c["B"], c["Sk"], c["Nkv"], c["D"], generator=g)
+    v = torch.randn(c["B"], c["Sk"], c["Nkv"], c["D"], generator=g)
+    qp = np.asarray(c["qp"](), dtype=np.int32)
+    kp = np.asarray(c["kp"](), dtype=np.int32)
+    o, lse = F.cp_attn_partial_f32(q.to(cuda_dev), k.to(cuda_dev), v.to(cuda_dev),
+                                   torch.as_tensor(qp).to(cuda_dev), torch.as_tensor(kp).to(cuda_dev))
+    torch.cuda.synchronize()
+    o_ref, l_ref = O.attn_direct(f64(q), f64(k), f64(v), qp, kp, nthreads=NTH)
+    assert_attn_close(o, lse, o_ref, l_ref, atol_o=TF32_ATOL, atol_lse=TF32_ATOL)
+    assert F.cp_device_status() == 0
+
+
+def test_attn_partial_f32_tiny_workload(cuda_dev):
+    """The tiny workload's fp32 draws (no bf16 rounding) through the tf32 path,
+    against fp64 of the same fp32 values."""
+    w = SY.WORKLOADS["tiny"]
+    _, _, _, raw = SY.make_qkv(w)
+    q, k, v = (t.to(cuda_dev) for t in raw)
+    p = torch.arange(w.S, dtype=torch.int32, device=cuda_dev)
+    o, lse = F.cp_attn_partial_f32(q, k, v, p, p)
+    torch.cuda.synchronize()
+    pn = np.arange(w.S, dtype=np.int32)
+    o_ref, l_ref = O.attn_direct(*(f64(t) for t in raw), pn, pn)
+    d_o, d_l = assert_attn_close(o, lse, o_ref, l_ref, atol_o=TF32_ATOL, atol_lse=TF32_ATOL)
+    print("tiny fp32 via tf32: max|do|=%.3g max|dlse|=%.3g" % (d_o, d_l))
+
+
+@pytest.mark.parametrize("wname,layout", [("tiny", "zigzag"), ("s4k_contig", "contiguous")])
+def test_ring_tf32_vs_oracle(cuda_dev, wname, layout):
+    """The ring over fp32 shards (CP_RING_TF32) against the oracle ring on the
+    same fp32 values (no bf16 rounding anywhere)."""
+    w = {"tiny": SY.WORKLOADS["tiny"],
+         "s4k_contig": SY.Workload("s4k_contig_f32", B=1, S=1024, N=4, Nkv=4, D=64, C=4, layout="contiguous")}[wname]
+    g = torch.Generator().manual_seed(11)
+    q, k, v = (torch.randn(w.B, w.S, w.N, w.D, generator=g) for _ in range(3))
+    lay = F.CP_ZIGZAG if layout == "zigzag" else F.CP_CONTIGUOUS
+    qs, ks, vs = (F.cp_zigzag_shard(t.to(cuda_dev), w.C, lay) for t in (q, k, v))
+    pos = F.cp_zigzag_positions(w.S, w.C, lay, device=cuda_dev)
+    o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, tf32=True)
+    torch.cuda.synchronize()
+    lay_o = O.ZIGZAG if layout == "zigzag" else O.CONTIGUOUS
+    o_ref, l_ref = O.ring_fwd(*(O.shard(f64(t), w.C, lay_o) for t in (q, k, v)), pos.cpu().numpy(), nthreads=NTH)
+    assert np.max(np.abs(f64(o_sh) - o_ref)) <= TF32_ATOL
+    assert np.max(np.abs(f64(lse_sh) - l_ref)) <= TF32_ATOL
+    with pytest.raises(F.CpError):
+        F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, tf32=True, prefetch=1)
