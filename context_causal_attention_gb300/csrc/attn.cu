@@ -73,7 +73,8 @@ struct Cfg {
     static constexpr int kOffTab = kOffV + kStages * kTileBytes;
     static constexpr int kOffOrder = kOffTab + kMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kMaxPairs * 4;
-    static constexpr int kOffBar = kOffCost + kMaxPairs * 4;
+    static constexpr int kOffSeg = kOffCost + kMaxPairs * 4;
+    static constexpr int kOffBar = kOffSeg + (kMaxPairs + 2) * 4;
     // barriers: q_full, q_empty, drain, k_full[S], v_full[S], k_empty[S], v_empty[S],
     //           s_full[2], p_full[2], o_full[2], o_empty[2]
     static constexpr int kNumBars = 3 + 4 * kStages + 8;
@@ -97,7 +98,9 @@ struct AttnArgs {
     float scale_log2;
     unsigned long long timeout_ns;
     const int *hold;  // failure injection (self-test only), else null
-    FastDiv div_bn, div_nqb, div_n;  // by B*N, nqb, N (work-item decoding)
+    int nsp;          // super-blocks per rank
+    int pair_blocks;  // a super-block holds query blocks u and nqb-1-u (else u alone)
+    FastDiv div_nsp, div_n;  // by nsp, N (work-item decoding)
 };
 
 struct Bars {
@@ -129,22 +132,56 @@ struct Item {
     int qmax;  // largest query position of the 256-row block (over valid rows)
 };
 
-__device__ __forceinline__ Item decode_item(int idx, const AttnArgs &a, const int *order, const int2 *qtab) {
+// A work item of the persistent schedule: one super-block (query blocks u and
+// nqb-1-u, or u alone) of one rank, batch entry and head.
+struct Super {
+    int r, u, b, h;
+};
+
+// Work-item index -> super item.  Items are laid out segment by segment, a
+// segment being a run of one rank's super-blocks with equal cost in the
+// longest-first order; inside a segment items go head-major (every super-block
+// of head 0, then head 1, ...), so CTAs running at the same time read the same
+// K/V heads.  seg_first[s] is the first ranked super-block of segment s (and
+// seg_first[#segments] their count); `seg` is the caller's cursor (the items of
+// one CTA come in increasing index order).
+__device__ __forceinline__ Super decode_super(int idx, const AttnArgs &a, const int *order, const int *seg_first,
+                                              int &seg) {
+    const int BN = a.B * a.N;
+    while (seg_first[seg + 1] * BN <= idx) ++seg;
+    const int f = seg_first[seg];
+    const int m = seg_first[seg + 1] - f;
+    const int local = idx - f * BN;
+    const int bh = local / m;
+    const uint32_t sp = static_cast<uint32_t>(order[f + (local - bh * m)]);
+    Super x;
+    x.r = static_cast<int>(fdiv(sp, a.div_nsp));
+    x.u = static_cast<int>(sp - static_cast<uint32_t>(x.r) * a.div_nsp.d);
+    x.b = static_cast<int>(fdiv(static_cast<uint32_t>(bh), a.div_n));
+    x.h = bh - x.b * a.N;
+    return x;
+}
+
+// Query block of part k (0 or 1) of a super item, -1 if it has no such part.
+__device__ __forceinline__ int sub_block(const Super &x, int k, const AttnArgs &a) {
+    if (k == 0) return x.u;
+    const int q2 = a.nqb - 1 - x.u;
+    return (a.pair_blocks && q2 != x.u) ? q2 : -1;
+}
+
+__device__ __forceinline__ Item make_item(const Super &x, int qb, const AttnArgs &a, const int2 *qtab) {
     Item it;
-    const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bn);
-    const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bn.d;
-    const uint32_t pr = static_cast<uint32_t>(order[pi]);
-    it.r = static_cast<int>(fdiv(pr, a.div_nqb));
-    it.qb = static_cast<int>(pr - static_cast<uint32_t>(it.r) * a.div_nqb.d);
-    it.b = static_cast<int>(fdiv(bh, a.div_n));
-    it.h = static_cast<int>(bh - static_cast<uint32_t>(it.b) * a.div_n.d);
+    it.r = x.r;
+    it.qb = qb;
+    it.b = x.b;
+    it.h = x.h;
     it.owner = it.r + a.kpos_shift;
     if (it.owner >= a.C) it.owner -= a.C;
     if (a.kpr == 1) it.owner = 0;
     it.kvr = it.r + a.kv_shift;
     if (it.kvr >= a.C) it.kvr -= a.C;
     if (a.kv_shared) it.kvr = 0;
-    const int qt0 = 2 * it.qb, qt1 = 2 * it.qb + 1;
+    const int qt0 = 2 * qb, qt1 = 2 * qb + 1;
     int qmax = qtab[it.r * a.nqt + qt0].y;
     if (qt1 < a.nqt) qmax = max(qmax, qtab[it.r * a.nqt + qt1].y);
     it.qmax = qmax;
@@ -300,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
     // per (rank, query block): number of key tiles it processes
     int *cost = reinterpret_cast<int *>(smem + K::kOffCost);
+    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
     int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
@@ -391,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sorted_flag[tid] = ok;
     }
     __syncthreads();
-    // longest-first order of (rank, query block) pairs
+    // key tiles of every (rank, query block) pair, then the longest-first
+    // order of the super-blocks cut into segments (see decode_super)
     {
         const int np = a.C * a.nqb;
         for (int p = tid; p < np; p += kThreads) {
@@ -414,14 +453,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             cost[p] = c;
         }
         __syncthreads();
-        for (int p = tid; p < np; p += kThreads) {
-            const int c = cost[p];
+        // super-block costs, held in the segment table until it is built
+        const int nsup = a.C * a.nsp;
+        int *sp_cost = seg_first;
+        for (int x = tid; x < nsup; x += kThreads) {
+            const int r = x / a.nsp, u = x - r * a.nsp, q2 = a.nqb - 1 - u;
+            int c = cost[r * a.nqb + u];
+            if (a.pair_blocks && q2 != u) c += cost[r * a.nqb + q2];
+            sp_cost[x] = c;
+        }
+        __syncthreads();
+        // rank by cost (descending), ties by index, i.e. by rank then block: so
+        // the super-blocks of one rank and cost are contiguous, and the first
+        // of them (no equal-cost one of its rank before it) opens a segment
+        constexpr int kHead = 1 << 30;
+        for (int x = tid; x < nsup; x += kThreads) {
+            const int c = sp_cost[x];
+            const int r0 = (x / a.nsp) * a.nsp;
             int rank = 0;
-            for (int q = 0; q < np; ++q) {
-                const int cq = cost[q];
-                rank += (cq > c) || (cq == c && q < p);
+            bool head = true;
+            for (int y = 0; y < nsup; ++y) {
+                const int cy = sp_cost[y];
+                rank += (cy > c) || (cy == c && y < x);
+                head &= !(cy == c && y >= r0 && y < x);
             }
-            order[rank] = p;
+            order[rank] = x | (head ? kHead : 0);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int nseg = 0;
+            for (int c0 = 0; c0 < nsup; c0 += 32) {
+                const int i = c0 + lane;
+                bool head = false;
+                if (i < nsup) {
+                    const int v = order[i];
+                    head = (v & kHead) != 0;
+                    order[i] = v & ~kHead;
+                }
+                const unsigned msk = __ballot_sync(0xffffffffu, head);
+                if (head) seg_first[nseg + __popc(msk & ((1u << lane) - 1u))] = i;
+                nseg += __popc(msk);
+            }
+            if (lane == 0) seg_first[nseg] = nsup;
         }
     }
     tc_fence_before();
@@ -429,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_items = a.C * a.nqb * a.B * a.N;
+    const int n_items = a.C * a.nsp * a.B * a.N;
     const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     const int hq_per_kv = a.N / a.Nkv;
     uint8_t *sQ = smem + K::kOffQ;
@@ -473,41 +546,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pend = false;
                 return true;
             };
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                const Item itm = decode_item(idx, a, order, qtab);
-                const int2 *kt_o = ktab + itm.owner * a.nkt;
-                const bool srt = sorted_flag[itm.owner];
-                int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt);
-                if (kt >= a.nkt) continue;
-                if (pend && !issue_v()) { ok = false; break; }  // last V of the previous item
-                if (!mbar_wait(bars.q_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(bars.q_full, 2 * K::kTileBytes);
-                q_parity = it & 1u;
-                const int qrow = itm.r * a.B + itm.b;
-                for (int i = 0; i < 2; ++i)
-                    for (int at = 0; at < K::kAtoms; ++at)
-                        tma_load_4d(sQ + i * K::kTileBytes + at * kAtomBytes, &tmQ, bars.q_full, 64 * at, itm.h,
-                                    (2 * itm.qb + i) * 128, qrow);
-                ++it;
-                const int hk = itm.h / hq_per_kv;
-                const int kvrow = itm.kvr * a.B + itm.b;
-                for (; kt < a.nkt; kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt)) {
-                    const uint32_t st = k_it % K::kStages, ph = (k_it / K::kStages) & 1u;
-                    if (!mbar_wait(bars.k_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    mbar_arrive_expect_tx(bars.k_full + st, K::kTileBytes);
-                    for (int at = 0; at < K::kAtoms; ++at)
-                        tma_load_4d(sK + st * K::kTileBytes + at * kAtomBytes, &tmK, bars.k_full + st, 64 * at, hk,
-                                    kt * 128, kvrow);
-                    k_issued |= 1u << st;
-                    k_par = (k_par & ~(1u << st)) | (ph << st);
-                    ++k_it;
-                    if (pend && !issue_v()) { ok = false; break; }
-                    pend = true;
-                    pend_kt = kt;
-                    pend_hk = hk;
-                    pend_row = kvrow;
+                const Super sup = decode_super(idx, a, order, seg_first, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int qb = sub_block(sup, part, a);
+                    if (qb < 0) continue;
+                    const Item itm = make_item(sup, qb, a, qtab);
+                    const int2 *kt_o = ktab + itm.owner * a.nkt;
+                    const bool srt = sorted_flag[itm.owner];
+                    int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt);
+                    if (kt >= a.nkt) continue;
+                    if (pend && !issue_v()) { ok = false; break; }  // last V of the previous item
+                    if (!mbar_wait(bars.q_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(bars.q_full, 2 * K::kTileBytes);
+                    q_parity = it & 1u;
+                    const int qrow = itm.r * a.B + itm.b;
+                    for (int i = 0; i < 2; ++i)
+                        for (int at = 0; at < K::kAtoms; ++at)
+                            tma_load_4d(sQ + i * K::kTileBytes + at * kAtomBytes, &tmQ, bars.q_full, 64 * at, itm.h,
+                                        (2 * itm.qb + i) * 128, qrow);
+                    ++it;
+                    const int hk = itm.h / hq_per_kv;
+                    const int kvrow = itm.kvr * a.B + itm.b;
+                    for (; kt < a.nkt; kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt)) {
+                        const uint32_t st = k_it % K::kStages, ph = (k_it / K::kStages) & 1u;
+                        if (!mbar_wait(bars.k_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        mbar_arrive_expect_tx(bars.k_full + st, K::kTileBytes);
+                        for (int at = 0; at < K::kAtoms; ++at)
+                            tma_load_4d(sK + st * K::kTileBytes + at * kAtomBytes, &tmK, bars.k_full + st, 64 * at, hk,
+                                        kt * 128, kvrow);
+                        k_issued |= 1u << st;
+                        k_par = (k_par & ~(1u << st)) | (ph << st);
+                        ++k_it;
+                        if (pend && !issue_v()) { ok = false; break; }
+                        pend = true;
+                        pend_kt = kt;
+                        pend_hk = hk;
+                        pend_row = kvrow;
+                    }
                 }
             }
             if (ok && pend && !issue_v()) ok = false;
@@ -546,51 +625,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_pv_group(tmem + 256 + i * D, tmem + i * 128 + 64, dv0 + st * kStageDesc, kIdescPV,
                               acc ? 1u : 0u);
             };
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                const Item itm = decode_item(idx, a, order, qtab);
-                const int n = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
-                if (n == 0) continue;
-                if (!mbar_wait(bars.q_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t prev_st = 0;
-                for (int j = 0; j < n && ok; ++j) {
-                    const uint32_t st = kv_it % K::kStages, ph = (kv_it / K::kStages) & 1u;
-                    if (!mbar_wait(bars.k_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                const Super sup = decode_super(idx, a, order, seg_first, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int qb = sub_block(sup, part, a);
+                    if (qb < 0) continue;
+                    const Item itm = make_item(sup, qb, a, qtab);
+                    const int n = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
+                    if (n == 0) continue;
+                    if (!mbar_wait(bars.q_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    for (int i = 0; i < 2; ++i) {
-                        if (j > 0) {
-                            const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
-                            if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                            if (j == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                            if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
-                            tc_fence_after();
-                            issue_pv(i, prev_st, j > 1);
-                            if (i == 1) umma_commit(bars.v_empty + prev_st);
+                    uint32_t prev_st = 0;
+                    for (int j = 0; j < n && ok; ++j) {
+                        const uint32_t st = kv_it % K::kStages, ph = (kv_it / K::kStages) & 1u;
+                        if (!mbar_wait(bars.k_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        for (int i = 0; i < 2; ++i) {
+                            if (j > 0) {
+                                const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
+                                if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                                if (j == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                                if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                                tc_fence_after();
+                                issue_pv(i, prev_st, j > 1);
+                                if (i == 1) umma_commit(bars.v_empty + prev_st);
+                            }
+                            issue_qk(i, st);
+                            umma_commit(bars.s_full + i);
                         }
-                        issue_qk(i, st);
-                        umma_commit(bars.s_full + i);
+                        if (ok) umma_commit(bars.k_empty + st);  // both tiles' Q K^T read this K stage
+                        if (!ok) break;
+                        if (j == n - 1) umma_commit(bars.q_empty);
+                        prev_st = st;
+                        ++kv_it;
                     }
-                    if (ok) umma_commit(bars.k_empty + st);  // both tiles' Q K^T read this K stage
                     if (!ok) break;
-                    if (j == n - 1) umma_commit(bars.q_empty);
-                    prev_st = st;
-                    ++kv_it;
+                    // tail: P V of the last key tile, then hand O to the epilogue
+                    for (int i = 0; i < 2; ++i) {
+                        const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
+                        if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (n == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(i, prev_st, n > 1);
+                        if (i == 1) umma_commit(bars.v_empty + prev_st);
+                        umma_commit(bars.o_full + i);
+                    }
+                    ++it;
                 }
-                if (!ok) break;
-                // tail: P V of the last key tile, then hand O to the epilogue
-                for (int i = 0; i < 2; ++i) {
-                    const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
-                    if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    if (n == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    if (!mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_pv(i, prev_st, n > 1);
-                    if (i == 1) umma_commit(bars.v_empty + prev_st);
-                    umma_commit(bars.o_full + i);
-                }
-                ++it;
             }
             // no MMA may still be running when TMEM is released
             umma_commit(bars.drain);
@@ -609,195 +694,201 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = a.scale_log2;
         uint32_t kv_count = 0, it = 0;
         bool ok = true;
+        int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
             const int idx = item_of_round(rk, n_items);
             if (idx < 0) continue;
-            const Item itm = decode_item(idx, a, order, qtab);
-            const int2 *kt_o = ktab + itm.owner * a.nkt;
-            const bool srt = sorted_flag[itm.owner];
-            const int qt = 2 * itm.qb + wg;
-            const int row = qt * 128 + row_in_tile;
-            const bool row_valid = row < a.Sq;
-            const int qpos = row_valid ? __ldg(a.q_pos + itm.r * a.q_pos_stride + row) : INT_MIN;
-            const int qmin_t = (qt < a.nqt) ? qtab[itm.r * a.nqt + qt].x : INT_MAX;
-            const int32_t *kpos_o = a.k_pos + itm.owner * a.k_pos_stride;
-            const long long orow = static_cast<long long>(itm.r * a.B + itm.b) * a.Sq + row;
-            float *o_row = a.o + (orow * a.N + itm.h) * D;
-            float *lse_out = a.lse + (static_cast<long long>(itm.r * a.B + itm.b) * a.N + itm.h) * a.Sq + row;
-            const int n_item = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
-            float m_run = -INFINITY, l_run = 0.f;
-            int j = 0;
-            for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
-                 kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt), ++j) {
-                if (!mbar_wait_warp(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+            const Super sup = decode_super(idx, a, order, seg_first, seg);
+            for (int part = 0; part < 2 && ok; ++part) {
+                const int qb = sub_block(sup, part, a);
+                if (qb < 0) continue;
+                const Item itm = make_item(sup, qb, a, qtab);
+                const int2 *kt_o = ktab + itm.owner * a.nkt;
+                const bool srt = sorted_flag[itm.owner];
+                const int qt = 2 * itm.qb + wg;
+                const int row = qt * 128 + row_in_tile;
+                const bool row_valid = row < a.Sq;
+                const int qpos = row_valid ? __ldg(a.q_pos + itm.r * a.q_pos_stride + row) : INT_MIN;
+                const int qmin_t = (qt < a.nqt) ? qtab[itm.r * a.nqt + qt].x : INT_MAX;
+                const int32_t *kpos_o = a.k_pos + itm.owner * a.k_pos_stride;
+                const long long orow = static_cast<long long>(itm.r * a.B + itm.b) * a.Sq + row;
+                float *o_row = a.o + (orow * a.N + itm.h) * D;
+                float *lse_out = a.lse + (static_cast<long long>(itm.r * a.B + itm.b) * a.N + itm.h) * a.Sq + row;
+                const int n_item = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
+                float m_run = -INFINITY, l_run = 0.f;
+                int j = 0;
+                for (int kt = next_ktile(0, a.nkt, kt_o, itm.qmax, srt); kt < a.nkt;
+                     kt = next_ktile(kt + 1, a.nkt, kt_o, itm.qmax, srt), ++j) {
+                    if (!mbar_wait_warp(bars.s_full + wg, kv_count & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    if (a.merge_into && row_valid && j == n_item - 1) {
+                        // the epilogue will read this row of the accumulator: start it towards L2
+    #pragma unroll
+                        for (int c = 0; c < D; c += 32) prefetch_l2(o_row + c);
+                    }
+                    uint32_t sa[64], sb[64];
+                    const int2 kmm = kt_o[kt];
+                    const bool need_mask = (kmm.y > qmin_t) || (kt * 128 + 128 > a.Sk);
+                    const int kbase = kt * 128;
+                    const int gk = itm.owner * a.nkt + kt;
+                    const int nvalid = min(128, a.Sk - kbase);
+                    const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
+                    // P (bf16 pairs) goes to columns 64..127 of the S region, so S
+                    // columns 0..63 stay readable until this tile's P V is issued.
+                    uint32_t pa[32], pb[32];
+                    float t_sum;
+                    bool stored = false;
+                    // TMEM loads/stores are warp-collective: the path must be warp-uniform
+                    if (__all_sync(0xffffffffu, m_run != -INFINITY)) {
+                        // Steady state (max already set): pipeline the tile in two halves --
+                        // the second half's TMEM load and the first half's P store overlap
+                        // exp work.
+                        tmem_ld64_nowait(tS, sa);
+                        tmem_wait_ld(sa);
+                        tmem_ld64_nowait(tS + 64, sb);
+                        if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
+                        const float s0 = exp_pack64(sa, sl2, -m_run, pa);
+                        tmem_wait_ld(sb);  // columns 64..127 read: P may overwrite them
+                        tmem_st32_nowait(tS + 64, pa);
+                        if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 64, sb);
+                        const float s1 = exp_pack64(sb, sl2, -m_run, pb);
+                        tmem_st32_nowait(tS + 96, pb);
+                        t_sum = s0 + s1;
+                        stored = true;
+                    } else {
+                        load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
+                        // rows without a running max yet (first visible tile): set it
+                        if (m_run == -INFINITY) {
+                            const float m_tile = row_max128(sa, sb) * sl2;
+                            if (m_tile > -INFINITY) m_run = ceilf(m_tile);
+                        }
+                        exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
+                    }
+                    float factor = 1.f;
+                    bool rescale = false;
+                    const bool big = !(t_sum <= 0x1p64f);  // also true for inf / nan
+                    if (__any_sync(0xffffffffu, big)) {
+                        // rare: scores grew by more than 2^64 over the running max.  Columns
+                        // 0..63 of S are still in TMEM; columns 64..127 are still in sb.
+                        if (stored) tmem_wait_st();
+                        tmem_ld64(tS, sa);
+                        if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
+                        if (big) {
+                            const float m_new = ceilf(row_max128(sa, sb) * sl2);
+                            // exact 2^(m_run - m_new): both are integers
+                            const float dk = m_run - m_new;
+                            factor = (dk >= -126.f) ? __int_as_float((127 + static_cast<int>(dk)) << 23) : 0.f;
+                            rescale = true;
+                            l_run *= factor;
+                            m_run = m_new;
+                        }
+                        // every lane recomputes (unchanged rows reproduce their values)
+                        exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
+                        stored = false;
+                    }
+                    l_run += t_sum;
+                    if (stored) {
+                        tmem_wait_st();
+                    } else {
+                        tmem_st64(tS + 64, pa, pb);
+                    }
+                    // O is quiescent here (the P V of this tile waits for p_full below)
+                    if (__any_sync(0xffffffffu, rescale)) {
+    #pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t ov[32];
+                            tmem_ld32(tO + c0, ov);
+    #pragma unroll
+                            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * factor);
+                            tmem_st32(tO + c0, ov);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.p_full + wg);
+                    ++kv_count;
+                }
+                if (!ok) break;
+                if (j == 0) {
+                    // nothing visible for this whole block: o = 0, lse = -inf (a merge
+                    // leaves the accumulator as it is)
+                    if (row_valid && !a.merge_into) {
+    #pragma unroll
+                        for (int c = 0; c < D; c += 8) st_global_v8(o_row + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
+                        *lse_out = -INFINITY;
+                    }
+                    continue;
+                }
+                if (!mbar_wait_warp(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                 tc_fence_after();
-                if (a.merge_into && row_valid && j == n_item - 1) {
-                    // the epilogue will read this row of the accumulator: start it towards L2
-#pragma unroll
-                    for (int c = 0; c < D; c += 32) prefetch_l2(o_row + c);
-                }
-                uint32_t sa[64], sb[64];
-                const int2 kmm = kt_o[kt];
-                const bool need_mask = (kmm.y > qmin_t) || (kt * 128 + 128 > a.Sk);
-                const int kbase = kt * 128;
-                const int gk = itm.owner * a.nkt + kt;
-                const int nvalid = min(128, a.Sk - kbase);
-                const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
-                // P (bf16 pairs) goes to columns 64..127 of the S region, so S
-                // columns 0..63 stay readable until this tile's P V is issued.
-                uint32_t pa[32], pb[32];
-                float t_sum;
-                bool stored = false;
-                // TMEM loads/stores are warp-collective: the path must be warp-uniform
-                if (__all_sync(0xffffffffu, m_run != -INFINITY)) {
-                    // Steady state (max already set): pipeline the tile in two halves --
-                    // the second half's TMEM load and the first half's P store overlap
-                    // exp work.
-                    tmem_ld64_nowait(tS, sa);
-                    tmem_wait_ld(sa);
-                    tmem_ld64_nowait(tS + 64, sb);
-                    if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
-                    const float s0 = exp_pack64(sa, sl2, -m_run, pa);
-                    tmem_wait_ld(sb);  // columns 64..127 read: P may overwrite them
-                    tmem_st32_nowait(tS + 64, pa);
-                    if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 64, sb);
-                    const float s1 = exp_pack64(sb, sl2, -m_run, pb);
-                    tmem_st32_nowait(tS + 96, pb);
-                    t_sum = s0 + s1;
-                    stored = true;
-                } else {
-                    load_scores(tS, need_mask, arith, qpos, kmm.x, nvalid, kpos_o + kbase, sa, sb);
-                    // rows without a running max yet (first visible tile): set it
-                    if (m_run == -INFINITY) {
-                        const float m_tile = row_max128(sa, sb) * sl2;
-                        if (m_tile > -INFINITY) m_run = ceilf(m_tile);
+                const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+                const float lse_t = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+                // o_row <- wa * o_row + wt * O (O unnormalised in TMEM); plain write: wa = 0
+                bool write = row_valid;
+                float wa = 0.f, wt = inv_l, lse_new = lse_t;
+                if (a.merge_into && row_valid) {
+                    // "On Context Parallelism", Peer-to-peer / Forward, the tile merge
+                    const float la = *lse_out;
+                    if (lse_t == -INFINITY) {
+                        write = false;
+                    } else if (la != -INFINITY) {
+                        const float mx = fmaxf(la, lse_t), mn = fminf(la, lse_t);
+                        lse_new = mx + log1pf(expf(mn - mx));
+                        wa = expf(la - lse_new);
+                        wt = expf(lse_t - lse_new) * inv_l;
                     }
-                    exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
                 }
-                float factor = 1.f;
-                bool rescale = false;
-                const bool big = !(t_sum <= 0x1p64f);  // also true for inf / nan
-                if (__any_sync(0xffffffffu, big)) {
-                    // rare: scores grew by more than 2^64 over the running max.  Columns
-                    // 0..63 of S are still in TMEM; columns 64..127 are still in sb.
-                    if (stored) tmem_wait_st();
-                    tmem_ld64(tS, sa);
-                    if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
-                    if (big) {
-                        const float m_new = ceilf(row_max128(sa, sb) * sl2);
-                        // exact 2^(m_run - m_new): both are integers
-                        const float dk = m_run - m_new;
-                        factor = (dk >= -126.f) ? __int_as_float((127 + static_cast<int>(dk)) << 23) : 0.f;
-                        rescale = true;
-                        l_run *= factor;
-                        m_run = m_new;
-                    }
-                    // every lane recomputes (unchanged rows reproduce their values)
-                    exp_pack128(sa, sb, sl2, (m_run == -INFINITY) ? 0.f : -m_run, pa, pb, &t_sum);
-                    stored = false;
-                }
-                l_run += t_sum;
-                if (stored) {
-                    tmem_wait_st();
-                } else {
-                    tmem_st64(tS + 64, pa, pb);
-                }
-                // O is quiescent here (the P V of this tile waits for p_full below)
-                if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
+                if (!a.merge_into) {
+    #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t ov[32];
                         tmem_ld32(tO + c0, ov);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * factor);
-                        tmem_st32(tO + c0, ov);
+                        if (write) {
+    #pragma unroll
+                            for (int c = 0; c < 32; c += 8)
+                                st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * wt, __uint_as_float(ov[c + 1]) * wt,
+                                             __uint_as_float(ov[c + 2]) * wt, __uint_as_float(ov[c + 3]) * wt,
+                                             __uint_as_float(ov[c + 4]) * wt, __uint_as_float(ov[c + 5]) * wt,
+                                             __uint_as_float(ov[c + 6]) * wt, __uint_as_float(ov[c + 7]) * wt);
+                        }
                     }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.p_full + wg);
-                ++kv_count;
-            }
-            if (!ok) break;
-            if (j == 0) {
-                // nothing visible for this whole block: o = 0, lse = -inf (a merge
-                // leaves the accumulator as it is)
-                if (row_valid && !a.merge_into) {
-#pragma unroll
-                    for (int c = 0; c < D; c += 8) st_global_v8(o_row + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
-                    *lse_out = -INFINITY;
-                }
-                continue;
-            }
-            if (!mbar_wait_warp(bars.o_full + wg, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-            tc_fence_after();
-            const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-            const float lse_t = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-            // o_row <- wa * o_row + wt * O (O unnormalised in TMEM); plain write: wa = 0
-            bool write = row_valid;
-            float wa = 0.f, wt = inv_l, lse_new = lse_t;
-            if (a.merge_into && row_valid) {
-                // "On Context Parallelism", Peer-to-peer / Forward, the tile merge
-                const float la = *lse_out;
-                if (lse_t == -INFINITY) {
-                    write = false;
-                } else if (la != -INFINITY) {
-                    const float mx = fmaxf(la, lse_t), mn = fminf(la, lse_t);
-                    lse_new = mx + log1pf(expf(mn - mx));
-                    wa = expf(la - lse_new);
-                    wt = expf(lse_t - lse_new) * inv_l;
-                }
-            }
-            if (!a.merge_into) {
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + c0, ov);
-                    if (write) {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8)
-                            st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * wt, __uint_as_float(ov[c + 1]) * wt,
-                                         __uint_as_float(ov[c + 2]) * wt, __uint_as_float(ov[c + 3]) * wt,
-                                         __uint_as_float(ov[c + 4]) * wt, __uint_as_float(ov[c + 5]) * wt,
-                                         __uint_as_float(ov[c + 6]) * wt, __uint_as_float(ov[c + 7]) * wt);
-                    }
-                }
-            } else {
-                const bool read_acc = write && wa != 0.f;
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 16) {
-                    float acc[16];
-                    if (read_acc) {
-                        // issued before the TMEM load so both latencies overlap (the row
-                        // was sent towards L2 when the item's last tile started)
-                        float t8[8];
-                        ld_global_v8(o_row + c0, t8);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = t8[e];
-                        ld_global_v8(o_row + c0 + 8, t8);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[8 + e] = t8[e];
-                    }
-                    uint32_t ov[16];
-                    tmem_ld16(tO + c0, ov);
-                    if (write) {
-#pragma unroll
-                        for (int c = 0; c < 16; c += 8) {
-                            float r8[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                r8[e] = read_acc ? fmaf(wa, acc[c + e], wt * __uint_as_float(ov[c + e]))
-                                                 : wt * __uint_as_float(ov[c + e]);
-                            st_global_v8(o_row + c0 + c, r8[0], r8[1], r8[2], r8[3], r8[4], r8[5], r8[6], r8[7]);
+                } else {
+                    const bool read_acc = write && wa != 0.f;
+    #pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 16) {
+                        float acc[16];
+                        if (read_acc) {
+                            // issued before the TMEM load so both latencies overlap (the row
+                            // was sent towards L2 when the item's last tile started)
+                            float t8[8];
+                            ld_global_v8(o_row + c0, t8);
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = t8[e];
+                            ld_global_v8(o_row + c0 + 8, t8);
+    #pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[8 + e] = t8[e];
+                        }
+                        uint32_t ov[16];
+                        tmem_ld16(tO + c0, ov);
+                        if (write) {
+    #pragma unroll
+                            for (int c = 0; c < 16; c += 8) {
+                                float r8[8];
+    #pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    r8[e] = read_acc ? fmaf(wa, acc[c + e], wt * __uint_as_float(ov[c + e]))
+                                                     : wt * __uint_as_float(ov[c + e]);
+                                st_global_v8(o_row + c0 + c, r8[0], r8[1], r8[2], r8[3], r8[4], r8[5], r8[6], r8[7]);
+                            }
                         }
                     }
                 }
+                if (write) *lse_out = lse_new;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.o_empty + wg);
+                ++it;
             }
-            if (write) *lse_out = lse_new;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.o_empty + wg);
-            ++it;
         }
     }
 
@@ -909,10 +1000,18 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
     a.timeout_ns = p.timeout_ns ? p.timeout_ns : 2000000000ull;
     a.hold = p.hold;
-    a.div_bn = make_fastdiv(static_cast<uint32_t>(a.B * a.N));
-    a.div_nqb = make_fastdiv(static_cast<uint32_t>(a.nqb));
+    // Pair query block u with block nqb-1-u in one work item when there are
+    // enough items for at least 8 rounds over the SMs: under a causal mask the
+    // two costs add up to about the same for every u, so every item costs about
+    // the same and the head-major order (decode_super) keeps the CTAs that run
+    // together on the same K/V; with fewer rounds the finer single blocks
+    // balance the SMs better.
+    const long long paired = static_cast<long long>(p.C) * ((a.nqb + 1) / 2) * p.B * p.N;
+    a.pair_blocks = (a.nqb >= 2 && paired >= 8LL * sm_count()) ? 1 : 0;
+    a.nsp = a.pair_blocks ? (a.nqb + 1) / 2 : a.nqb;
+    a.div_nsp = make_fastdiv(static_cast<uint32_t>(a.nsp));
     a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
-    const long long n_items = static_cast<long long>(p.C) * a.nqb * p.B * p.N;
+    const long long n_items = static_cast<long long>(p.C) * a.nsp * p.B * p.N;
     if (n_items <= 0) return CP_OK;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
