@@ -309,6 +309,60 @@ def test_ring_full_size_sampled_rows(cuda_dev, wname):
     assert np.max(np.abs(l_g - l_ref[0].T)) <= ATOL_LSE
 
 
+def _pairs_blocks(C, Sq, B, N):
+    """The kernel pairs query blocks u and nqb-1-u into one work item when that
+    still leaves at least 8 rounds of items over the SMs."""
+    nqb = ((Sq + 127) // 128 + 1) // 2
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return nqb >= 2 and C * ((nqb + 1) // 2) * B * N >= 8 * sms
+
+
+def test_attn_partial_paired_blocks_gqa_ragged(cuda_dev):
+    """A launch large enough for paired query blocks, with 13 query heads per
+    K/V head, ragged Sq / Sk and an odd number of 256-row blocks (the middle
+    block is unpaired); causal positions; sampled rows of every block and head
+    against the oracle."""
+    B, Sq, Sk, N, Nkv, D = 2, 2800, 2900, 104, 8, 128
+    assert _pairs_blocks(1, Sq, B, N)
+    g = torch.Generator().manual_seed(41)
+    q = rand_bf16(B, Sq, N, D, gen=g)
+    k = rand_bf16(B, Sk, Nkv, D, gen=g)
+    v = rand_bf16(B, Sk, Nkv, D, gen=g)
+    qp = np.arange(Sk - Sq, Sk, dtype=np.int32)
+    kp = np.arange(Sk, dtype=np.int32)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = F.cp_attn_partial(q.to(cuda_dev), k.to(cuda_dev), v.to(cuda_dev), torch.as_tensor(qp).to(cuda_dev),
+                               torch.as_tensor(kp).to(cuda_dev), scale)
+    rows = np.unique(np.concatenate([np.arange(0, Sq, 23), np.arange(Sq - 3, Sq), [127, 128, 255, 256]]))
+    o_ref, l_ref = O.attn_rows(f64(q), f64(k), f64(v), qp, kp, rows, scale, nthreads=NTH)
+    r_idx = torch.as_tensor(rows, device=cuda_dev)
+    assert np.max(np.abs(f64(o[:, r_idx]) - o_ref)) <= ATOL_O
+    assert np.max(np.abs(f64(lse[:, :, r_idx]) - l_ref)) <= ATOL_LSE
+
+
+def test_ring_paired_blocks_sampled_rows(cuda_dev):
+    """Zigzag ring (4 ranks, S=16384, 40 heads) whose launches pair query
+    blocks; sampled rows of three heads against the oracle."""
+    w = SY.Workload("pairs16k", B=1, S=16384, N=40, Nkv=40, D=128, C=4)
+    assert _pairs_blocks(w.C, w.S // w.C, w.B, w.N)
+    (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, "zigzag")
+    o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1)
+    torch.cuda.synchronize()
+    rows = SY.sample_rows(w, n_random=64, edge=2)
+    heads = [0, 17, w.N - 1]
+    gp = np.arange(w.S, dtype=np.int32)
+    o_ref, l_ref = O.attn_rows(f64(q[:, :, heads]), f64(k[:, :, heads]), f64(v[:, :, heads]), gp, gp, rows,
+                               nthreads=NTH)
+    inv = _inverse_positions(pos.cpu().numpy())
+    r_idx = torch.as_tensor(inv[rows, 0], device=cuda_dev)
+    u_idx = torch.as_tensor(inv[rows, 1], device=cuda_dev)
+    h_idx = torch.as_tensor(heads, device=cuda_dev)
+    o_g = f64(o_sh[r_idx, 0, u_idx][:, h_idx])
+    l_g = f64(lse_sh[r_idx, 0, :, u_idx][:, h_idx])
+    assert np.max(np.abs(o_g - o_ref[0])) <= ATOL_O
+    assert np.max(np.abs(l_g - l_ref[0].T)) <= ATOL_LSE
+
+
 def test_device_status_clean(cuda_dev):
     assert F.cp_device_status(clear=True) == 0
 
