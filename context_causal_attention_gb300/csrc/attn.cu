@@ -132,49 +132,13 @@ struct Item {
     int qmax;  // largest query position of the 256-row block (over valid rows)
 };
 
-// A work item of the persistent schedule: one super-block (query blocks u and
-// nqb-1-u, or u alone) of one rank, batch entry and head.
-struct Super {
-    int r, u, b, h;
-};
-
-// Work-item index -> super item.  Items are laid out segment by segment, a
-// segment being a run of one rank's super-blocks with equal cost in the
-// longest-first order; inside a segment items go head-major (every super-block
-// of head 0, then head 1, ...), so CTAs running at the same time read the same
-// K/V heads.  seg_first[s] is the first ranked super-block of segment s (and
-// seg_first[#segments] their count); `seg` is the caller's cursor (the items of
-// one CTA come in increasing index order).
-__device__ __forceinline__ Super decode_super(int idx, const AttnArgs &a, const int *order, const int *seg_first,
-                                              int &seg) {
-    const int BN = a.B * a.N;
-    while (seg_first[seg + 1] * BN <= idx) ++seg;
-    const int f = seg_first[seg];
-    const int m = seg_first[seg + 1] - f;
-    const int local = idx - f * BN;
-    const int bh = local / m;
-    const uint32_t sp = static_cast<uint32_t>(order[f + (local - bh * m)]);
-    Super x;
-    x.r = static_cast<int>(fdiv(sp, a.div_nsp));
-    x.u = static_cast<int>(sp - static_cast<uint32_t>(x.r) * a.div_nsp.d);
-    x.b = static_cast<int>(fdiv(static_cast<uint32_t>(bh), a.div_n));
-    x.h = bh - x.b * a.N;
-    return x;
-}
-
-// Query block of part k (0 or 1) of a super item, -1 if it has no such part.
-__device__ __forceinline__ int sub_block(const Super &x, int k, const AttnArgs &a) {
-    if (k == 0) return x.u;
-    const int q2 = a.nqb - 1 - x.u;
-    return (a.pair_blocks && q2 != x.u) ? q2 : -1;
-}
-
-__device__ __forceinline__ Item make_item(const Super &x, int qb, const AttnArgs &a, const int2 *qtab) {
+// Work item of query block qb (a part of super item x) -> Item.
+__device__ __forceinline__ Item make_item(const SuperItem &x, int qb, const AttnArgs &a, const int2 *qtab) {
     Item it;
     it.r = x.r;
     it.qb = qb;
-    it.b = x.b;
-    it.h = x.h;
+    it.b = static_cast<int>(fdiv(static_cast<uint32_t>(x.bh), a.div_n));
+    it.h = x.bh - it.b * a.N;
     it.owner = it.r + a.kpos_shift;
     if (it.owner >= a.C) it.owner -= a.C;
     if (a.kpr == 1) it.owner = 0;
@@ -453,49 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cost[p] = c;
         }
         __syncthreads();
-        // super-block costs, held in the segment table until it is built
-        const int nsup = a.C * a.nsp;
-        int *sp_cost = seg_first;
-        for (int x = tid; x < nsup; x += kThreads) {
-            const int r = x / a.nsp, u = x - r * a.nsp, q2 = a.nqb - 1 - u;
-            int c = cost[r * a.nqb + u];
-            if (a.pair_blocks && q2 != u) c += cost[r * a.nqb + q2];
-            sp_cost[x] = c;
-        }
-        __syncthreads();
-        // rank by cost (descending), ties by index, i.e. by rank then block: so
-        // the super-blocks of one rank and cost are contiguous, and the first
-        // of them (no equal-cost one of its rank before it) opens a segment
-        constexpr int kHead = 1 << 30;
-        for (int x = tid; x < nsup; x += kThreads) {
-            const int c = sp_cost[x];
-            const int r0 = (x / a.nsp) * a.nsp;
-            int rank = 0;
-            bool head = true;
-            for (int y = 0; y < nsup; ++y) {
-                const int cy = sp_cost[y];
-                rank += (cy > c) || (cy == c && y < x);
-                head &= !(cy == c && y >= r0 && y < x);
-            }
-            order[rank] = x | (head ? kHead : 0);
-        }
-        __syncthreads();
-        if (warp == 0) {
-            int nseg = 0;
-            for (int c0 = 0; c0 < nsup; c0 += 32) {
-                const int i = c0 + lane;
-                bool head = false;
-                if (i < nsup) {
-                    const int v = order[i];
-                    head = (v & kHead) != 0;
-                    order[i] = v & ~kHead;
-                }
-                const unsigned msk = __ballot_sync(0xffffffffu, head);
-                if (head) seg_first[nseg + __popc(msk & ((1u << lane) - 1u))] = i;
-                nseg += __popc(msk);
-            }
-            if (lane == 0) seg_first[nseg] = nsup;
-        }
+        build_segments<kThreads>(cost, a.C, a.nqb, a.pair_blocks != 0, order, seg_first);
     }
     tc_fence_before();
     __syncthreads();
@@ -550,9 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                const Super sup = decode_super(idx, a, order, seg_first, seg);
+                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
                 for (int part = 0; part < 2 && ok; ++part) {
-                    const int qb = sub_block(sup, part, a);
+                    const int qb = super_part(sup.u, part, a.nqb, a.pair_blocks != 0);
                     if (qb < 0) continue;
                     const Item itm = make_item(sup, qb, a, qtab);
                     const int2 *kt_o = ktab + itm.owner * a.nkt;
@@ -629,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                const Super sup = decode_super(idx, a, order, seg_first, seg);
+                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
                 for (int part = 0; part < 2 && ok; ++part) {
-                    const int qb = sub_block(sup, part, a);
+                    const int qb = super_part(sup.u, part, a.nqb, a.pair_blocks != 0);
                     if (qb < 0) continue;
                     const Item itm = make_item(sup, qb, a, qtab);
                     const int n = cost[itm.r * a.nqb + itm.qb];  // key tiles of this item
@@ -698,9 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
             const int idx = item_of_round(rk, n_items);
             if (idx < 0) continue;
-            const Super sup = decode_super(idx, a, order, seg_first, seg);
+            const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
             for (int part = 0; part < 2 && ok; ++part) {
-                const int qb = sub_block(sup, part, a);
+                const int qb = super_part(sup.u, part, a.nqb, a.pair_blocks != 0);
                 if (qb < 0) continue;
                 const Item itm = make_item(sup, qb, a, qtab);
                 const int2 *kt_o = ktab + itm.owner * a.nkt;
@@ -1000,15 +922,11 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
     a.timeout_ns = p.timeout_ns ? p.timeout_ns : 2000000000ull;
     a.hold = p.hold;
-    // Pair query block u with block nqb-1-u in one work item when there are
-    // enough items for at least 8 rounds over the SMs: under a causal mask the
-    // two costs add up to about the same for every u, so every item costs about
-    // the same and the head-major order (decode_super) keeps the CTAs that run
-    // together on the same K/V; with fewer rounds the finer single blocks
-    // balance the SMs better.
-    const long long paired = static_cast<long long>(p.C) * ((a.nqb + 1) / 2) * p.B * p.N;
-    a.pair_blocks = (a.nqb >= 2 && paired >= 8LL * sm_count()) ? 1 : 0;
-    a.nsp = a.pair_blocks ? (a.nqb + 1) / 2 : a.nqb;
+    // query blocks u and nqb-1-u in one work item when that still leaves 8 rounds
+    // (then every item costs about the same and the head-major order keeps the
+    // CTAs that run together on the same K/V)
+    a.pair_blocks = pair_units(a.nqb, p.C, p.B * p.N, sm_count()) ? 1 : 0;
+    a.nsp = super_count(a.nqb, a.pair_blocks != 0);
     a.div_nsp = make_fastdiv(static_cast<uint32_t>(a.nsp));
     a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
     const long long n_items = static_cast<long long>(p.C) * a.nsp * p.B * p.N;

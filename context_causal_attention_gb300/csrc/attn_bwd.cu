@@ -76,7 +76,7 @@ struct Tiles {
 };
 
 // K/V-stationary kernel: K, V | Q, dO stages | nl2/nd strips per stage |
-// tables | order | cost | barriers | misc.
+// tables | order | cost | segments | barriers | misc.
 template <int D>
 struct CfgKV : Tiles<D> {
     using T = Tiles<D>;
@@ -88,7 +88,8 @@ struct CfgKV : Tiles<D> {
     static constexpr int kOffTab = kOffStat + kBStages * 1024;
     static constexpr int kOffOrder = kOffTab + kBwdMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kBwdMaxPairs * 4;
-    static constexpr int kOffBar = kOffCost + kBwdMaxPairs * 4;
+    static constexpr int kOffSeg = kOffCost + kBwdMaxPairs * 4;
+    static constexpr int kOffBar = kOffSeg + (kBwdMaxPairs + 2) * 4;
     // kv_full, kv_empty, qd_full[S], qd_empty[S], s_full, p_half, p_full, o_full, o_empty, drain
     // (p_half, p_full, o_empty: one arrival per compute warp)
     static constexpr int kNumBars = 2 + 2 * kBStages + 6;
@@ -98,7 +99,7 @@ struct CfgKV : Tiles<D> {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Q-stationary kernel: Q, dO | K, V stages | tables | order | cost | ...
+// Q-stationary kernel: Q, dO | K, V stages | tables | order | cost | segments | ...
 template <int D>
 struct CfgQ : Tiles<D> {
     using T = Tiles<D>;
@@ -109,7 +110,8 @@ struct CfgQ : Tiles<D> {
     static constexpr int kOffTab = kOffV + kBStages * T::kTile;
     static constexpr int kOffOrder = kOffTab + kBwdMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kBwdMaxPairs * 4;
-    static constexpr int kOffBar = kOffCost + kBwdMaxPairs * 4;
+    static constexpr int kOffSeg = kOffCost + kBwdMaxPairs * 4;
+    static constexpr int kOffBar = kOffSeg + (kBwdMaxPairs + 2) * 4;
     // qd_full, qd_empty, kv_full[S], kv_empty[S], s_full, p_half, p_full, o_full, o_empty, drain
     static constexpr int kNumBars = 2 + 2 * kBStages + 6;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -130,7 +132,8 @@ struct BwdArgs {
     int accumulate;
     float scale, scale_log2;
     unsigned long long timeout_ns;
-    FastDiv div_bh, div_nt, div_h;  // by B * (heads per item), stationary tiles per rank, heads per item
+    int pair;         // a super-block holds stationary tiles u and nt-1-u (else u alone)
+    FastDiv div_nsp, div_h;  // by super-blocks per rank, heads per item
 };
 
 // (min, max) of the positions of one 128-row tile (one warp per tile); when
@@ -214,20 +217,6 @@ __device__ __forceinline__ int count_k(const int2 *kt_o, int nk, int qmax, bool 
     return c;
 }
 
-// Longest-first order of the np (rank, stationary tile) pairs by cost; ties
-// keep index order.
-__device__ __forceinline__ void sort_pairs(const int *cost, int *order, int np, int tid) {
-    for (int p = tid; p < np; p += kBThreads) {
-        const int c = cost[p];
-        int rank = 0;
-        for (int q = 0; q < np; ++q) {
-            const int cq = cost[q];
-            rank += (cq > c) || (cq == c && q < p);
-        }
-        order[rank] = p;
-    }
-}
-
 // Row of D fp32 values from TMEM columns [col, col + D) of this thread's lane,
 // times `mul`, written to (or added to) dst (32-byte aligned).  Warp-collective.
 template <int D>
@@ -289,6 +278,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
     int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
     int *cost = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, key tile): visible query tiles
+    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
     int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per rank
@@ -354,27 +344,25 @@ __global__ void __launch_bounds__(kBThreads, 1)
         cost[p] = count_q(qtab + r * a.nq, a.nq, ktab[owner * a.nk + kt].x, sorted_flag[r] != 0);
     }
     __syncthreads();
-    sort_pairs(cost, order, np, tid);
+    build_segments<kBThreads>(cost, a.C, a.nk, a.pair != 0, order, seg_first);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_items = np * a.B * a.Nkv;
+    const int n_items = a.C * super_count(a.nk, a.pair != 0) * a.B * a.Nkv;
     const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     const int g_heads = a.N / a.Nkv;
     uint8_t *sK = smem + K::kOffK, *sV = smem + K::kOffV, *sQ = smem + K::kOffQ, *sDO = smem + K::kOffDO;
     float *sStat = reinterpret_cast<float *>(smem + K::kOffStat);
 
-    // item idx -> (pair, b, KV head)
-    auto decode = [&](int idx, int &r, int &kt, int &b, int &hk, int &owner, int &kvr, int &pr) {
-        const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bh);
-        const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bh.d;
-        pr = order[pi];
-        r = static_cast<int>(fdiv(static_cast<uint32_t>(pr), a.div_nt));
-        kt = pr - r * a.nk;
-        b = static_cast<int>(fdiv(bh, a.div_h));
-        hk = static_cast<int>(bh) - b * a.Nkv;
+    // key tile `unit` of super item x -> (rank, key tile, b, KV head, ...)
+    auto decode = [&](const SuperItem &x, int unit, int &r, int &kt, int &b, int &hk, int &owner, int &kvr, int &pr) {
+        r = x.r;
+        kt = unit;
+        pr = r * a.nk + kt;
+        b = static_cast<int>(fdiv(static_cast<uint32_t>(x.bh), a.div_h));
+        hk = x.bh - b * a.Nkv;
         owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
         kvr = (r + a.kv_shift) % a.C;
     };
@@ -386,43 +374,49 @@ __global__ void __launch_bounds__(kBThreads, 1)
             bool ok = true;
             int kv_par = -1;
             uint32_t qd_issued = 0, qd_par = 0;
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                int r, kt, b, hk, owner, kvr, pr;
-                decode(idx, r, kt, b, hk, owner, kvr, pr);
-                if (cost[pr] == 0) continue;
-                if (!mbar_wait(kv_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(kv_full, 2 * K::kTile);
-                kv_par = static_cast<int>(it & 1u);
-                const int kvrow = kvr * a.B + b;
-                for (int at = 0; at < K::kAtoms; ++at) {
-                    tma_load_4d(sK + at * K::kAtom, &tmK, kv_full, 64 * at, hk, kt * 128, kvrow);
-                    tma_load_4d(sV + at * K::kAtom, &tmV, kv_full, 64 * at, hk, kt * 128, kvrow);
-                }
-                ++it;
-                const int2 *qt_r = qtab + r * a.nq;
-                const int kmin = ktab[owner * a.nk + kt].x;
-                const bool srt = sorted_flag[r] != 0;
-                const int qrow = r * a.B + b;
-                for (int hh = 0; hh < g_heads && ok; ++hh) {
-                    const int h = hk * g_heads + hh;
-                    const int srow = qrow * a.N + h;
-                    for (int qt = first_q(qt_r, a.nq, kmin, srt); qt < a.nq; qt = next_q(qt + 1, qt_r, a.nq, kmin)) {
-                        const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
-                        if (!mbar_wait(qd_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                        mbar_arrive_expect_tx(qd_full + st, 2 * K::kTile + 1024);
-                        for (int at = 0; at < K::kAtoms; ++at) {
-                            tma_load_4d(sQ + st * K::kTile + at * K::kAtom, &tmQ, qd_full + st, 64 * at, h, qt * 128,
-                                        qrow);
-                            tma_load_4d(sDO + st * K::kTile + at * K::kAtom, &tmDO, qd_full + st, 64 * at, h, qt * 128,
-                                        qrow);
+                const SuperItem sup = decode_super(idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int unit = super_part(sup.u, part, a.nk, a.pair != 0);
+                    if (unit < 0) continue;
+                    int r, kt, b, hk, owner, kvr, pr;
+                    decode(sup, unit, r, kt, b, hk, owner, kvr, pr);
+                    if (cost[pr] == 0) continue;
+                    if (!mbar_wait(kv_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(kv_full, 2 * K::kTile);
+                    kv_par = static_cast<int>(it & 1u);
+                    const int kvrow = kvr * a.B + b;
+                    for (int at = 0; at < K::kAtoms; ++at) {
+                        tma_load_4d(sK + at * K::kAtom, &tmK, kv_full, 64 * at, hk, kt * 128, kvrow);
+                        tma_load_4d(sV + at * K::kAtom, &tmV, kv_full, 64 * at, hk, kt * 128, kvrow);
+                    }
+                    ++it;
+                    const int2 *qt_r = qtab + r * a.nq;
+                    const int kmin = ktab[owner * a.nk + kt].x;
+                    const bool srt = sorted_flag[r] != 0;
+                    const int qrow = r * a.B + b;
+                    for (int hh = 0; hh < g_heads && ok; ++hh) {
+                        const int h = hk * g_heads + hh;
+                        const int srow = qrow * a.N + h;
+                        for (int qt = first_q(qt_r, a.nq, kmin, srt); qt < a.nq; qt = next_q(qt + 1, qt_r, a.nq, kmin)) {
+                            const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
+                            if (!mbar_wait(qd_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                            mbar_arrive_expect_tx(qd_full + st, 2 * K::kTile + 1024);
+                            for (int at = 0; at < K::kAtoms; ++at) {
+                                tma_load_4d(sQ + st * K::kTile + at * K::kAtom, &tmQ, qd_full + st, 64 * at, h, qt * 128,
+                                            qrow);
+                                tma_load_4d(sDO + st * K::kTile + at * K::kAtom, &tmDO, qd_full + st, 64 * at, h, qt * 128,
+                                            qrow);
+                            }
+                            tma_load_2d(sStat + st * 256, &tmNL2, qd_full + st, qt * 128, srow);
+                            tma_load_2d(sStat + st * 256 + 128, &tmND, qd_full + st, qt * 128, srow);
+                            qd_issued |= 1u << st;
+                            qd_par = (qd_par & ~(1u << st)) | (ph << st);
+                            ++t;
                         }
-                        tma_load_2d(sStat + st * 256, &tmNL2, qd_full + st, qt * 128, srow);
-                        tma_load_2d(sStat + st * 256 + 128, &tmND, qd_full + st, qt * 128, srow);
-                        qd_issued |= 1u << st;
-                        qd_par = (qd_par & ~(1u << st)) | (ph << st);
-                        ++t;
                     }
                 }
             }
@@ -450,41 +444,47 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const uint64_t dOm = smem_desc_sw128(smem_u32(sDO), K::kAtom, 1024);
             uint32_t it = 0, t = 0;
             bool ok = true;
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                int r, kt, b, hk, owner, kvr, pr;
-                decode(idx, r, kt, b, hk, owner, kvr, pr);
-                const int n = g_heads * cost[pr];
-                if (n == 0) continue;
-                if (!mbar_wait(kv_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
-                for (int i = 0; i < n; ++i, ++t) {
-                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
-                    if (!mbar_wait(qd_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                const SuperItem sup = decode_super(idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int unit = super_part(sup.u, part, a.nk, a.pair != 0);
+                    if (unit < 0) continue;
+                    int r, kt, b, hk, owner, kvr, pr;
+                    decode(sup, unit, r, kt, b, hk, owner, kvr, pr);
+                    const int n = g_heads * cost[pr];
+                    if (n == 0) continue;
+                    if (!mbar_wait(kv_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    // S^T and dP^T overwrite the previous tile's P^T / dS^T: in
-                    // issue order after that tile's gradient MMAs
-                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem, dK, dQk + st * kStU, kIdS);
-                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem + 128, dV, dOk + st * kStU, kIdS);
-                    umma_commit(s_full);
-                    if (i == n - 1) umma_commit(kv_empty);  // K and V are read by S^T / dP^T only
-                    // dV += P^T dO, dK += dS^T Q over the tile's first 64 queries,
-                    // then over the second 64; `first` overwrites the accumulators
-                    if (!mbar_wait(p_half, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    if (i == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    umma_ts_k64_split(tmem + 256, tmem, dOm + st * kStU, kIdG, i == 0 ? 0u : 1u);
-                    umma_ts_k64_split(tmem + 256 + D, tmem + 128, dQm + st * kStU, kIdG, i == 0 ? 0u : 1u);
-                    if (!mbar_wait(p_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    umma_ts_k64_split(tmem + 256, tmem + 64, dOm + st * kStU + kHalfU, kIdG, 1u);
-                    umma_ts_k64_split(tmem + 256 + D, tmem + 192, dQm + st * kStU + kHalfU, kIdG, 1u);
-                    umma_commit(qd_empty + st);
+                    for (int i = 0; i < n; ++i, ++t) {
+                        const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
+                        if (!mbar_wait(qd_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        // S^T and dP^T overwrite the previous tile's P^T / dS^T: in
+                        // issue order after that tile's gradient MMAs
+                        umma_ss_kgroup<D / 16, 1024, 1024>(tmem, dK, dQk + st * kStU, kIdS);
+                        umma_ss_kgroup<D / 16, 1024, 1024>(tmem + 128, dV, dOk + st * kStU, kIdS);
+                        umma_commit(s_full);
+                        if (i == n - 1) umma_commit(kv_empty);  // K and V are read by S^T / dP^T only
+                        // dV += P^T dO, dK += dS^T Q over the tile's first 64 queries,
+                        // then over the second 64; `first` overwrites the accumulators
+                        if (!mbar_wait(p_half, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (i == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        umma_ts_k64_split(tmem + 256, tmem, dOm + st * kStU, kIdG, i == 0 ? 0u : 1u);
+                        umma_ts_k64_split(tmem + 256 + D, tmem + 128, dQm + st * kStU, kIdG, i == 0 ? 0u : 1u);
+                        if (!mbar_wait(p_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        umma_ts_k64_split(tmem + 256, tmem + 64, dOm + st * kStU + kHalfU, kIdG, 1u);
+                        umma_ts_k64_split(tmem + 256 + D, tmem + 192, dQm + st * kStU + kHalfU, kIdG, 1u);
+                        umma_commit(qd_empty + st);
+                    }
+                    if (!ok) break;
+                    umma_commit(o_full);
+                    ++it;
                 }
-                if (!ok) break;
-                umma_commit(o_full);
-                ++it;
             }
             // no MMA may still be running when TMEM is released
             umma_commit(drain);
@@ -501,113 +501,119 @@ __global__ void __launch_bounds__(kBThreads, 1)
         const uint64_t sl2x2 = f2_packf(a.scale_log2, a.scale_log2);
         uint32_t it = 0, t = 0;
         bool ok = true;
+        int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
             const int idx = item_of_round(rk, n_items);
             if (idx < 0) continue;
-            int r, kt, b, hk, owner, kvr, pr;
-            decode(idx, r, kt, b, hk, owner, kvr, pr);
-            const int key = kt * 128 + row_in;
-            const bool key_valid = key < a.Sk;
-            const int kpos = key_valid ? __ldg(a.k_pos + owner * a.k_pos_stride + key) : INT_MAX;
-            const long long krow = (static_cast<long long>(kvr * a.B + b) * a.Sk + key) * a.Nkv + hk;
-            // each group writes half of the row's D columns
-            float *dk_row = a.dk + krow * D + grp * (D / 2);
-            float *dv_row = a.dv + krow * D + grp * (D / 2);
-            if (cost[pr] == 0) {
-                // no query sees these keys: their gradients are zero
-                if (key_valid && !a.accumulate) {
-                    zero_row<D / 2>(dk_row);
-                    zero_row<D / 2>(dv_row);
+            const SuperItem sup = decode_super(idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
+            for (int part = 0; part < 2 && ok; ++part) {
+                const int unit = super_part(sup.u, part, a.nk, a.pair != 0);
+                if (unit < 0) continue;
+                int r, kt, b, hk, owner, kvr, pr;
+                decode(sup, unit, r, kt, b, hk, owner, kvr, pr);
+                const int key = kt * 128 + row_in;
+                const bool key_valid = key < a.Sk;
+                const int kpos = key_valid ? __ldg(a.k_pos + owner * a.k_pos_stride + key) : INT_MAX;
+                const long long krow = (static_cast<long long>(kvr * a.B + b) * a.Sk + key) * a.Nkv + hk;
+                // each group writes half of the row's D columns
+                float *dk_row = a.dk + krow * D + grp * (D / 2);
+                float *dv_row = a.dv + krow * D + grp * (D / 2);
+                if (cost[pr] == 0) {
+                    // no query sees these keys: their gradients are zero
+                    if (key_valid && !a.accumulate) {
+                        zero_row<D / 2>(dk_row);
+                        zero_row<D / 2>(dv_row);
+                    }
+                    continue;
                 }
-                continue;
-            }
-            const int2 kmm = ktab[owner * a.nk + kt];
-            const int2 *qt_r = qtab + r * a.nq;
-            const bool srt = sorted_flag[r] != 0;
-            const int32_t *qpos_r = a.q_pos + r * a.q_pos_stride;
-            for (int hh = 0; hh < g_heads && ok; ++hh) {
-                for (int qt = first_q(qt_r, a.nq, kmm.x, srt); qt < a.nq;
-                     qt = next_q(qt + 1, qt_r, a.nq, kmm.x), ++t) {
-                    const uint32_t st = t % kBStages;
-                    if (!mbar_wait_warp(s_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    const int2 qmm = qt_r[qt];
-                    const int q0 = qt * 128;
-                    const bool need_mask = kmm.y > qmm.x || q0 + 128 > a.Sq;
-                    const int gq = r * a.nq + qt;
-                    const bool arith = (arith_bits[gq >> 5] >> (gq & 31)) & 1u;
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        // this warp's columns: cb .. cb+31 = queries q0 + cb ..
-                        const int cb = 64 * h + 32 * grp;
-                        uint32_t s[32], dp[32];
-                        tmem_ld32_nowait(tA + cb, s);
-                        tmem_ld32_nowait(tA + 128 + cb, dp);
-                        tmem_wait_ld32(s);
-                        tmem_wait_ld32(dp);
-                        if (need_mask) {
-                            const int qh = q0 + cb;
-                            const int nvalid = min(32, a.Sq - qh);
-                            if (arith) {
-                                // query positions qmin + cb + c: column c visible iff c >= kpos - qmin - cb
-                                const long long dlo = static_cast<long long>(kpos) - qmm.x - cb;
-                                const int lo = dlo <= 0 ? 0 : (dlo > 32 ? 32 : static_cast<int>(dlo));
-#pragma unroll
-                                for (int c = 0; c < 32; ++c)
-                                    if (c < lo || c >= nvalid) s[c] = kNegInfBits;
-                            } else {
-#pragma unroll
-                                for (int c0 = 0; c0 < 32; c0 += 16) {
-#pragma unroll
-                                    for (int c = c0; c < c0 + 16; ++c) {
-                                        const int qp = (c < nvalid) ? __ldg(qpos_r + qh + c) : INT_MIN;
-                                        if (kpos > qp) s[c] = kNegInfBits;
+                const int2 kmm = ktab[owner * a.nk + kt];
+                const int2 *qt_r = qtab + r * a.nq;
+                const bool srt = sorted_flag[r] != 0;
+                const int32_t *qpos_r = a.q_pos + r * a.q_pos_stride;
+                for (int hh = 0; hh < g_heads && ok; ++hh) {
+                    for (int qt = first_q(qt_r, a.nq, kmm.x, srt); qt < a.nq;
+                         qt = next_q(qt + 1, qt_r, a.nq, kmm.x), ++t) {
+                        const uint32_t st = t % kBStages;
+                        if (!mbar_wait_warp(s_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        const int2 qmm = qt_r[qt];
+                        const int q0 = qt * 128;
+                        const bool need_mask = kmm.y > qmm.x || q0 + 128 > a.Sq;
+                        const int gq = r * a.nq + qt;
+                        const bool arith = (arith_bits[gq >> 5] >> (gq & 31)) & 1u;
+    #pragma unroll 1
+                        for (int h = 0; h < 2; ++h) {
+                            // this warp's columns: cb .. cb+31 = queries q0 + cb ..
+                            const int cb = 64 * h + 32 * grp;
+                            uint32_t s[32], dp[32];
+                            tmem_ld32_nowait(tA + cb, s);
+                            tmem_ld32_nowait(tA + 128 + cb, dp);
+                            tmem_wait_ld32(s);
+                            tmem_wait_ld32(dp);
+                            if (need_mask) {
+                                const int qh = q0 + cb;
+                                const int nvalid = min(32, a.Sq - qh);
+                                if (arith) {
+                                    // query positions qmin + cb + c: column c visible iff c >= kpos - qmin - cb
+                                    const long long dlo = static_cast<long long>(kpos) - qmm.x - cb;
+                                    const int lo = dlo <= 0 ? 0 : (dlo > 32 ? 32 : static_cast<int>(dlo));
+    #pragma unroll
+                                    for (int c = 0; c < 32; ++c)
+                                        if (c < lo || c >= nvalid) s[c] = kNegInfBits;
+                                } else {
+    #pragma unroll
+                                    for (int c0 = 0; c0 < 32; c0 += 16) {
+    #pragma unroll
+                                        for (int c = c0; c < c0 + 16; ++c) {
+                                            const int qp = (c < nvalid) ? __ldg(qpos_r + qh + c) : INT_MIN;
+                                            if (kpos > qp) s[c] = kNegInfBits;
+                                        }
+                                        asm volatile("" ::: "memory");
                                     }
-                                    asm volatile("" ::: "memory");
                                 }
                             }
+                            // P^T = 2^(s sl2 + nl2_c), dS^T = P^T (dP^T + nd_c), column stats from the stage
+                            const float *nl = sStat + st * 256 + cb, *nd = nl + 128;
+                            uint32_t pk_p[16], pk_d[16];
+    #pragma unroll
+                            for (int c = 0; c < 32; c += 4) {
+                                const float4 l4 = *reinterpret_cast<const float4 *>(nl + c);
+                                const float4 d4 = *reinterpret_cast<const float4 *>(nd + c);
+                                float x0, x1, x2, x3, g0, g1, g2, g3;
+                                f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, f2_packf(l4.x, l4.y)), x0, x1);
+                                f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, f2_packf(l4.z, l4.w)), x2, x3);
+                                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2),
+                                            p3 = fast_exp2(x3);
+                                f2_unpack(f2_fma(f2_packf(p0, p1),
+                                                 f2_add(f2_pack(dp[c], dp[c + 1]), f2_packf(d4.x, d4.y)), 0ull),
+                                          g0, g1);
+                                f2_unpack(f2_fma(f2_packf(p2, p3),
+                                                 f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_packf(d4.z, d4.w)), 0ull),
+                                          g2, g3);
+                                pk_p[c >> 1] = pack_bf16x2(p0, p1);
+                                pk_p[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+                                pk_d[c >> 1] = pack_bf16x2(g0, g1);
+                                pk_d[(c >> 1) + 1] = pack_bf16x2(g2, g3);
+                            }
+                            // packed over the first 16 of this warp's own 32 columns (already
+                            // read; no other warp reads them): the MMA finds the half's
+                            // 64 packed queries at columns 64h + {0..15, 32..47}
+                            tmem_st16_nowait(tA + cb, pk_p);
+                            tmem_st16_nowait(tA + 128 + cb, pk_d);
+                            release_half(h == 0 ? p_half : p_full, lane);
                         }
-                        // P^T = 2^(s sl2 + nl2_c), dS^T = P^T (dP^T + nd_c), column stats from the stage
-                        const float *nl = sStat + st * 256 + cb, *nd = nl + 128;
-                        uint32_t pk_p[16], pk_d[16];
-#pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            const float4 l4 = *reinterpret_cast<const float4 *>(nl + c);
-                            const float4 d4 = *reinterpret_cast<const float4 *>(nd + c);
-                            float x0, x1, x2, x3, g0, g1, g2, g3;
-                            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, f2_packf(l4.x, l4.y)), x0, x1);
-                            f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, f2_packf(l4.z, l4.w)), x2, x3);
-                            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2),
-                                        p3 = fast_exp2(x3);
-                            f2_unpack(f2_fma(f2_packf(p0, p1),
-                                             f2_add(f2_pack(dp[c], dp[c + 1]), f2_packf(d4.x, d4.y)), 0ull),
-                                      g0, g1);
-                            f2_unpack(f2_fma(f2_packf(p2, p3),
-                                             f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_packf(d4.z, d4.w)), 0ull),
-                                      g2, g3);
-                            pk_p[c >> 1] = pack_bf16x2(p0, p1);
-                            pk_p[(c >> 1) + 1] = pack_bf16x2(p2, p3);
-                            pk_d[c >> 1] = pack_bf16x2(g0, g1);
-                            pk_d[(c >> 1) + 1] = pack_bf16x2(g2, g3);
-                        }
-                        // packed over the first 16 of this warp's own 32 columns (already
-                        // read; no other warp reads them): the MMA finds the half's
-                        // 64 packed queries at columns 64h + {0..15, 32..47}
-                        tmem_st16_nowait(tA + cb, pk_p);
-                        tmem_st16_nowait(tA + 128 + cb, pk_d);
-                        release_half(h == 0 ? p_half : p_full, lane);
                     }
                 }
+                if (!ok) break;
+                if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                store_acc_row<D / 2>(tA + 256 + grp * (D / 2), dv_row, 1.f, key_valid, a.accumulate != 0);
+                store_acc_row<D / 2>(tA + 256 + D + grp * (D / 2), dk_row, a.scale, key_valid, a.accumulate != 0);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty);
+                ++it;
             }
-            if (!ok) break;
-            if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-            tc_fence_after();
-            store_acc_row<D / 2>(tA + 256 + grp * (D / 2), dv_row, 1.f, key_valid, a.accumulate != 0);
-            store_acc_row<D / 2>(tA + 256 + D + grp * (D / 2), dk_row, a.scale, key_valid, a.accumulate != 0);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_empty);
-            ++it;
         }
     }
 
@@ -636,6 +642,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
     int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
     int *cost = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, query tile): visible key tiles
+    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
     int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per key-position rank
@@ -699,25 +706,24 @@ __global__ void __launch_bounds__(kBThreads, 1)
         cost[p] = count_k(ktab + owner * a.nk, a.nk, qtab[r * a.nq + qt].y, sorted_flag[owner] != 0);
     }
     __syncthreads();
-    sort_pairs(cost, order, np, tid);
+    build_segments<kBThreads>(cost, a.C, a.nq, a.pair != 0, order, seg_first);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_items = np * a.B * a.N;
+    const int n_items = a.C * super_count(a.nq, a.pair != 0) * a.B * a.N;
     const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     const int g_heads = a.N / a.Nkv;
     uint8_t *sQ = smem + K::kOffQ, *sDO = smem + K::kOffDO, *sK = smem + K::kOffK, *sV = smem + K::kOffV;
 
-    auto decode = [&](int idx, int &r, int &qt, int &b, int &h, int &owner, int &kvr, int &pr) {
-        const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bh);
-        const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bh.d;
-        pr = order[pi];
-        r = static_cast<int>(fdiv(static_cast<uint32_t>(pr), a.div_nt));
-        qt = pr - r * a.nq;
-        b = static_cast<int>(fdiv(bh, a.div_h));
-        h = static_cast<int>(bh) - b * a.N;
+    // query tile `unit` of super item x -> (rank, query tile, b, head, ...)
+    auto decode = [&](const SuperItem &x, int unit, int &r, int &qt, int &b, int &h, int &owner, int &kvr, int &pr) {
+        r = x.r;
+        qt = unit;
+        pr = r * a.nq + qt;
+        b = static_cast<int>(fdiv(static_cast<uint32_t>(x.bh), a.div_h));
+        h = x.bh - b * a.N;
         owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
         kvr = (r + a.kv_shift) % a.C;
     };
@@ -729,39 +735,45 @@ __global__ void __launch_bounds__(kBThreads, 1)
             bool ok = true;
             int qd_par = -1;
             uint32_t kv_issued = 0, kv_par = 0;
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                int r, qt, b, h, owner, kvr, pr;
-                decode(idx, r, qt, b, h, owner, kvr, pr);
-                if (cost[pr] == 0) continue;
-                if (!mbar_wait(qd_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(qd_full, 2 * K::kTile);
-                qd_par = static_cast<int>(it & 1u);
-                const int qrow = r * a.B + b;
-                for (int at = 0; at < K::kAtoms; ++at) {
-                    tma_load_4d(sQ + at * K::kAtom, &tmQ, qd_full, 64 * at, h, qt * 128, qrow);
-                    tma_load_4d(sDO + at * K::kAtom, &tmDO, qd_full, 64 * at, h, qt * 128, qrow);
-                }
-                ++it;
-                const int2 *kt_o = ktab + owner * a.nk;
-                const int qmax = qtab[r * a.nq + qt].y;
-                const bool srt = sorted_flag[owner] != 0;
-                const int hk = h / g_heads;
-                const int kvrow = kvr * a.B + b;
-                for (int kt = next_k(0, kt_o, a.nk, qmax, srt); kt < a.nk; kt = next_k(kt + 1, kt_o, a.nk, qmax, srt)) {
-                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
-                    if (!mbar_wait(kv_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    mbar_arrive_expect_tx(kv_full + st, 2 * K::kTile);
+                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int unit = super_part(sup.u, part, a.nq, a.pair != 0);
+                    if (unit < 0) continue;
+                    int r, qt, b, h, owner, kvr, pr;
+                    decode(sup, unit, r, qt, b, h, owner, kvr, pr);
+                    if (cost[pr] == 0) continue;
+                    if (!mbar_wait(qd_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(qd_full, 2 * K::kTile);
+                    qd_par = static_cast<int>(it & 1u);
+                    const int qrow = r * a.B + b;
                     for (int at = 0; at < K::kAtoms; ++at) {
-                        tma_load_4d(sK + st * K::kTile + at * K::kAtom, &tmK, kv_full + st, 64 * at, hk, kt * 128,
-                                    kvrow);
-                        tma_load_4d(sV + st * K::kTile + at * K::kAtom, &tmV, kv_full + st, 64 * at, hk, kt * 128,
-                                    kvrow);
+                        tma_load_4d(sQ + at * K::kAtom, &tmQ, qd_full, 64 * at, h, qt * 128, qrow);
+                        tma_load_4d(sDO + at * K::kAtom, &tmDO, qd_full, 64 * at, h, qt * 128, qrow);
                     }
-                    kv_issued |= 1u << st;
-                    kv_par = (kv_par & ~(1u << st)) | (ph << st);
-                    ++t;
+                    ++it;
+                    const int2 *kt_o = ktab + owner * a.nk;
+                    const int qmax = qtab[r * a.nq + qt].y;
+                    const bool srt = sorted_flag[owner] != 0;
+                    const int hk = h / g_heads;
+                    const int kvrow = kvr * a.B + b;
+                    for (int kt = next_k(0, kt_o, a.nk, qmax, srt); kt < a.nk; kt = next_k(kt + 1, kt_o, a.nk, qmax, srt)) {
+                        const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
+                        if (!mbar_wait(kv_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        mbar_arrive_expect_tx(kv_full + st, 2 * K::kTile);
+                        for (int at = 0; at < K::kAtoms; ++at) {
+                            tma_load_4d(sK + st * K::kTile + at * K::kAtom, &tmK, kv_full + st, 64 * at, hk, kt * 128,
+                                        kvrow);
+                            tma_load_4d(sV + st * K::kTile + at * K::kAtom, &tmV, kv_full + st, 64 * at, hk, kt * 128,
+                                        kvrow);
+                        }
+                        kv_issued |= 1u << st;
+                        kv_par = (kv_par & ~(1u << st)) | (ph << st);
+                        ++t;
+                    }
                 }
             }
             if (!ok) {
@@ -787,36 +799,42 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const uint64_t dKm = smem_desc_sw128(smem_u32(sK), K::kAtom, 1024);
             uint32_t it = 0, t = 0;
             bool ok = true;
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                int r, qt, b, h, owner, kvr, pr;
-                decode(idx, r, qt, b, h, owner, kvr, pr);
-                const int n = cost[pr];
-                if (n == 0) continue;
-                if (!mbar_wait(qd_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
-                for (int j = 0; j < n; ++j, ++t) {
-                    const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
-                    if (!mbar_wait(kv_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int unit = super_part(sup.u, part, a.nq, a.pair != 0);
+                    if (unit < 0) continue;
+                    int r, qt, b, h, owner, kvr, pr;
+                    decode(sup, unit, r, qt, b, h, owner, kvr, pr);
+                    const int n = cost[pr];
+                    if (n == 0) continue;
+                    if (!mbar_wait(qd_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem, dQa, dKb + st * kStU, kIdS);
-                    umma_ss_kgroup<D / 16, 1024, 1024>(tmem + 128, dOa, dVb + st * kStU, kIdS);
-                    umma_commit(s_full);
-                    if (j == n - 1) umma_commit(qd_empty);  // Q and dO are read by S / dP only
-                    // dQ += dS K over the tile's first 64 keys, then the second 64
-                    if (!mbar_wait(p_half, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    umma_ts_k64_split(tmem + 256, tmem, dKm + st * kStU, kIdG, j == 0 ? 0u : 1u);
-                    if (!mbar_wait(p_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    umma_ts_k64_split(tmem + 256, tmem + 64, dKm + st * kStU + kHalfU, kIdG, 1u);
-                    umma_commit(kv_empty + st);  // K (S and dQ) and V (dP) of this stage are read
+                    for (int j = 0; j < n; ++j, ++t) {
+                        const uint32_t st = t % kBStages, ph = (t / kBStages) & 1u;
+                        if (!mbar_wait(kv_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        umma_ss_kgroup<D / 16, 1024, 1024>(tmem, dQa, dKb + st * kStU, kIdS);
+                        umma_ss_kgroup<D / 16, 1024, 1024>(tmem + 128, dOa, dVb + st * kStU, kIdS);
+                        umma_commit(s_full);
+                        if (j == n - 1) umma_commit(qd_empty);  // Q and dO are read by S / dP only
+                        // dQ += dS K over the tile's first 64 keys, then the second 64
+                        if (!mbar_wait(p_half, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        umma_ts_k64_split(tmem + 256, tmem, dKm + st * kStU, kIdG, j == 0 ? 0u : 1u);
+                        if (!mbar_wait(p_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        umma_ts_k64_split(tmem + 256, tmem + 64, dKm + st * kStU + kHalfU, kIdG, 1u);
+                        umma_commit(kv_empty + st);  // K (S and dQ) and V (dP) of this stage are read
+                    }
+                    if (!ok) break;
+                    umma_commit(o_full);
+                    ++it;
                 }
-                if (!ok) break;
-                umma_commit(o_full);
-                ++it;
             }
             umma_commit(drain);
             volatile int no_abort = 0;
@@ -832,91 +850,97 @@ __global__ void __launch_bounds__(kBThreads, 1)
         const uint64_t sl2x2 = f2_packf(a.scale_log2, a.scale_log2);
         uint32_t it = 0, t = 0;
         bool ok = true;
+        int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
             const int idx = item_of_round(rk, n_items);
             if (idx < 0) continue;
-            int r, qt, b, h, owner, kvr, pr;
-            decode(idx, r, qt, b, h, owner, kvr, pr);
-            const int row = qt * 128 + row_in;
-            const bool row_valid = row < a.Sq;
-            const int qpos = row_valid ? __ldg(a.q_pos + r * a.q_pos_stride + row) : INT_MIN;
-            const long long qrow = static_cast<long long>(r * a.B + b);
-            float *dq_row = a.dq + ((qrow * a.Sq + row) * a.N + h) * D + grp * (D / 2);
-            if (cost[pr] == 0) {
-                if (row_valid && !a.accumulate) zero_row<D / 2>(dq_row);
-                continue;
-            }
-            // rows past Sq read the padding (-inf, 0): they see nothing
-            const long long srow = (qrow * a.N + h) * a.sq_pad + row;
-            const float nl2 = __ldg(a.nl2 + srow), ndv = __ldg(a.nd + srow);
-            const uint64_t nl2x2 = f2_packf(nl2, nl2), ndx2 = f2_packf(ndv, ndv);
-            const int2 *kt_o = ktab + owner * a.nk;
-            const int2 qmm = qtab[r * a.nq + qt];
-            const bool srt = sorted_flag[owner] != 0;
-            const int32_t *kpos_o = a.k_pos + owner * a.k_pos_stride;
-            for (int kt = next_k(0, kt_o, a.nk, qmm.y, srt); kt < a.nk;
-                 kt = next_k(kt + 1, kt_o, a.nk, qmm.y, srt), ++t) {
-                if (!mbar_wait_warp(s_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
-                const int2 kmm = kt_o[kt];
-                const int k0 = kt * 128;
-                const bool need_mask = kmm.y > qmm.x || k0 + 128 > a.Sk;
-                const int gk = owner * a.nk + kt;
-                const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
-#pragma unroll 1
-                for (int hf = 0; hf < 2; ++hf) {
-                    // this warp's columns: cb .. cb+31 = keys k0 + cb ..
-                    const int cb = 64 * hf + 32 * grp;
-                    uint32_t s[32], dp[32];
-                    tmem_ld32_nowait(tA + cb, s);
-                    tmem_ld32_nowait(tA + 128 + cb, dp);
-                    tmem_wait_ld32(s);
-                    tmem_wait_ld32(dp);
-                    if (need_mask) {
-                        const int kh = k0 + cb;
-                        const int nvalid = min(32, a.Sk - kh);
-                        if (arith) {
-                            // key positions kmin + cb + c: column c visible iff c <= qpos - kmin - cb
-                            const long long dhi = static_cast<long long>(qpos) - kmm.x - cb;
-                            const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                if (c > lim) s[c] = kNegInfBits;
-                        } else {
-#pragma unroll
-                            for (int c0 = 0; c0 < 32; c0 += 16) {
-#pragma unroll
-                                for (int c = c0; c < c0 + 16; ++c) {
-                                    const int kp = (c < nvalid) ? __ldg(kpos_o + kh + c) : INT_MAX;
-                                    if (kp > qpos) s[c] = kNegInfBits;
+            const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+            for (int part = 0; part < 2 && ok; ++part) {
+                const int unit = super_part(sup.u, part, a.nq, a.pair != 0);
+                if (unit < 0) continue;
+                int r, qt, b, h, owner, kvr, pr;
+                decode(sup, unit, r, qt, b, h, owner, kvr, pr);
+                const int row = qt * 128 + row_in;
+                const bool row_valid = row < a.Sq;
+                const int qpos = row_valid ? __ldg(a.q_pos + r * a.q_pos_stride + row) : INT_MIN;
+                const long long qrow = static_cast<long long>(r * a.B + b);
+                float *dq_row = a.dq + ((qrow * a.Sq + row) * a.N + h) * D + grp * (D / 2);
+                if (cost[pr] == 0) {
+                    if (row_valid && !a.accumulate) zero_row<D / 2>(dq_row);
+                    continue;
+                }
+                // rows past Sq read the padding (-inf, 0): they see nothing
+                const long long srow = (qrow * a.N + h) * a.sq_pad + row;
+                const float nl2 = __ldg(a.nl2 + srow), ndv = __ldg(a.nd + srow);
+                const uint64_t nl2x2 = f2_packf(nl2, nl2), ndx2 = f2_packf(ndv, ndv);
+                const int2 *kt_o = ktab + owner * a.nk;
+                const int2 qmm = qtab[r * a.nq + qt];
+                const bool srt = sorted_flag[owner] != 0;
+                const int32_t *kpos_o = a.k_pos + owner * a.k_pos_stride;
+                for (int kt = next_k(0, kt_o, a.nk, qmm.y, srt); kt < a.nk;
+                     kt = next_k(kt + 1, kt_o, a.nk, qmm.y, srt), ++t) {
+                    if (!mbar_wait_warp(s_full, t & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const int2 kmm = kt_o[kt];
+                    const int k0 = kt * 128;
+                    const bool need_mask = kmm.y > qmm.x || k0 + 128 > a.Sk;
+                    const int gk = owner * a.nk + kt;
+                    const bool arith = (arith_bits[gk >> 5] >> (gk & 31)) & 1u;
+    #pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        // this warp's columns: cb .. cb+31 = keys k0 + cb ..
+                        const int cb = 64 * hf + 32 * grp;
+                        uint32_t s[32], dp[32];
+                        tmem_ld32_nowait(tA + cb, s);
+                        tmem_ld32_nowait(tA + 128 + cb, dp);
+                        tmem_wait_ld32(s);
+                        tmem_wait_ld32(dp);
+                        if (need_mask) {
+                            const int kh = k0 + cb;
+                            const int nvalid = min(32, a.Sk - kh);
+                            if (arith) {
+                                // key positions kmin + cb + c: column c visible iff c <= qpos - kmin - cb
+                                const long long dhi = static_cast<long long>(qpos) - kmm.x - cb;
+                                const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
+    #pragma unroll
+                                for (int c = 0; c < 32; ++c)
+                                    if (c > lim) s[c] = kNegInfBits;
+                            } else {
+    #pragma unroll
+                                for (int c0 = 0; c0 < 32; c0 += 16) {
+    #pragma unroll
+                                    for (int c = c0; c < c0 + 16; ++c) {
+                                        const int kp = (c < nvalid) ? __ldg(kpos_o + kh + c) : INT_MAX;
+                                        if (kp > qpos) s[c] = kNegInfBits;
+                                    }
+                                    asm volatile("" ::: "memory");
                                 }
-                                asm volatile("" ::: "memory");
                             }
                         }
+                        // dS = 2^(s sl2 + nl2) (dP + nd)
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            float x0, x1, g0, g1;
+                            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nl2x2), x0, x1);
+                            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                            f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), ndx2), 0ull), g0, g1);
+                            pk[c >> 1] = pack_bf16x2(g0, g1);
+                        }
+                        // packed over the first 16 of this warp's own 32 columns (see dK / dV)
+                        tmem_st16_nowait(tA + cb, pk);
+                        release_half(hf == 0 ? p_half : p_full, lane);
                     }
-                    // dS = 2^(s sl2 + nl2) (dP + nd)
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        float x0, x1, g0, g1;
-                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nl2x2), x0, x1);
-                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                        f2_unpack(f2_fma(f2_packf(p0, p1), f2_add(f2_pack(dp[c], dp[c + 1]), ndx2), 0ull), g0, g1);
-                        pk[c >> 1] = pack_bf16x2(g0, g1);
-                    }
-                    // packed over the first 16 of this warp's own 32 columns (see dK / dV)
-                    tmem_st16_nowait(tA + cb, pk);
-                    release_half(hf == 0 ? p_half : p_full, lane);
                 }
+                if (!ok) break;
+                if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                store_acc_row<D / 2>(tA + 256 + grp * (D / 2), dq_row, a.scale, row_valid, a.accumulate != 0);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_empty);
+                ++it;
             }
-            if (!ok) break;
-            if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-            tc_fence_after();
-            store_acc_row<D / 2>(tA + 256 + grp * (D / 2), dq_row, a.scale, row_valid, a.accumulate != 0);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_empty);
-            ++it;
         }
     }
 
@@ -1000,7 +1024,6 @@ BwdArgs make_args(const BwdProblem &p, int nq, int nk, int heads_per_item) {
     a.scale = p.scale;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
     a.timeout_ns = 2000000000ull;
-    a.div_bh = make_fastdiv(static_cast<uint32_t>(a.B * heads_per_item));
     a.div_h = make_fastdiv(static_cast<uint32_t>(heads_per_item));
     return a;
 }
@@ -1017,8 +1040,10 @@ cp_status launch_dkdv_typed(const BwdProblem &p, cudaStream_t stream) {
         return CP_ERR_CUDA;
     const int nq = static_cast<int>((p.Sq + 127) / 128), nk = static_cast<int>((p.Sk + 127) / 128);
     BwdArgs a = make_args<D>(p, nq, nk, static_cast<int>(p.Nkv));
-    a.div_nt = make_fastdiv(static_cast<uint32_t>(nk));
-    const long long n_items = static_cast<long long>(p.C) * nk * p.B * p.Nkv;
+    // key tiles u and nk-1-u in one work item when that still leaves 8 rounds
+    a.pair = pair_units(nk, p.C, p.B * p.Nkv, sm_count()) ? 1 : 0;
+    a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(nk, a.pair != 0)));
+    const long long n_items = static_cast<long long>(p.C) * super_count(nk, a.pair != 0) * p.B * p.Nkv;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -1040,8 +1065,10 @@ cp_status launch_dq_typed(const BwdProblem &p, cudaStream_t stream) {
         return CP_ERR_CUDA;
     const int nq = static_cast<int>((p.Sq + 127) / 128), nk = static_cast<int>((p.Sk + 127) / 128);
     BwdArgs a = make_args<D>(p, nq, nk, static_cast<int>(p.N));
-    a.div_nt = make_fastdiv(static_cast<uint32_t>(nq));
-    const long long n_items = static_cast<long long>(p.C) * nq * p.B * p.N;
+    // query tiles u and nq-1-u in one work item when that still leaves 8 rounds
+    a.pair = pair_units(nq, p.C, p.B * p.N, sm_count()) ? 1 : 0;
+    a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(nq, a.pair != 0)));
+    const long long n_items = static_cast<long long>(p.C) * super_count(nq, a.pair != 0) * p.B * p.N;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
