@@ -223,7 +223,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, prefetch=None),
+        "config": workload_config(w, prefetch=None, device_timing=False),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "%d random query rows x all %d heads per step of the %s workload"
                                    % (rows_per_step, w.N, w.name)},
@@ -233,14 +233,78 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, prefetch):
+L2_BYTES = 129e6
+FLUSH_BYTES = 256 << 20
+
+
+def input_bytes(w):
+    return w.B * w.S * (w.N + 2 * w.Nkv) * w.D * 2
+
+
+def needs_l2_flush(w):
+    """q, k, v together within 1.5x of L2: flush L2 between timed steps."""
+    return input_bytes(w) < 1.5 * L2_BYTES
+
+
+def workload_config(w, prefetch, device_timing=True):
     cfg = {"workload": "%s: B=%d S=%d N=%d Nkv=%d D=%d, C=%d %s ring%s" % (
         w.name, w.B, w.S, w.N, w.Nkv, w.D, w.C, w.layout, ", RoPE" if w.rope else ""),
-        "B": w.B, "S": w.S, "N": w.N, "Nkv": w.Nkv, "D": w.D, "C": w.C, "layout": w.layout,
-        "l2": "inputs larger than L2 (q, k, v %.0f MB each)" % (w.B * w.S * w.N * w.D * 2 / 1e6)}
+        "B": w.B, "S": w.S, "N": w.N, "Nkv": w.Nkv, "D": w.D, "C": w.C, "layout": w.layout}
+    if device_timing:
+        cfg["l2"] = ("L2 flushed between timed steps (%d MB write, outside each step's events); q, k, v %.1f MB in all"
+                     % (FLUSH_BYTES >> 20, input_bytes(w) / 1e6) if needs_l2_flush(w)
+                     else "inputs larger than L2 (q, k, v %.0f MB each)" % (w.B * w.S * w.N * w.D * 2 / 1e6))
     if prefetch is not None:
         cfg["prefetch"] = prefetch
     return cfg
+
+
+def graph_replay_times(args, torch, F, step, inputs, flush_buf, parts):
+    """Median time of >= 20 replays of one CUDA graph of `step(*inputs, None)` and
+    of each permutation in `parts` (name -> (callable, algorithmic bytes)), each
+    beside the same work launched eagerly; L2 flushed between runs when
+    flush_buf is given (outside the events)."""
+    reps = max(20, args.steps)
+
+    def median_ms(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            if flush_buf is not None:
+                flush_buf.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def capture(fn):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    eager_step = lambda: step(*inputs, None)
+    g = capture(eager_step)
+    out = {"reps": reps, "statistic": "median", "step_ms_graph": median_ms(g.replay),
+           "step_ms_eager": median_ms(eager_step)}
+    for name, (fn, nbytes) in parts.items():
+        gp = capture(fn)
+        tg, te = median_ms(gp.replay), median_ms(fn)
+        out[name + "_gbs_graph"] = nbytes / (tg * 1e-3) / 1e9
+        out[name + "_gbs_eager"] = nbytes / (te * 1e-3) / 1e9
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -320,6 +384,9 @@ def run_ours(args, w):
     evsets = [{"ring": mk_events(n_ring_ev), "shard": mk_events(2), "unshard": mk_events(2),
                "relayout": mk_events(2)} for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = needs_l2_flush(w)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -328,12 +395,16 @@ def run_ours(args, w):
     wall0 = time.perf_counter()
     t_start.record()
     for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()  # evicts the previous step's data from L2 (outside the step's events)
+        step_ev[i][0].record()
         step(qd, kd, vd, evsets[i])
+        step_ev[i][1].record()
     t_end.record()
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = (sum(a.elapsed_time(b) for a, b in step_ev) if flush else t_start.elapsed_time(t_end))
     clk = clocks.stop()
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
@@ -433,6 +504,18 @@ def run_ours(args, w):
     h2d = qkv_bytes
     d2h = B * S * N * D * 4 + C * B * N * s * 4
 
+    # ---- CUDA-graph replay: the whole step and each permutation alone, each
+    # beside the same work launched eagerly (median of the replays)
+    graph_info = None
+    if args.graph:
+        graph_info = graph_replay_times(args, torch, F, step, (qd, kd, vd), flush_buf, dict(
+            shard=(lambda: F.cp_zigzag_shard(qd, C, lay, out=qs), 2 * B * S * N * D * 2),
+            unshard=(lambda: F.cp_zigzag_unshard(o_sh, lay, out=o_full), 2 * B * S * N * D * 4),
+            relayout=(lambda: F.cp_ulysses_relayout(qs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=qh),
+                      2 * B * S * N * D * 2)))
+        graph_info["step_value_graph_tflops"] = flops_step / (graph_info["step_ms_graph"] * 1e-3) / 1e12
+        graph_info["step_value_eager_tflops"] = flops_step / (graph_info["step_ms_eager"] * 1e-3) / 1e12
+
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -461,6 +544,8 @@ def run_ours(args, w):
         },
         "wall_s_timed": wall,
     }
+    if graph_info is not None:
+        line["graph"] = graph_info
     if rank == 0 and not args.no_cpu_baseline:
         qkv64 = prepare_oracle_inputs(w, q, k, v)
         line["cpu_baseline"] = cpu_baseline(w, qkv64, target_s=args.cpu_seconds)
@@ -758,6 +843,8 @@ def main():
     ap.add_argument("--fused-merge", dest="fused_merge", action="store_true",
                     help="merge each ring step in the attention epilogue instead of with the standalone merge kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time CUDA-graph replays of the step and of each permutation (with the eager times)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="run the contiguous-vs-zigzag sweep instead")
     ap.add_argument("--strategies", default="",
