@@ -56,10 +56,11 @@ struct CfgT {
     static constexpr int kOffTab = kOffV + kTStages * kKBytes;
     static constexpr int kOffOrder = kOffTab + kMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kMaxPairs * 4;
+    static constexpr int kOffSeg = kOffCost + kMaxPairs * 4;
     // q_full, q_empty, k_full[S], k_empty[S] (K and V of a stage travel together),
     // s_full[2], p_full[2], pv_done, o_full, o_empty, drain
     static constexpr int kNumBars = 2 + 2 * kTStages + 9;
-    static constexpr int kOffBar = kOffCost + kMaxPairs * 4;
+    static constexpr int kOffBar = kOffSeg + (kMaxPairs + 2) * 4;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMiscBytes = 16 + kMaxC * 4 + kMaxTables / 8;
     static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;
@@ -75,7 +76,8 @@ struct TArgs {
     int kv_shift, kpos_shift, kv_shared, kpr;
     float scale_log2;
     unsigned long long timeout_ns;
-    FastDiv div_bn, div_nq, div_n;
+    int pair;  // a super-block holds query tiles u and nqt-1-u (else u alone)
+    FastDiv div_nsp, div_n;
 };
 
 // kind::tf32 instruction descriptor: D fp32 (bits 4-5 = 1), A and B tf32
@@ -139,6 +141,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
     int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
     int *cost = reinterpret_cast<int *>(smem + K::kOffCost);
+    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
     int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
@@ -207,29 +210,23 @@ __global__ void __launch_bounds__(kTThreads, 1)
         cost[p] = c;
     }
     __syncthreads();
-    for (int p = tid; p < np; p += kTThreads) {
-        const int c = cost[p];
-        int rank = 0;
-        for (int q = 0; q < np; ++q) rank += (cost[q] > c) || (cost[q] == c && q < p);
-        order[rank] = p;
-    }
+    build_segments<kTThreads>(cost, a.C, a.nqt, a.pair != 0, order, seg_first);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int n_items = np * a.B * a.N;
+    const int n_items = a.C * super_count(a.nqt, a.pair != 0) * a.B * a.N;
     const int n_rounds = (n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
     const int hq_per_kv = a.N / a.Nkv;
     uint8_t *sQ = smem + K::kOffQ, *sK = smem + K::kOffK, *sV = smem + K::kOffV;  // sV holds V^T tiles
-    auto decode = [&](int idx, int &r, int &qt, int &b, int &h, int &owner, int &kvr, int &pr) {
-        const uint32_t pi = fdiv(static_cast<uint32_t>(idx), a.div_bn);
-        const uint32_t bh = static_cast<uint32_t>(idx) - pi * a.div_bn.d;
-        pr = order[pi];
-        r = static_cast<int>(fdiv(static_cast<uint32_t>(pr), a.div_nq));
-        qt = pr - r * a.nqt;
-        b = static_cast<int>(fdiv(bh, a.div_n));
-        h = static_cast<int>(bh) - b * a.N;
+    // query tile `unit` of super item x -> (rank, query tile, b, head, ...)
+    auto decode = [&](const SuperItem &x, int unit, int &r, int &qt, int &b, int &h, int &owner, int &kvr, int &pr) {
+        r = x.r;
+        qt = unit;
+        pr = r * a.nqt + qt;
+        b = static_cast<int>(fdiv(static_cast<uint32_t>(x.bh), a.div_n));
+        h = x.bh - b * a.N;
         owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
         kvr = a.kv_shared ? 0 : (r + a.kv_shift) % a.C;
     };
@@ -248,35 +245,41 @@ __global__ void __launch_bounds__(kTThreads, 1)
             uint32_t it = 0, t = 0, k_issued = 0, k_par = 0;
             int q_par = -1;
             bool ok = true;
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                int r, qt, b, h, owner, kvr, pr;
-                decode(idx, r, qt, b, h, owner, kvr, pr);
-                if (cost[pr] == 0) continue;
-                if (!mbar_wait(q_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                mbar_arrive_expect_tx(q_full, K::kQBytes);
-                q_par = static_cast<int>(it & 1u);
-                for (int at = 0; at < K::kAtoms; ++at)
-                    tma_load_4d(sQ + at * K::kQAtom, &tmQ, q_full, 32 * at, h, qt * 128, r * a.B + b);
-                ++it;
-                const int2 *kt_o = ktab + owner * a.nkt;
-                const int qmax = qtab[r * a.nqt + qt].y;
-                const bool srt = sorted_flag[owner] != 0;
-                const int hk = h / hq_per_kv, kvrow = kvr * a.B + b;
-                for (int kt = next_kt(0, kt_o, qmax, srt); kt < a.nkt; kt = next_kt(kt + 1, kt_o, qmax, srt)) {
-                    const uint32_t st = t % kTStages, ph = (t / kTStages) & 1u;
-                    if (!mbar_wait(k_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    mbar_arrive_expect_tx(k_full + st, 2 * K::kKBytes);
+                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int unit = super_part(sup.u, part, a.nqt, a.pair != 0);
+                    if (unit < 0) continue;
+                    int r, qt, b, h, owner, kvr, pr;
+                    decode(sup, unit, r, qt, b, h, owner, kvr, pr);
+                    if (cost[pr] == 0) continue;
+                    if (!mbar_wait(q_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    mbar_arrive_expect_tx(q_full, K::kQBytes);
+                    q_par = static_cast<int>(it & 1u);
                     for (int at = 0; at < K::kAtoms; ++at)
-                        tma_load_4d(sK + st * K::kKBytes + at * K::kKAtom, &tmK, k_full + st, 32 * at, hk, kt * 64, kvrow);
-                    // V^T [D rows][keys kt*64 ..]: two atoms of 32 keys
-                    for (int at = 0; at < 2; ++at)
-                        tma_load_4d(sV + st * K::kKBytes + at * K::kVtAtom, &tmVt, k_full + st, kt * 64 + 32 * at, 0, hk,
-                                    kvrow);
-                    k_issued |= 1u << st;
-                    k_par = (k_par & ~(1u << st)) | (ph << st);
-                    ++t;
+                        tma_load_4d(sQ + at * K::kQAtom, &tmQ, q_full, 32 * at, h, qt * 128, r * a.B + b);
+                    ++it;
+                    const int2 *kt_o = ktab + owner * a.nkt;
+                    const int qmax = qtab[r * a.nqt + qt].y;
+                    const bool srt = sorted_flag[owner] != 0;
+                    const int hk = h / hq_per_kv, kvrow = kvr * a.B + b;
+                    for (int kt = next_kt(0, kt_o, qmax, srt); kt < a.nkt; kt = next_kt(kt + 1, kt_o, qmax, srt)) {
+                        const uint32_t st = t % kTStages, ph = (t / kTStages) & 1u;
+                        if (!mbar_wait(k_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        mbar_arrive_expect_tx(k_full + st, 2 * K::kKBytes);
+                        for (int at = 0; at < K::kAtoms; ++at)
+                            tma_load_4d(sK + st * K::kKBytes + at * K::kKAtom, &tmK, k_full + st, 32 * at, hk, kt * 64, kvrow);
+                        // V^T [D rows][keys kt*64 ..]: two atoms of 32 keys
+                        for (int at = 0; at < 2; ++at)
+                            tma_load_4d(sV + st * K::kKBytes + at * K::kVtAtom, &tmVt, k_full + st, kt * 64 + 32 * at, 0, hk,
+                                        kvrow);
+                        k_issued |= 1u << st;
+                        k_par = (k_par & ~(1u << st)) | (ph << st);
+                        ++t;
+                    }
                 }
             }
             if (!ok) {
@@ -306,49 +309,55 @@ __global__ void __launch_bounds__(kTThreads, 1)
                                  dk + st * kKU + (kk >> 2) * (K::kKAtom >> 4) + (kk & 3) * 2, kIdS, kk > 0 ? 1u : 0u);
                 umma_commit(s_full + b);
             };
+            int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
                 if (idx < 0) continue;
-                int r, qt, b, h, owner, kvr, pr;
-                decode(idx, r, qt, b, h, owner, kvr, pr);
-                const int n = cost[pr];
-                if (n == 0) continue;
-                if (!mbar_wait(q_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
-                // the first two tiles' scores, then per tile: P V, and the scores
-                // of the tile after next into the buffer P V has just read
-                for (int j = 0; j < 2 && j < n; ++j) {
-                    const uint32_t st = (t + j) % kTStages, ph = ((t + j) / kTStages) & 1u;
-                    if (!mbar_wait(k_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = 0; part < 2 && ok; ++part) {
+                    const int unit = super_part(sup.u, part, a.nqt, a.pair != 0);
+                    if (unit < 0) continue;
+                    int r, qt, b, h, owner, kvr, pr;
+                    decode(sup, unit, r, qt, b, h, owner, kvr, pr);
+                    const int n = cost[pr];
+                    if (n == 0) continue;
+                    if (!mbar_wait(q_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                     tc_fence_after();
-                    issue_s((t + j) & 1u, st);
-                }
-                if (!ok) break;
-                if (n <= 2) umma_commit(q_empty);
-                for (int j = 0; j < n; ++j, ++t) {
-                    const uint32_t bb = t & 1u, st = t % kTStages;
-                    if (!mbar_wait(p_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-                    // O (+)= P V: 64 keys in 8 k-steps of 8 (P columns +8; V^T k-step kk
-                    // at (kk / 4) atoms + (kk % 4) * 32 bytes)
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_tf32_ts(tmem + 128, tmem + 64 * bb + 8 * kk,
-                                     dv + st * kKU + (kk >> 2) * (K::kVtAtom >> 4) + (kk & 3) * 2, kIdO,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(pv_done);
-                    umma_commit(k_empty + st);
-                    if (j + 2 < n) {
-                        const uint32_t st2 = (t + 2) % kTStages, ph2 = ((t + 2) / kTStages) & 1u;
-                        if (!mbar_wait(k_full + st2, ph2, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    // the first two tiles' scores, then per tile: P V, and the scores
+                    // of the tile after next into the buffer P V has just read
+                    for (int j = 0; j < 2 && j < n; ++j) {
+                        const uint32_t st = (t + j) % kTStages, ph = ((t + j) / kTStages) & 1u;
+                        if (!mbar_wait(k_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
                         tc_fence_after();
-                        issue_s(bb, st2);
-                        if (j + 3 == n) umma_commit(q_empty);
+                        issue_s((t + j) & 1u, st);
                     }
+                    if (!ok) break;
+                    if (n <= 2) umma_commit(q_empty);
+                    for (int j = 0; j < n; ++j, ++t) {
+                        const uint32_t bb = t & 1u, st = t % kTStages;
+                        if (!mbar_wait(p_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+                        // O (+)= P V: 64 keys in 8 k-steps of 8 (P columns +8; V^T k-step kk
+                        // at (kk / 4) atoms + (kk % 4) * 32 bytes)
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_tf32_ts(tmem + 128, tmem + 64 * bb + 8 * kk,
+                                         dv + st * kKU + (kk >> 2) * (K::kVtAtom >> 4) + (kk & 3) * 2, kIdO,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(pv_done);
+                        umma_commit(k_empty + st);
+                        if (j + 2 < n) {
+                            const uint32_t st2 = (t + 2) % kTStages, ph2 = ((t + 2) / kTStages) & 1u;
+                            if (!mbar_wait(k_full + st2, ph2, abort_flag, a.timeout_ns)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_s(bb, st2);
+                            if (j + 3 == n) umma_commit(q_empty);
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(o_full);
+                    ++it;
                 }
-                if (!ok) break;
-                umma_commit(o_full);
-                ++it;
             }
             umma_commit(drain);
             volatile int no_abort = 0;
@@ -363,131 +372,137 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const float sl2 = a.scale_log2;
         uint32_t it = 0, t = 0;
         bool ok = true;
+        int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
             const int idx = item_of_round(rk, n_items);
             if (idx < 0) continue;
-            int r, qt, b, h, owner, kvr, pr;
-            decode(idx, r, qt, b, h, owner, kvr, pr);
-            const int row = qt * 128 + row_in;
-            const bool row_valid = row < a.Sq;
-            const int qpos = row_valid ? __ldg(a.q_pos + r * a.q_pos_stride + row) : INT_MIN;
-            const long long orow = static_cast<long long>(r * a.B + b) * a.Sq + row;
-            float *o_row = a.o + (orow * a.N + h) * D;
-            float *lse_out = a.lse + (static_cast<long long>(r * a.B + b) * a.N + h) * a.Sq + row;
-            if (cost[pr] == 0) {
-                if (row_valid) {
-                    for (int c = 0; c < D; c += 8) st_global_v8(o_row + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
-                    *lse_out = -INFINITY;
+            const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+            for (int part = 0; part < 2 && ok; ++part) {
+                const int unit = super_part(sup.u, part, a.nqt, a.pair != 0);
+                if (unit < 0) continue;
+                int r, qt, b, h, owner, kvr, pr;
+                decode(sup, unit, r, qt, b, h, owner, kvr, pr);
+                const int row = qt * 128 + row_in;
+                const bool row_valid = row < a.Sq;
+                const int qpos = row_valid ? __ldg(a.q_pos + r * a.q_pos_stride + row) : INT_MIN;
+                const long long orow = static_cast<long long>(r * a.B + b) * a.Sq + row;
+                float *o_row = a.o + (orow * a.N + h) * D;
+                float *lse_out = a.lse + (static_cast<long long>(r * a.B + b) * a.N + h) * a.Sq + row;
+                if (cost[pr] == 0) {
+                    if (row_valid) {
+                        for (int c = 0; c < D; c += 8) st_global_v8(o_row + c, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f);
+                        *lse_out = -INFINITY;
+                    }
+                    continue;
                 }
-                continue;
-            }
-            const int2 *kt_o = ktab + owner * a.nkt;
-            const int2 qmm = qtab[r * a.nqt + qt];
-            const bool srt = sorted_flag[owner] != 0;
-            const int32_t *kpos_o = a.k_pos + owner * a.k_pos_stride;
-            float m_run = -INFINITY, l_run = 0.f;
-            bool first_tile = true;
-            for (int kt = next_kt(0, kt_o, qmm.y, srt); kt < a.nkt; kt = next_kt(kt + 1, kt_o, qmm.y, srt), ++t) {
-                const uint32_t bb = t & 1u;
-                if (!mbar_wait_warp(s_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t s[64];
-                tmem_ld64(tA + 64 * bb, s);
-                const int2 kmm = kt_o[kt];
-                const int k0 = kt * 64, nvalid = min(64, a.Sk - k0);
-                if (kmm.y > qmm.x || nvalid < 64) {
-                    const int gk = owner * a.nkt + kt;
-                    if ((arith_bits[gk >> 5] >> (gk & 31)) & 1u) {
-                        const long long dhi = static_cast<long long>(qpos) - kmm.x;
-                        const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c > lim) s[c] = kTNegInf;
-                    } else {
-#pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
-#pragma unroll
-                            for (int c = c0; c < c0 + 16; ++c) {
-                                const int kp = (c < nvalid) ? __ldg(kpos_o + k0 + c) : INT_MAX;
-                                if (kp > qpos) s[c] = kTNegInf;
+                const int2 *kt_o = ktab + owner * a.nkt;
+                const int2 qmm = qtab[r * a.nqt + qt];
+                const bool srt = sorted_flag[owner] != 0;
+                const int32_t *kpos_o = a.k_pos + owner * a.k_pos_stride;
+                float m_run = -INFINITY, l_run = 0.f;
+                bool first_tile = true;
+                for (int kt = next_kt(0, kt_o, qmm.y, srt); kt < a.nkt; kt = next_kt(kt + 1, kt_o, qmm.y, srt), ++t) {
+                    const uint32_t bb = t & 1u;
+                    if (!mbar_wait_warp(s_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t s[64];
+                    tmem_ld64(tA + 64 * bb, s);
+                    const int2 kmm = kt_o[kt];
+                    const int k0 = kt * 64, nvalid = min(64, a.Sk - k0);
+                    if (kmm.y > qmm.x || nvalid < 64) {
+                        const int gk = owner * a.nkt + kt;
+                        if ((arith_bits[gk >> 5] >> (gk & 31)) & 1u) {
+                            const long long dhi = static_cast<long long>(qpos) - kmm.x;
+                            const int lim = dhi < 0 ? -1 : static_cast<int>(min(dhi, static_cast<long long>(nvalid - 1)));
+    #pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                if (c > lim) s[c] = kTNegInf;
+                        } else {
+    #pragma unroll
+                            for (int c0 = 0; c0 < 64; c0 += 16) {
+    #pragma unroll
+                                for (int c = c0; c < c0 + 16; ++c) {
+                                    const int kp = (c < nvalid) ? __ldg(kpos_o + k0 + c) : INT_MAX;
+                                    if (kp > qpos) s[c] = kTNegInf;
+                                }
+                                asm volatile("" ::: "memory");
                             }
-                            asm volatile("" ::: "memory");
                         }
                     }
+                    // lazy integer max (log2 domain): set on the row's first visible tile,
+                    // moved only when a score exceeds it by more than 57 (64 keys x 2^57
+                    // keeps a tile's P sum below 2^64)
+                    float mx = -INFINITY;
+    #pragma unroll
+                    for (int c = 0; c < 64; c += 2) mx = fmax3(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+                    const float m_tile = mx * sl2;
+                    float factor = 1.f;
+                    bool rescale = false;
+                    if (m_run == -INFINITY) {
+                        if (m_tile > -INFINITY) m_run = ceilf(m_tile);
+                    } else if (!(m_tile - m_run <= 57.f)) {
+                        const float m_new = ceilf(m_tile);
+                        const float dk = m_run - m_new;
+                        factor = (dk >= -126.f) ? __int_as_float((127 + static_cast<int>(dk)) << 23) : 0.f;
+                        rescale = true;
+                        l_run *= factor;
+                        m_run = m_new;
+                    }
+                    const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                    float sum = 0.f;
+    #pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const float p = fast_exp2(fmaf(__uint_as_float(s[c]), sl2, neg_m));
+                        sum += p;
+                        s[c] = round_tf32(p);
+                    }
+                    l_run += sum;
+                    // P over S (fp32, the A operand of P V)
+                    tmem_st32_nowait(tA + 64 * bb, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                    tmem_st32_nowait(tA + 64 * bb + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                    tmem_wait_st();
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        // O must be quiescent: the previous tile's P V has completed
+                        if (!first_tile && !mbar_wait_warp(pv_done, (t - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        tc_fence_after();
+    #pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t ov[32];
+                            tmem_ld32(tA + 128 + c0, ov);
+    #pragma unroll
+                            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * factor);
+                            tmem_st32(tA + 128 + c0, ov);
+                        }
+                    }
+                    first_tile = false;
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full + bb);
                 }
-                // lazy integer max (log2 domain): set on the row's first visible tile,
-                // moved only when a score exceeds it by more than 57 (64 keys x 2^57
-                // keeps a tile's P sum below 2^64)
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 64; c += 2) mx = fmax3(mx, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-                const float m_tile = mx * sl2;
-                float factor = 1.f;
-                bool rescale = false;
-                if (m_run == -INFINITY) {
-                    if (m_tile > -INFINITY) m_run = ceilf(m_tile);
-                } else if (!(m_tile - m_run <= 57.f)) {
-                    const float m_new = ceilf(m_tile);
-                    const float dk = m_run - m_new;
-                    factor = (dk >= -126.f) ? __int_as_float((127 + static_cast<int>(dk)) << 23) : 0.f;
-                    rescale = true;
-                    l_run *= factor;
-                    m_run = m_new;
-                }
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                float sum = 0.f;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float p = fast_exp2(fmaf(__uint_as_float(s[c]), sl2, neg_m));
-                    sum += p;
-                    s[c] = round_tf32(p);
-                }
-                l_run += sum;
-                // P over S (fp32, the A operand of P V)
-                tmem_st32_nowait(tA + 64 * bb, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                tmem_st32_nowait(tA + 64 * bb + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-                tmem_wait_st();
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O must be quiescent: the previous tile's P V has completed
-                    if (!first_tile && !mbar_wait_warp(pv_done, (t - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t ov[32];
-                        tmem_ld32(tA + 128 + c0, ov);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * factor);
-                        tmem_st32(tA + 128 + c0, ov);
+                if (!ok) break;
+                if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                tc_fence_after();
+                const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    #pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tA + 128 + c0, ov);
+                    if (row_valid) {
+    #pragma unroll
+                        for (int c = 0; c < 32; c += 8)
+                            st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l,
+                                         __uint_as_float(ov[c + 2]) * inv_l, __uint_as_float(ov[c + 3]) * inv_l,
+                                         __uint_as_float(ov[c + 4]) * inv_l, __uint_as_float(ov[c + 5]) * inv_l,
+                                         __uint_as_float(ov[c + 6]) * inv_l, __uint_as_float(ov[c + 7]) * inv_l);
                     }
                 }
-                first_tile = false;
+                if (row_valid)
+                    *lse_out = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + bb);
+                if (lane == 0) mbar_arrive(o_empty);
+                ++it;
             }
-            if (!ok) break;
-            if (!mbar_wait_warp(o_full, it & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-            tc_fence_after();
-            const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32(tA + 128 + c0, ov);
-                if (row_valid) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 8)
-                        st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l,
-                                     __uint_as_float(ov[c + 2]) * inv_l, __uint_as_float(ov[c + 3]) * inv_l,
-                                     __uint_as_float(ov[c + 4]) * inv_l, __uint_as_float(ov[c + 5]) * inv_l,
-                                     __uint_as_float(ov[c + 6]) * inv_l, __uint_as_float(ov[c + 7]) * inv_l);
-                }
-            }
-            if (row_valid)
-                *lse_out = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_empty);
-            ++it;
         }
     }
 
@@ -551,10 +566,11 @@ cp_status launch_tf32_typed(const AttnProblem &p, const float *vt, int64_t sk_pa
     a.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
     a.timeout_ns = 2000000000ull;
-    a.div_bn = make_fastdiv(static_cast<uint32_t>(a.B * a.N));
-    a.div_nq = make_fastdiv(static_cast<uint32_t>(a.nqt));
+    // query tiles u and nqt-1-u in one work item when that still leaves 8 rounds
+    a.pair = pair_units(a.nqt, p.C, p.B * p.N, sm_count()) ? 1 : 0;
+    a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(a.nqt, a.pair != 0)));
     a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
-    const long long n_items = static_cast<long long>(p.C) * a.nqt * p.B * p.N;
+    const long long n_items = static_cast<long long>(p.C) * super_count(a.nqt, a.pair != 0) * p.B * p.N;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {

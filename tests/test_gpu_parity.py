@@ -407,6 +407,31 @@ def test_attn_partial_f32_vs_oracle(cuda_dev, name):
     assert F.cp_device_status() == 0
 
 
+def test_attn_partial_f32_paired_tiles_gqa_ragged(cuda_dev):
+    """tf32 path on a launch large enough for paired 128-row query tiles (23
+    tiles: the middle one unpaired), 13 query heads per K/V head, ragged Sq / Sk,
+    causal positions; sampled rows of every tile and head against the oracle."""
+    B, Sq, Sk, N, Nkv, D = 2, 2900, 3000, 104, 8, 128
+    nqt = (Sq + 127) // 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert nqt % 2 == 1 and ((nqt + 1) // 2) * B * N >= 8 * sms
+    g = torch.Generator().manual_seed(43)
+    q = torch.randn(B, Sq, N, D, generator=g)
+    k = torch.randn(B, Sk, Nkv, D, generator=g)
+    v = torch.randn(B, Sk, Nkv, D, generator=g)
+    qp = np.arange(Sk - Sq, Sk, dtype=np.int32)
+    kp = np.arange(Sk, dtype=np.int32)
+    o, lse = F.cp_attn_partial_f32(q.to(cuda_dev), k.to(cuda_dev), v.to(cuda_dev), torch.as_tensor(qp).to(cuda_dev),
+                                   torch.as_tensor(kp).to(cuda_dev))
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(0, Sq, 23), np.arange(Sq - 3, Sq), [127, 128, 1407, 1408, 1535, 1536]]))
+    o_ref, l_ref = O.attn_rows(f64(q), f64(k), f64(v), qp, kp, rows, nthreads=NTH)
+    r_idx = torch.as_tensor(rows, device=cuda_dev)
+    assert np.max(np.abs(f64(o[:, r_idx]) - o_ref)) <= TF32_ATOL
+    assert np.max(np.abs(f64(lse[:, :, r_idx]) - l_ref)) <= TF32_ATOL
+    assert F.cp_device_status() == 0
+
+
 def test_attn_partial_f32_tiny_workload(cuda_dev):
     """The tiny workload's fp32 draws (no bf16 rounding) through the tf32 path,
     against fp64 of the same fp32 values."""
