@@ -760,19 +760,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wt = expf(lse_t - lse_new) * inv_l;
                     }
                 }
+                bool o_released = false;
                 if (!a.merge_into) {
+                    // all of O from TMEM under one wait; O is handed back before the stores
+                    uint32_t ov[D / 32][32];
     #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + c0, ov);
-                        if (write) {
+                    for (int q = 0; q < D / 32; ++q) tmem_ld32_nowait(tO + 32 * q, ov[q]);
+    #pragma unroll
+                    for (int q = 0; q < D / 32; ++q) tmem_wait_ld32(ov[q]);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.o_empty + wg);
+                    o_released = true;
+                    if (write) {
+    #pragma unroll
+                        for (int q = 0; q < D / 32; ++q)
     #pragma unroll
                             for (int c = 0; c < 32; c += 8)
-                                st_global_v8(o_row + c0 + c, __uint_as_float(ov[c]) * wt, __uint_as_float(ov[c + 1]) * wt,
-                                             __uint_as_float(ov[c + 2]) * wt, __uint_as_float(ov[c + 3]) * wt,
-                                             __uint_as_float(ov[c + 4]) * wt, __uint_as_float(ov[c + 5]) * wt,
-                                             __uint_as_float(ov[c + 6]) * wt, __uint_as_float(ov[c + 7]) * wt);
-                        }
+                                st_global_v8(o_row + 32 * q + c, __uint_as_float(ov[q][c]) * wt,
+                                             __uint_as_float(ov[q][c + 1]) * wt, __uint_as_float(ov[q][c + 2]) * wt,
+                                             __uint_as_float(ov[q][c + 3]) * wt, __uint_as_float(ov[q][c + 4]) * wt,
+                                             __uint_as_float(ov[q][c + 5]) * wt, __uint_as_float(ov[q][c + 6]) * wt,
+                                             __uint_as_float(ov[q][c + 7]) * wt);
                     }
                 } else {
                     const bool read_acc = write && wa != 0.f;
@@ -806,9 +815,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (write) *lse_out = lse_new;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars.o_empty + wg);
+                if (!o_released) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.o_empty + wg);
+                }
                 ++it;
             }
         }
