@@ -42,11 +42,37 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def _code_only(text):
+    """C/C++ source without comments and whitespace (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def attn_source_hash():
+    """Hash of the attention kernel's code (comments and whitespace ignored), so
+    a recorded traffic figure stays valid across comment edits only."""
     h = hashlib.sha256()
-    for f in ("attn.cu", "cp_ptx.cuh"):
-        with open(os.path.join(ROOT, "context_causal_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in ("attn.cu", "cp_ptx.cuh", "cp_sched.cuh"):
+        with open(os.path.join(ROOT, "context_causal_attention_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,7 +10,9 @@
 // o = 0, lse = -inf.
 //
 // How: one persistent CTA per SM walks a list of work items (rank, b, h,
-// 256-row query block) ordered longest-first and dealt out boustrophedon.  Inside a CTA:
+// super-block: one 256-row query block, or blocks u and nqb-1-u back to back)
+// ordered longest-first, head-major within equal cost, and dealt out
+// boustrophedon (cp_sched.cuh).  Inside a CTA:
 //   warp 0      TMA producer: Q block (two 128-row tiles) and a ring of K/V
 //               128-key stages, 128-byte swizzled;
 //   warp 1      TMEM allocator (512 columns: S0 | S1 | O0 | O1) and MMA
@@ -22,7 +24,8 @@
 //               ("Context Parallelism & Ring Attention", "Softmax is
 //               decomposable": running max, running sum, rescaled output),
 //               P written back to TMEM over S columns 64..127 as packed bf16, epilogue
-//               o = O / l and lse = (m + log2 l) ln 2.
+//               o = O / l and lse = (m + log2 l) ln 2 (O is read from TMEM and
+//               handed back to the MMA before the global stores).
 // Key tiles whose smallest position exceeds the block's largest query
 // position are skipped; tiles whose positions are all <= the tile's
 // smallest query position run unmasked; the rest are masked per element.
