@@ -25,6 +25,9 @@
 //                     keeps dQ += dS K in TMEM.
 // S and dP are formed in both (seven 128x128xD-class products per tile pair
 // instead of five), in exchange for no atomics and deterministic sums.
+// Both deal their work items like the forward (cp_sched.cuh): stationary tiles
+// u and nt-1-u of a rank back to back in one item when the launch is large
+// enough, equal-cost items head-major, longest first, boustrophedon.
 //
 // Both kernels: one persistent CTA per SM, 384 threads.
 //   warp 0      TMA producer (stationary tiles once per item, a 2-stage ring

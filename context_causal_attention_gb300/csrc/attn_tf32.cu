@@ -5,7 +5,9 @@
 // positions), same rank batching (AttnProblem), same causal tile skipping and
 // the same lazy integer running max in the log2 domain as the bf16 kernel.
 //
-// Layout of the work: one persistent CTA per SM, 256 threads.
+// Layout of the work: one persistent CTA per SM, 256 threads; work items are
+// (rank, b, h, 128-row query tile, or tiles u and nqt-1-u back to back), in the
+// shared order of cp_sched.cuh.
 //   warp 0      TMA producer: the 128-row fp32 query tile of the item, then a
 //               2-stage ring of 64-key K tiles and 64-key V^T tiles (128-byte
 //               swizzle, 32 fp32 columns per swizzle atom);
