@@ -60,3 +60,17 @@ def test_two_rank_aggregation_gloo():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(7.0, 1) == 7.0
     assert bench.job_throughput(10.0, 1, 1000.0) == pytest.approx(10.0)
+
+
+def test_code_hash_ignores_comments_only():
+    """The recorded-traffic check hashes kernel code with comments and
+    whitespace removed: a comment edit keeps the hash, a code edit changes it."""
+    import bench
+    src = 'int f(int a) {  // twice\n  /* body */ return a * 2; }\nconst char *s = "x // y";\n'
+    same = 'int f(int a) { // doubled\n  return a * 2;   /* note */ }\nconst char *s = "x // y";\n'
+    other = 'int f(int a) { return a * 3; }\nconst char *s = "x // y";\n'
+    strings = 'int f(int a) { return a * 2; }\nconst char *s = "x // z";\n'
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+    assert bench._code_only(src) != bench._code_only(strings)  # string literals are code
+    assert len(bench.attn_source_hash()) == 16
