@@ -76,14 +76,16 @@ def attn_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def recorded_traffic(workload, fused=False):
+    """Per-launch DRAM bytes of the attention kernel (the ring's launches with the
+    merge fused into the epilogue, or with the standalone merge) from the
+    committed ncu summary, if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "attn_fwd_kernel_%s.md" % workload)
     if not os.path.exists(p):
         return None
     txt = open(p).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source\s+([0-9a-f]+)\)", txt)
+    key = "traffic_bytes_per_launch_fused_merge" if fused else "traffic_bytes_per_launch"
+    m = re.search(key + r":\s*([0-9.eE+]+)\s*\(source\s+([0-9a-f]+)\)", txt)
     if not m or m.group(2) != attn_source_hash():
         return None
     return float(m.group(1))
@@ -499,7 +501,7 @@ def run_ours(args, w):
     unshard_gbs = 2 * (B * S * N * D * 4) / (unshard_ms * 1e-3) / 1e9
     relayout_gbs = 2 * qkv_bytes / (relayout_ms * 1e-3) / 1e9
     peak_tc = peaks["bf16_tflops_sustained"]
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name, fused)
 
     # ---- end to end: pinned host inputs -> device, step, result -> host
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
@@ -551,7 +553,8 @@ def run_ours(args, w):
                        if fused else "standalone merge kernel per ring step"),
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak_tc, "traffic": traffic,
-                     "kernel": "attn_fwd_kernel<%d>" % D,
+                     "kernel": "attn_fwd_kernel<%d>" % D + (" (ring steps >= 1 also merge into the accumulator in "
+                                                            "the epilogue)" if fused else ""),
                      "peak_note": "bf16_tflops_sustained of %s peaks (kernel timed inside a long step); "
                                   "frac of burst %.1f: %.3f" % (peaks["source"], peaks["bf16_tflops"],
                                                                 attn_tflops / peaks["bf16_tflops"])},
@@ -866,8 +869,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="s32k")
     ap.add_argument("--no-prefetch", dest="prefetch", action="store_false")
-    ap.add_argument("--fused-merge", dest="fused_merge", action="store_true",
-                    help="merge each ring step in the attention epilogue instead of with the standalone merge kernel")
+    ap.add_argument("--separate-merge", dest="fused_merge", action="store_false",
+                    help="merge each ring step with the standalone merge kernel instead of in the attention epilogue "
+                         "(the default fuses it: faster whole steps)")
+    ap.add_argument("--fused-merge", dest="fused_merge", action="store_true", help="the default; kept for scripts")
+    ap.set_defaults(fused_merge=True)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="also time CUDA-graph replays of the step and of each permutation (with the eager times)")
