@@ -178,6 +178,24 @@ cp_status launch_segments(SegArgs a, long long nseg, cudaStream_t stream) {
     return last_launch_status();
 }
 
+// The kernels may dereference [p, p + n): device (or managed) memory, or host
+// memory that is pinned and mapped into the device address space at the same
+// address.  Both ends of the range are checked.
+bool device_reachable(const void *p, size_t n) {
+    const char *ends[2] = {static_cast<const char *>(p), static_cast<const char *>(p) + (n ? n - 1 : 0)};
+    for (const char *e : ends) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, e) != cudaSuccess) {
+            cudaGetLastError();  // clear the sticky error of the query
+            return false;
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) continue;
+        if (at.type == cudaMemoryTypeHost && at.devicePointer == e) continue;
+        return false;
+    }
+    return true;
+}
+
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
@@ -194,6 +212,7 @@ cp_status shard_impl(const void *x, void *x_sh, int64_t B, int64_t S, int64_t N,
     if (!aligned16(x) || !aligned16(x_sh) || row_bytes % 16 != 0) return CP_ERR_ALIGNMENT;
     const size_t nbytes = static_cast<size_t>(B * S) * static_cast<size_t>(row_bytes);
     if (ranges_overlap(x, nbytes, x_sh, nbytes)) return CP_ERR_ARGUMENT;
+    if (!device_reachable(x, nbytes) || !device_reachable(x_sh, nbytes)) return CP_ERR_ARGUMENT;
     SegArgs a{};
     a.src = static_cast<const uint8_t *>(unshard ? x_sh : x);
     a.dst = static_cast<uint8_t *>(unshard ? const_cast<void *>(x) : x_sh);

@@ -51,17 +51,24 @@ def cp_version():
 
 
 def cp_zigzag_shard(x, C, layout=CP_ZIGZAG, out=None, stream=None):
-    """x [B,S,N,D] -> rank-major shards [C,B,S/C,N,D] (bit-exact permutation)."""
+    """x [B,S,N,D] -> rank-major shards [C,B,S/C,N,D] (bit-exact permutation).
+
+    x may be a pinned host tensor: the kernel then reads it across the host
+    link (copy and shard in one pass) into `out` on the current CUDA device."""
     B, S, N, D = x.shape
     if out is None:
-        out = torch.empty((C, B, S // C, N, D), dtype=x.dtype, device=x.device)
+        dev = x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty((C, B, S // C, N, D), dtype=x.dtype, device=dev)
     st = _lib.lib().cp_zigzag_shard(_ptr(x), _ptr(out), B, S, N, D, C, _dtype_code(x), layout, _stream(stream))
     _lib.check("cp_zigzag_shard", st)
     return out
 
 
 def cp_zigzag_unshard(x_sh, layout=CP_ZIGZAG, out=None, stream=None):
-    """Rank-major shards [C,B,s,N,D] -> x [B,C*s,N,D] in global order."""
+    """Rank-major shards [C,B,s,N,D] -> x [B,C*s,N,D] in global order.
+
+    `out` may be a pinned host tensor: the kernel then writes it across the
+    host link (unshard and device-to-host copy in one pass)."""
     C, B, s, N, D = x_sh.shape
     if out is None:
         out = torch.empty((B, C * s, N, D), dtype=x_sh.dtype, device=x_sh.device)

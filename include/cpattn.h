@@ -76,9 +76,15 @@ const char *cp_last_cuda_error(void);
  * owns [chunk r | chunk 2C-1-r] (layout CP_ZIGZAG; TE's "DualChunkSwap").
  * [RING] "The last remaining axis": rank r owns tokens [r*s, (r+1)*s)
  * (layout CP_CONTIGUOUS).
- *   x     : device, [B][S][N][D] of `dtype`, read only
+ *   x     : [B][S][N][D] of `dtype`, read only; device memory, or pinned host
+ *           memory mapped at the same address (cudaHostAlloc / cudaMallocHost /
+ *           cudaHostRegister under unified addressing), which the kernel then
+ *           reads across the host link (the host-to-device copy and the shard
+ *           in one pass)
  *   x_sh  : device, [C][B][S/C][N][D] of `dtype`, written (must not overlap x)
  * Requires S % (2C) == 0 (zigzag) or S % C == 0 (contiguous), C >= 1.
+ * Any other host memory (pageable, or pinned but not mapped at its host
+ * address) is refused with CP_ERR_ARGUMENT before anything is launched.
  * The result is a bit-exact permutation of x.
  */
 cp_status cp_zigzag_shard(const void *x, void *x_sh, int64_t B, int64_t S, int64_t N, int64_t D,
@@ -89,7 +95,10 @@ cp_status cp_zigzag_shard(const void *x, void *x_sh, int64_t B, int64_t S, int64
  * into global sequence order ([OCP] All-gather: the rank-order result
  * [chunk 0, chunk 7, chunk 1, chunk 6, ...] reordered to sequence order).
  *   x_sh  : device, [C][B][S/C][N][D], read only
- *   x     : device, [B][S][N][D], written (must not overlap x_sh)
+ *   x     : [B][S][N][D], written (must not overlap x_sh); device memory, or
+ *           pinned host memory mapped at the same address (the kernel then
+ *           writes across the host link: unshard and device-to-host copy in
+ *           one pass); other host memory -> CP_ERR_ARGUMENT
  */
 cp_status cp_zigzag_unshard(const void *x_sh, void *x, int64_t B, int64_t S, int64_t N, int64_t D,
                             int C, cp_dtype dtype, cp_layout layout, cudaStream_t stream);

@@ -52,6 +52,9 @@ def test_shard_validation(cplib):
     assert f(FAKE, ctypes.c_void_p(1 << 30), 1, 256, 1, 4, 2, 0, 0, None) == 5   # row of 8 bytes
     assert f(FAKE, FAKE, 1, 256, 2, 64, 2, 0, 0, None) == 10  # in/out overlap
     assert cplib.cp_zigzag_unshard(FAKE, MISALIGNED, 1, 256, 2, 64, 2, 0, 0, None) == 5
+    # well-formed, but memory the device cannot reach: refused before any launch
+    assert f(FAKE, ctypes.c_void_p(1 << 30), 1, 256, 2, 64, 2, 0, 0, None) == 10
+    assert cplib.cp_zigzag_unshard(FAKE, ctypes.c_void_p(1 << 30), 1, 256, 2, 64, 2, 0, 0, None) == 10
 
 
 def test_positions_and_relayout_validation(cplib):

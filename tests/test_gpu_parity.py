@@ -82,6 +82,26 @@ def test_shard_unshard_bit_exact(cuda_dev, B, S, N, D, C, layout, dtype):
     assert np.array_equal(bits(back), bits(x))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_shard_unshard_pinned_host_direct(cuda_dev, dtype):
+    """Shard straight from pinned host memory and unshard straight into it
+    (the kernels cross the host link themselves): bit-identical to the
+    device-to-device permutations; pageable host memory is refused."""
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(2, 1024, 4, 64, generator=g).to(dtype)
+    for layout in (F.CP_ZIGZAG, F.CP_CONTIGUOUS):
+        ref = F.cp_zigzag_shard(x.to(cuda_dev), 4, layout)
+        sh = F.cp_zigzag_shard(x.pin_memory(), 4, layout, out=torch.empty_like(ref))
+        back = torch.empty(x.shape, dtype=dtype).pin_memory()
+        F.cp_zigzag_unshard(ref, layout, out=back)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(sh), bits(ref))
+        assert np.array_equal(bits(back), bits(x))
+    with pytest.raises(RuntimeError):
+        F.cp_zigzag_shard(x, 4, out=torch.empty_like(ref))  # pageable
+    assert F.cp_device_status() == 0
+
+
 @pytest.mark.parametrize("S,C,layout", [(256, 2, 0), (4096, 4, 0), (131072, 8, 0), (96, 3, 1), (8192, 8, 1)])
 def test_positions_device_bit_exact(cuda_dev, S, C, layout):
     pos = F.cp_zigzag_positions(S, C, layout, device=cuda_dev)
