@@ -250,13 +250,20 @@ def ring_inputs(w, cuda_dev, layout):
 
 
 @pytest.mark.parametrize("wname,layout", [("tiny", "zigzag"), ("s4k", "zigzag"), ("s4k_contig", "contiguous"),
-                                          ("c8", "zigzag")])
+                                          ("c8", "zigzag"), ("c1", "zigzag"), ("c64_max", "zigzag"),
+                                          ("c64_max_contig", "contiguous"), ("ragged_gqa", "zigzag")])
 def test_ring_vs_oracle(cuda_dev, wname, layout):
     """Every ring mode (zero copy / prefetched K/V rotation x separate / fused
     merge) against the fp64 oracle ring."""
     extra = {
         "s4k_contig": SY.Workload("s4k_contig", B=1, S=1024, N=4, Nkv=4, D=64, C=4, layout="contiguous"),
         "c8": SY.Workload("c8", B=1, S=2048, N=2, Nkv=2, D=128, C=8),
+        # degenerate ring (one rank: the monolithic call) and the most virtual ranks one launch takes
+        "c1": SY.Workload("c1", B=1, S=640, N=2, Nkv=2, D=64, C=1),
+        "c64_max": SY.Workload("c64", B=1, S=8192, N=2, Nkv=1, D=64, C=64),
+        "c64_max_contig": SY.Workload("c64c", B=1, S=8192, N=2, Nkv=2, D=128, C=64, layout="contiguous"),
+        # 450 rows per rank (a ragged last tile in every shard), two query heads per K/V head
+        "ragged_gqa": SY.Workload("rg", B=2, S=1800, N=4, Nkv=2, D=128, C=4),
     }
     w = extra.get(wname) or SY.WORKLOADS[wname]
     (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, layout)
