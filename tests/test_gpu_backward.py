@@ -127,6 +127,10 @@ RING = {
     "contig_c4": (SY.Workload("rb_contig", B=1, S=1024, N=4, Nkv=4, D=64, C=4, layout="contiguous"), "contiguous"),
     "c8_d128": (SY.Workload("rb_c8", B=1, S=2048, N=2, Nkv=2, D=128, C=8), "zigzag"),
     "gqa_c2": (SY.Workload("rb_gqa", B=2, S=768, N=8, Nkv=4, D=64, C=2), "zigzag"),
+    # degenerate one-rank ring, the most virtual ranks one launch takes, and ragged 450-row shards with GQA
+    "c1": (SY.Workload("rb_c1", B=1, S=640, N=2, Nkv=2, D=64, C=1), "zigzag"),
+    "c64_max": (SY.Workload("rb_c64", B=1, S=8192, N=2, Nkv=1, D=64, C=64), "zigzag"),
+    "ragged_gqa_c4": (SY.Workload("rb_rg", B=1, S=1800, N=4, Nkv=2, D=128, C=4), "zigzag"),
 }
 
 
