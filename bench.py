@@ -666,6 +666,41 @@ def run_ours(args, w):
 # --------------------------------------------------------------------------
 # sweep: work balance per virtual rank, contiguous vs zigzag
 # --------------------------------------------------------------------------
+def tile_counts_per_rank(pos, q_block=256, k_tile=128, q_tile=128):
+    """Per virtual rank, over all ring steps, the attention kernel's key-tile
+    work under its per-tile causal rule: for every (256-row query block, 128-key
+    tile) pair, `issued` if the tile's smallest key position is <= the block's
+    largest query position, else `skipped`; issued pairs counted again per
+    128-row query tile as `unmasked` (tile's largest key position <= the query
+    tile's smallest position) or `masked`.  pos: int [C][s] global positions.
+    Returns a list of dicts (one per rank)."""
+    import numpy as np
+    pos = np.asarray(pos)
+    C, s = pos.shape
+
+    def ranges(p, n):
+        t = [p[i:i + n] for i in range(0, len(p), n)]
+        return np.array([x.min() for x in t]), np.array([x.max() for x in t])
+
+    out = []
+    for r in range(C):
+        bmin, bmax = ranges(pos[r], q_block)
+        tmin, tmax = ranges(pos[r], q_tile)
+        c = {"issued": 0, "skipped": 0, "unmasked": 0, "masked": 0}
+        for st in range(C):
+            kmin, kmax = ranges(pos[(r - st) % C], k_tile)
+            iss = kmin[None, :] <= bmax[:, None]            # [blocks, key tiles]
+            c["issued"] += int(iss.sum())
+            c["skipped"] += int((~iss).sum())
+            for qb in range(len(bmin)):
+                for qt in range(2 * qb, min(2 * qb + 2, len(tmin))):
+                    un = iss[qb] & (kmax <= tmin[qt])
+                    c["unmasked"] += int(un.sum())
+                    c["masked"] += int((iss[qb] & ~un).sum())
+        out.append(c)
+    return out
+
+
 def exact_pairs_per_rank(S, C, layout):
     """Visible (query, key) pairs per rank (per batch and head), closed forms."""
     s = S // C
@@ -777,6 +812,7 @@ def run_sweep(args):
             "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "kv_rotation_copy_gbs": copy_gbs,
             "hbm_peak_gbs": peaks["hbm_gbs"],
             "merge_rows_per_step": rows,
+            "key_tiles_per_rank": tile_counts_per_rank(pos.cpu().numpy()),
         }
         print(json.dumps(line), flush=True)
         del q, k, v, qs, ks, vs, o, lse, ws, x, kbuf, o1, l1

@@ -74,3 +74,32 @@ def test_code_hash_ignores_comments_only():
     assert bench._code_only(src) != bench._code_only(other)
     assert bench._code_only(src) != bench._code_only(strings)  # string literals are code
     assert len(bench.attn_source_hash()) == 16
+
+
+def test_tile_counts_brute_force():
+    """The sweep's per-rank tile counts equal a per-element brute force of the
+    kernel's tile rules (issue a key tile for a 256-row block if any of its keys
+    is visible to any of the block's queries; run it unmasked for a 128-row
+    query tile if every key is visible to every query of the tile)."""
+    import numpy as np
+    import bench
+    import oracle as O
+    for C, S, layout in ((2, 1024, O.ZIGZAG), (4, 2048, O.ZIGZAG), (4, 2048, O.CONTIGUOUS), (3, 1536, O.CONTIGUOUS)):
+        pos = O.positions(S, C, layout)
+        got = bench.tile_counts_per_rank(pos)
+        s = S // C
+        for r in range(C):
+            c = {"issued": 0, "skipped": 0, "unmasked": 0, "masked": 0}
+            for st in range(C):
+                kp = pos[(r - st) % C]
+                for qb in range(0, s, 256):
+                    for kt in range(0, s, 128):
+                        vis = kp[kt:kt + 128][None, :] <= pos[r][qb:qb + 256][:, None]
+                        if vis.any():
+                            c["issued"] += 1
+                            for qt in range(qb, min(qb + 256, s), 128):
+                                allv = (kp[kt:kt + 128][None, :] <= pos[r][qt:qt + 128][:, None]).all()
+                                c["unmasked" if allv else "masked"] += 1
+                        else:
+                            c["skipped"] += 1
+            assert got[r] == c, (C, S, layout, r, got[r], c)
