@@ -224,6 +224,7 @@ def cpu_baseline(w, qkv64, target_s=12.0):
         if dt < target_s / 8:
             batch *= 2
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "extrapolated_full_workload_s": w.flops / (flops / secs),
             "sample": "%d random query rows x all %d heads of the %s workload (fp64 C oracle, %d threads), %.1f s"
                       % (rows_total, w.N, w.name, cores, secs)}
 
