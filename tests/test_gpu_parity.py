@@ -311,14 +311,15 @@ def _inverse_positions(pos_np):
     return inv
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_merge", "separate_merge"])
 @pytest.mark.parametrize("wname", ["s32k", "s128k"])
-def test_ring_full_size_sampled_rows(cuda_dev, wname):
+def test_ring_full_size_sampled_rows(cuda_dev, wname, fused):
     """Full-size workloads in the benchmark's launch configuration (prefetch on,
-    separate merge, fp32 output); sampled query rows of two heads checked
-    against the oracle."""
+    merge fused into the attention epilogue, fp32 output) and with the separate
+    merge; sampled query rows of two heads checked against the oracle."""
     w = SY.WORKLOADS[wname]
     (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, "zigzag")
-    o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1)
+    o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1, fused_merge=fused)
     torch.cuda.synchronize()
     assert torch.isfinite(lse_sh).all().item() and torch.isfinite(o_sh).all().item()
     rows = SY.sample_rows(w, n_random=48, edge=2)
