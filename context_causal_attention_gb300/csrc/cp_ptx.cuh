@@ -141,26 +141,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
            ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T-style product, single CTA.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Same with the A operand read from tensor memory.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // S = Q K^T for one 128-row tile: D/16 MMAs (K = 16 each) over the 128-byte
 // swizzled K-major tiles whose descriptors for k-step 0 are `a` and `b`; k-step
 // kk starts (kk / 4) * 16 KB + (kk % 4) * 32 B further (descriptor units of
@@ -478,14 +458,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
-}
-// acc + lo(pk) + hi(pk), where pk holds two bf16 values (exact widening adds).
-__device__ __forceinline__ float add_bf16x2(float acc, uint32_t pk) {
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
-        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
-        : "+f"(acc)
-        : "r"(pk));
-    return acc;
 }
 
 // 32-byte global store (8 fp32); the address must be 32-byte aligned.
