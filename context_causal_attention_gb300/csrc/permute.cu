@@ -178,10 +178,15 @@ cp_status launch_segments(SegArgs a, long long nseg, cudaStream_t stream) {
     return last_launch_status();
 }
 
-// The kernels may dereference [p, p + n): device (or managed) memory, or host
-// memory that is pinned and mapped into the device address space at the same
-// address.  Both ends of the range are checked.
+// The kernels may dereference [p, p + n): memory of the current device (or
+// managed memory), or host memory that is pinned and mapped into the device
+// address space at the same address.  Both ends of the range are checked.
 bool device_reachable(const void *p, size_t n) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
     const char *ends[2] = {static_cast<const char *>(p), static_cast<const char *>(p) + (n ? n - 1 : 0)};
     for (const char *e : ends) {
         cudaPointerAttributes at;
@@ -189,7 +194,7 @@ bool device_reachable(const void *p, size_t n) {
             cudaGetLastError();  // clear the sticky error of the query
             return false;
         }
-        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) continue;
+        if (at.type == cudaMemoryTypeManaged || (at.type == cudaMemoryTypeDevice && at.device == dev)) continue;
         if (at.type == cudaMemoryTypeHost && at.devicePointer == e) continue;
         return false;
     }

@@ -76,7 +76,7 @@ const char *cp_last_cuda_error(void);
  * owns [chunk r | chunk 2C-1-r] (layout CP_ZIGZAG; TE's "DualChunkSwap").
  * [RING] "The last remaining axis": rank r owns tokens [r*s, (r+1)*s)
  * (layout CP_CONTIGUOUS).
- *   x     : [B][S][N][D] of `dtype`, read only; device memory, or pinned host
+ *   x     : [B][S][N][D] of `dtype`, read only; memory of the current device, or pinned host
  *           memory mapped at the same address (cudaHostAlloc / cudaMallocHost /
  *           cudaHostRegister under unified addressing), which the kernel then
  *           reads across the host link (the host-to-device copy and the shard
@@ -95,7 +95,7 @@ cp_status cp_zigzag_shard(const void *x, void *x_sh, int64_t B, int64_t S, int64
  * into global sequence order ([OCP] All-gather: the rank-order result
  * [chunk 0, chunk 7, chunk 1, chunk 6, ...] reordered to sequence order).
  *   x_sh  : device, [C][B][S/C][N][D], read only
- *   x     : [B][S][N][D], written (must not overlap x_sh); device memory, or
+ *   x     : [B][S][N][D], written (must not overlap x_sh); current-device memory, or
  *           pinned host memory mapped at the same address (the kernel then
  *           writes across the host link: unshard and device-to-host copy in
  *           one pass); other host memory -> CP_ERR_ARGUMENT
