@@ -38,11 +38,16 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _ptr(t):
+def _ptr(t, host_ok=False):
+    """Raw pointer of a contiguous tensor.  Device tensors only, unless host_ok
+    (the library then checks that host memory is pinned and mapped), so a CPU
+    tensor never reaches a kernel by mistake."""
     if t is None:
         return None
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
+    if not (t.is_cuda or host_ok):
+        raise ValueError("tensor must be a CUDA tensor")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -59,7 +64,8 @@ def cp_zigzag_shard(x, C, layout=CP_ZIGZAG, out=None, stream=None):
     if out is None:
         dev = x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
         out = torch.empty((C, B, S // C, N, D), dtype=x.dtype, device=dev)
-    st = _lib.lib().cp_zigzag_shard(_ptr(x), _ptr(out), B, S, N, D, C, _dtype_code(x), layout, _stream(stream))
+    st = _lib.lib().cp_zigzag_shard(_ptr(x, host_ok=True), _ptr(out), B, S, N, D, C, _dtype_code(x), layout,
+                                    _stream(stream))
     _lib.check("cp_zigzag_shard", st)
     return out
 
@@ -72,8 +78,8 @@ def cp_zigzag_unshard(x_sh, layout=CP_ZIGZAG, out=None, stream=None):
     C, B, s, N, D = x_sh.shape
     if out is None:
         out = torch.empty((B, C * s, N, D), dtype=x_sh.dtype, device=x_sh.device)
-    st = _lib.lib().cp_zigzag_unshard(_ptr(x_sh), _ptr(out), B, C * s, N, D, C, _dtype_code(x_sh), layout,
-                                      _stream(stream))
+    st = _lib.lib().cp_zigzag_unshard(_ptr(x_sh), _ptr(out, host_ok=True), B, C * s, N, D, C, _dtype_code(x_sh),
+                                      layout, _stream(stream))
     _lib.check("cp_zigzag_unshard", st)
     return out
 
@@ -84,7 +90,8 @@ def cp_zigzag_positions(S, C, layout=CP_ZIGZAG, device="cuda", out=None, stream=
     if out is None:
         out = torch.empty((C, S // C), dtype=torch.int32, device=dev)
     on_dev = 1 if out.is_cuda else 0
-    st = _lib.lib().cp_zigzag_positions(_ptr(out), S, C, layout, on_dev, _stream(stream) if on_dev else None)
+    st = _lib.lib().cp_zigzag_positions(_ptr(out, host_ok=True), S, C, layout, on_dev,
+                                        _stream(stream) if on_dev else None)
     _lib.check("cp_zigzag_positions", st)
     return out
 

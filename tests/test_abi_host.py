@@ -175,3 +175,19 @@ def test_selftest_timeout_range(cplib):
     assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == 10
     assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 999_999, None) == 10
     assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3_000_000_000, None) == 10
+
+
+def test_binding_refuses_cpu_tensors_before_any_call():
+    """The Python binding raises before reaching the library when a tensor that
+    must be on the GPU is a CPU tensor (host memory is accepted only where the
+    library can check and use it: the shard input, the unshard output, host
+    positions)."""
+    import pytest
+    import torch
+    from context_causal_attention_gb300 import ops as F
+    q = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
+    pos = torch.arange(128, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        F.cp_attn_partial(q, q, q, pos, pos, o=torch.zeros(1, 128, 2, 64), lse=torch.zeros(1, 2, 128))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        F.cp_lse_merge(torch.zeros(1, 4, 2, 64), torch.zeros(1, 2, 4), torch.zeros(1, 4, 2, 64), torch.zeros(1, 2, 4))
