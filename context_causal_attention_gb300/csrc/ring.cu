@@ -19,6 +19,9 @@
 //                 double buffer while step st computes ("start the next
 //                 async send/recv before computing", Peer-to-peer / Forward),
 //                 ordered with events and joined back into the caller's stream.
+//                 A buffer's refill waits for the step's merge as well as its
+//                 attention launch, so that the copy overlaps the next
+//                 compute-bound attention launch more and the merge less.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -224,17 +227,18 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         rec(4 * step + 0);
         if (st == CP_OK) st = tf32 ? launch_attn_tf32(ps, vt, stream) : launch_attn(ps, stream);
         rec(4 * step + 1);
+        rec(4 * step + 2);
+        if (step > 0 && !fused && st == CP_OK)
+            st = launch_merge(o_acc, lse_sh, o_tile, lse_tile, C * B, s, N, D, stream);
+        rec(4 * step + 3);
         if (use_prefetch && st == CP_OK && step + 2 < C) {
-            // buffer (step+2)%2 was last read by this step's launch
+            // buffer (step+2)%2 was last read by this step's attention launch;
+            // the refill is ordered after the merge too (see the file header)
             if (cudaEventRecord(res->attn_done[step % 2], stream) != cudaSuccess ||
                 cudaStreamWaitEvent(res->side, res->attn_done[step % 2], 0) != cudaSuccess)
                 st = CP_ERR_CUDA;
             issue_copy(step + 2);
         }
-        rec(4 * step + 2);
-        if (step > 0 && !fused && st == CP_OK)
-            st = launch_merge(o_acc, lse_sh, o_tile, lse_tile, C * B, s, N, D, stream);
-        rec(4 * step + 3);
     }
     if (use_prefetch) {
         // join the side stream back into the caller's stream in every case
