@@ -92,23 +92,30 @@ def recorded_traffic(workload, fused=False):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons, sampled every 50 ms while running.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Each sample carries nvidia-smi's own timestamp; `window(t0, t1)` (host
+    wall-clock seconds) marks the timed region, and the summary keeps the
+    samples taken inside it (all samples when none fell inside)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=50):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
         self.t = None
+        self.win = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -118,6 +125,41 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def window(self, t0, t1):
+        self.win = (t0, t1)
+
+    @staticmethod
+    def parse(lines):
+        """[(epoch seconds or None, sm MHz, max sm MHz, {reason: active})] from the csv lines."""
+        out = []
+        for ln in lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm, mx = float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                if "." in parts[0]:
+                    ts += float("0." + parts[0].split(".")[1])
+            except (ValueError, OverflowError):
+                ts = None
+            act = {nm: val.lower().startswith("active") for nm, val in zip(ClockSampler.REASONS, parts[6:10])}
+            out.append((ts, sm, mx, act))
+        return out
+
+    @staticmethod
+    def summarise(samples, win):
+        inside = [x for x in samples if win and x[0] is not None and win[0] <= x[0] <= win[1]]
+        use = inside if inside else samples
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_in_timed_region": 0}
+        reasons = sorted({nm for x in use for nm, on in x[3].items() if on})
+        return {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": max(x[2] for x in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
 
     def stop(self):
         if self.proc is None:
@@ -129,22 +171,7 @@ class ClockSampler:
             self.proc.kill()
         if self.t:
             self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return self.summarise(self.parse(self.lines), self.win)
 
 
 def dist_setup(n_gpus):
@@ -435,6 +462,9 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
+    now = time.time()
+    # nvidia-smi stamps whole milliseconds; widen the window by one interval
+    clocks.window(now - wall - 0.05, now + 0.05)
     ms_total = (sum(a.elapsed_time(b) for a, b in step_ev) if flush else t_start.elapsed_time(t_end))
     clk = clocks.stop()
     ms_total = max_over_ranks(ms_total, world)

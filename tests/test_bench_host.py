@@ -3,6 +3,7 @@ oracle, and the multi-process aggregation (barrier + max over ranks) on a
 world_size-2 gloo group."""
 import os
 import socket
+import time
 
 import numpy as np
 import pytest
@@ -103,3 +104,26 @@ def test_tile_counts_brute_force():
                         else:
                             c["skipped"] += 1
             assert got[r] == c, (C, S, layout, r, got[r], c)
+
+
+def _smi_line(t, sm, power_cap=False):
+    """One line of `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits`."""
+    stamp = time.strftime("%Y/%m/%d %H:%M:%S", time.localtime(t)) + ".%03d" % int(round((t % 1) * 1000) % 1000)
+    cap = "Active" if power_cap else "Not Active"
+    return f"{stamp}, 0, {sm}, 2070, 950.5, 0x0000000000000004, Not Active, Not Active, Not Active, {cap}"
+
+
+def test_clock_samples_kept_inside_timed_region():
+    t0 = 1_700_000_000.0
+    # idle before (low clock), loaded and power-capped inside, idle after
+    lines = [_smi_line(t0 + 0.05 * k, 2070 if 4 <= k < 8 else 345, power_cap=(k == 5)) for k in range(12)]
+    lines.append("garbage line")
+    samples = bench.ClockSampler.parse(lines)
+    assert len(samples) == 12
+    assert abs(samples[3][0] - (t0 + 0.15)) < 2e-3
+    got = bench.ClockSampler.summarise(samples, (t0 + 0.19, t0 + 0.36))
+    assert got["samples_in_timed_region"] == 4 and got["samples"] == 4
+    assert got["sm_mhz"] == 2070 and got["sm_max_mhz"] == 2070 and got["reasons"] == ["sw_power_cap"]
+    # a window no sample fell in: every sample is used, and that is reported
+    got = bench.ClockSampler.summarise(samples, (t0 + 100, t0 + 101))
+    assert got["samples_in_timed_region"] == 0 and got["samples"] == 12
