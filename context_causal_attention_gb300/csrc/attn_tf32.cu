@@ -8,9 +8,11 @@
 // Layout of the work: one persistent CTA per SM, 256 threads; work items are
 // (rank, b, h, 128-row query tile, or tiles u and nqt-1-u back to back), in the
 // shared order of cp_sched.cuh.
-//   warp 0      TMA producer: the 128-row fp32 query tile of the item, then a
-//               2-stage ring of 64-key K tiles and 64-key V^T tiles (128-byte
-//               swizzle, 32 fp32 columns per swizzle atom);
+//   warp 0      TMA producer: the 128-row fp32 query tile of the item, then
+//               2-stage rings of 64-key K tiles and 64-key V^T tiles (128-byte
+//               swizzle, 32 fp32 columns per swizzle atom), with separate
+//               barriers: a K stage is refilled as soon as its scores are
+//               computed, and each V^T tile is loaded one tile after its K;
 //   warp 1      TMEM allocator (256 columns: S0 | S1 | O) and MMA issuer:
 //               S_b = Q K^T (M = 128, N = 64, K = 8 per instruction) into the
 //               score buffer b = tile parity, O += P V with P read from TMEM;
@@ -59,9 +61,9 @@ struct CfgT {
     static constexpr int kOffOrder = kOffTab + kMaxTables * 8;
     static constexpr int kOffCost = kOffOrder + kMaxPairs * 4;
     static constexpr int kOffSeg = kOffCost + kMaxPairs * 4;
-    // q_full, q_empty, k_full[S], k_empty[S] (K and V of a stage travel together),
-    // s_full[2], p_full[2], pv_done, o_full, o_empty, drain
-    static constexpr int kNumBars = 2 + 2 * kTStages + 9;
+    // q_full, q_empty, k_full[S], k_empty[S], s_full[2], p_full[2], pv_done, o_full,
+    // o_empty, drain, v_full[S], v_empty[S]
+    static constexpr int kNumBars = 2 + 2 * kTStages + 9 + 2 * kTStages;
     static constexpr int kOffBar = kOffSeg + (kMaxPairs + 2) * 4;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMiscBytes = 16 + kMaxC * 4 + kMaxTables / 8;
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     uint64_t *q_full = bar, *q_empty = bar + 1, *k_full = bar + 2, *k_empty = bar + 2 + kTStages;
     uint64_t *s_full = bar + 2 + 2 * kTStages, *p_full = s_full + 2, *pv_done = s_full + 4, *o_full = s_full + 5,
              *o_empty = s_full + 6, *drain = s_full + 7;
+    uint64_t *v_full = s_full + 8, *v_empty = v_full + kTStages;
     const int2 *ktab = tab;                 // [kpr][nkt] 64-key tiles
     const int2 *qtab = tab + a.kpr * a.nkt;  // [C][nqt] 128-row query tiles
 
@@ -163,6 +166,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
         for (int s = 0; s < kTStages; ++s) {
             mbar_init(k_full + s, 1);
             mbar_init(k_empty + s, 1);
+            mbar_init(v_full + s, 1);
+            mbar_init(v_empty + s, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
@@ -244,8 +249,22 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (warp == 0) {
         // -------------------------------------------------------- TMA producer
         if (lane == 0) {
-            uint32_t it = 0, t = 0, k_issued = 0, k_par = 0;
+            uint32_t it = 0, t = 0, k_issued = 0, k_par = 0, v_issued = 0, v_par = 0;
             int q_par = -1;
+            // V^T of a tile is loaded one tile after its K: a K stage is freed as soon
+            // as that tile's scores are computed, so the next K loads while the
+            // softmax and P V of earlier tiles run
+            auto load_v = [&](int kt, uint32_t st, uint32_t ph, int hk, int kvrow) -> bool {
+                if (!mbar_wait(v_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) return false;
+                mbar_arrive_expect_tx(v_full + st, K::kKBytes);
+                // V^T [D rows][keys kt*64 ..]: two atoms of 32 keys
+                for (int at = 0; at < 2; ++at)
+                    tma_load_4d(sV + st * K::kKBytes + at * K::kVtAtom, &tmVt, v_full + st, kt * 64 + 32 * at, 0, hk,
+                                kvrow);
+                v_issued |= 1u << st;
+                v_par = (v_par & ~(1u << st)) | (ph << st);
+                return true;
+            };
             bool ok = true;
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
@@ -268,27 +287,32 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     const int qmax = qtab[r * a.nqt + qt].y;
                     const bool srt = sorted_flag[owner] != 0;
                     const int hk = h / hq_per_kv, kvrow = kvr * a.B + b;
+                    int pkt = -1;  // tile whose V^T is still to be loaded
+                    uint32_t pst = 0, pph = 0;
                     for (int kt = next_kt(0, kt_o, qmax, srt); kt < a.nkt; kt = next_kt(kt + 1, kt_o, qmax, srt)) {
                         const uint32_t st = t % kTStages, ph = (t / kTStages) & 1u;
                         if (!mbar_wait(k_empty + st, ph ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                        mbar_arrive_expect_tx(k_full + st, 2 * K::kKBytes);
+                        mbar_arrive_expect_tx(k_full + st, K::kKBytes);
                         for (int at = 0; at < K::kAtoms; ++at)
                             tma_load_4d(sK + st * K::kKBytes + at * K::kKAtom, &tmK, k_full + st, 32 * at, hk, kt * 64, kvrow);
-                        // V^T [D rows][keys kt*64 ..]: two atoms of 32 keys
-                        for (int at = 0; at < 2; ++at)
-                            tma_load_4d(sV + st * K::kKBytes + at * K::kVtAtom, &tmVt, k_full + st, kt * 64 + 32 * at, 0, hk,
-                                        kvrow);
                         k_issued |= 1u << st;
                         k_par = (k_par & ~(1u << st)) | (ph << st);
+                        if (pkt >= 0 && !load_v(pkt, pst, pph, hk, kvrow)) { ok = false; break; }
+                        pkt = kt;
+                        pst = st;
+                        pph = ph;
                         ++t;
                     }
+                    if (ok && pkt >= 0 && !load_v(pkt, pst, pph, hk, kvrow)) ok = false;
                 }
             }
             if (!ok) {
                 volatile int no_abort = 0;
                 if (q_par >= 0) mbar_wait(q_full, static_cast<uint32_t>(q_par), &no_abort, 100000000ull);
-                for (int st = 0; st < kTStages; ++st)
+                for (int st = 0; st < kTStages; ++st) {
                     if ((k_issued >> st) & 1u) mbar_wait(k_full + st, (k_par >> st) & 1u, &no_abort, 100000000ull);
+                    if ((v_issued >> st) & 1u) mbar_wait(v_full + st, (v_par >> st) & 1u, &no_abort, 100000000ull);
+                }
             }
         }
         __syncwarp();
@@ -310,6 +334,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     umma_tf32_ss(tmem + 64 * b, dq + (kk >> 2) * (K::kQAtom >> 4) + (kk & 3) * 2,
                                  dk + st * kKU + (kk >> 2) * (K::kKAtom >> 4) + (kk & 3) * 2, kIdS, kk > 0 ? 1u : 0u);
                 umma_commit(s_full + b);
+                umma_commit(k_empty + st);  // the K stage is free once the scores are done
             };
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
@@ -336,9 +361,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     if (!ok) break;
                     if (n <= 2) umma_commit(q_empty);
                     for (int j = 0; j < n; ++j, ++t) {
-                        const uint32_t bb = t & 1u, st = t % kTStages;
+                        const uint32_t bb = t & 1u, st = t % kTStages, ph = (t / kTStages) & 1u;
                         if (!mbar_wait(p_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                         if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (!mbar_wait(v_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
                         tc_fence_after();
                         // O (+)= P V: 64 keys in 8 k-steps of 8 (P columns +8; V^T k-step kk
                         // at (kk / 4) atoms + (kk % 4) * 32 bytes)
@@ -347,7 +373,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                                          dv + st * kKU + (kk >> 2) * (K::kVtAtom >> 4) + (kk & 3) * 2, kIdO,
                                          (j > 0 || kk > 0) ? 1u : 0u);
                         umma_commit(pv_done);
-                        umma_commit(k_empty + st);
+                        umma_commit(v_empty + st);
                         if (j + 2 < n) {
                             const uint32_t st2 = (t + 2) % kTStages, ph2 = ((t + 2) / kTStages) & 1u;
                             if (!mbar_wait(k_full + st2, ph2, abort_flag, a.timeout_ns)) { ok = false; break; }
