@@ -415,6 +415,11 @@ TF32_CASES = {
                                kp=lambda: np.random.default_rng(6).permutation(500)),
     "multi_tile_1024": dict(B=1, Sq=1024, Sk=1024, N=2, Nkv=2, D=128, qp=lambda: np.arange(1024),
                             kp=lambda: np.arange(1024)),
+    # items of a single 64-key tile: the K and V^T stages of one tile, nothing streamed after it
+    "single_key_tile": dict(B=2, Sq=100, Sk=64, N=3, Nkv=3, D=128, qp=lambda: np.arange(100),
+                            kp=lambda: np.arange(64)),
+    "single_ragged_key_tile": dict(B=1, Sq=37, Sk=23, N=2, Nkv=1, D=64, qp=lambda: np.arange(37),
+                                   kp=lambda: np.arange(23)),
 }
 
 
