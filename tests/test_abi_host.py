@@ -101,6 +101,12 @@ def test_merge_and_ring_validation(cplib):
     assert ring(*bad, FAKE, 1 << 40, None) == 7
     ev = (ctypes.c_void_p * 3)()
     assert cplib.cp_ring_attention_fwd_traced(*args, FAKE, need, None, ev, 3) == 10  # needs 4C events
+    # ring flags: unknown bits are refused; the tf32 path is zero copy and merges separately
+    PREFETCH, FUSED, TF32 = 1, 2, 4
+    for flags, want in [(8, 10), (TF32 | PREFETCH, 7), (TF32 | FUSED, 7)]:
+        bad = list(args)
+        bad[12] = flags
+        assert ring(*bad, FAKE, 1 << 40, None) == want, flags
 
 
 def test_allgather_and_ulysses_validation(cplib):
