@@ -612,7 +612,7 @@ def run_ours(args, w):
         comp.wait_stream(s_in)
 
     def time_pipelined(reps):
-        # the host link's speed varies from run to run on a shared machine, so
+        # the host link's speed varies from run to run, so
         # the pipelined figure is the median of `reps` timed runs of K steps
         e2e_pipelined(2)
         torch.cuda.synchronize()
