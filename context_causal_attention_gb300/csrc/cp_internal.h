@@ -67,6 +67,12 @@ cp_status validate_attn(const AttnProblem &p);
 // Validate then enqueue the attention kernel on `stream`.
 cp_status launch_attn(const AttnProblem &p, cudaStream_t stream);
 
+// The checks of a ring forward call that do not involve its workspace
+// (pointers, enums, flags, shapes, divisibility, the attention problem).
+cp_status ring_check_args(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos, int64_t B,
+                          int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout,
+                          int flags, const void *o_sh, cp_dtype o_dtype, const float *lse_sh);
+
 // In-place LSE merge over `rows` rows of D fp32 values laid out as
 // o [B][Sq][N][D], lse [B][N][Sq] (B may fold the rank dimension).
 cp_status launch_merge(float *o_acc, float *lse_acc, const float *o_tile, const float *lse_tile, int64_t B,

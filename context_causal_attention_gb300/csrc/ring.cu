@@ -121,20 +121,59 @@ cp_status rotate_copy(void *dst, const void *src, size_t rank_bytes, int C, int 
     return CP_OK;
 }
 
-cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos, int64_t B, int64_t S,
-                    int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout, int flags,
-                    void *o_sh, cp_dtype o_dtype, float *lse_sh, void *workspace, size_t ws_bytes,
-                    cudaStream_t stream, const cudaEvent_t *events, int n_events) {
+}  // namespace
+
+// The checks of a ring call that do not involve its workspace: pointers,
+// enums, flags, shapes, divisibility and the attention problem itself.  The
+// fp32 accumulator of a bf16 output lives in the (256-byte aligned)
+// workspace, so for that case an aligned stand-in address takes its place.
+cp_status ring_check_args(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos, int64_t B,
+                          int64_t S, int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout,
+                          int flags, const void *o_sh, cp_dtype o_dtype, const float *lse_sh) {
     if (!q_sh || !k_sh || !v_sh || !pos || !o_sh || !lse_sh) return CP_ERR_NULL;
     if (o_dtype != CP_F32 && o_dtype != CP_BF16) return CP_ERR_DTYPE;
     if (layout != CP_ZIGZAG && layout != CP_CONTIGUOUS) return CP_ERR_ARGUMENT;
     if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE | CP_RING_TF32)) return CP_ERR_ARGUMENT;
+    const bool tf32 = (flags & CP_RING_TF32) != 0;
+    if (tf32 && (flags & (CP_RING_PREFETCH | CP_RING_FUSED_MERGE))) return CP_ERR_UNSUPPORTED;
+    if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
+    if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
+    alignas(256) static const float acc_stand_in[1] = {0.f};
+    AttnProblem chk{};
+    chk.q = q_sh;
+    chk.k = k_sh;
+    chk.v = v_sh;
+    chk.q_pos = pos;
+    chk.k_pos = pos;
+    chk.q_pos_stride = S / C;
+    chk.k_pos_stride = S / C;
+    chk.o = const_cast<float *>(o_dtype == CP_F32 ? static_cast<const float *>(o_sh) : acc_stand_in);
+    chk.lse = const_cast<float *>(lse_sh);
+    chk.C = C;
+    chk.B = B;
+    chk.N = N;
+    chk.Nkv = Nkv;
+    chk.D = D;
+    chk.Sq = S / C;
+    chk.Sk = S / C;
+    chk.scale = scale;
+    return tf32 ? validate_attn_tf32(chk) : validate_attn(chk);
+}
+
+namespace {
+
+cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const int32_t *pos, int64_t B, int64_t S,
+                    int64_t N, int64_t Nkv, int64_t D, int C, float scale, cp_layout layout, int flags,
+                    void *o_sh, cp_dtype o_dtype, float *lse_sh, void *workspace, size_t ws_bytes,
+                    cudaStream_t stream, const cudaEvent_t *events, int n_events) {
+    {
+        const cp_status a = ring_check_args(q_sh, k_sh, v_sh, pos, B, S, N, Nkv, D, C, scale, layout, flags, o_sh,
+                                            o_dtype, lse_sh);
+        if (a != CP_OK) return a;
+    }
     const int prefetch = (flags & CP_RING_PREFETCH) ? 1 : 0;
     const bool fused = (flags & CP_RING_FUSED_MERGE) != 0;
     const bool tf32 = (flags & CP_RING_TF32) != 0;
-    if (tf32 && (prefetch || fused)) return CP_ERR_UNSUPPORTED;
-    if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
-    if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
     if (events && n_events < 4 * C) return CP_ERR_ARGUMENT;
     const int64_t s = S / C;
     const Layout L = ws_layout(B, S, N, Nkv, D, C, flags, o_dtype);

@@ -419,14 +419,18 @@ cp_status cp_selftest_stalled_producer(const void *q, const void *k, const void 
  *   passes all inputs and outputs.
  *   Scratch: the call uses one file-scope device array of
  *   CP_NOALLOC_SCRATCH_BYTES bytes inside the library (every GPU on which the
- *   library is loaded keeps it until the process exits).  Sizes whose
- *   cp_ring_workspace_size(..., prefetch = 0, o_dtype, ...) exceeds
- *   CP_NOALLOC_SCRATCH_BYTES are rejected with CP_ERR_WORKSPACE before
- *   anything is enqueued.  The call never calls cudaMalloc, cudaFree or any
- *   allocating routine.
- *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and caches it; make
- *   that first call before any stream capture on that device.
+ *   library is loaded keeps it until the process exits).  The ring's own
+ *   argument checks (pointers, enums, shapes, divisibility, alignment) run
+ *   first; then sizes whose cp_ring_workspace_size(..., prefetch = 0,
+ *   o_dtype, ...) exceeds CP_NOALLOC_SCRATCH_BYTES are rejected with
+ *   CP_ERR_WORKSPACE.  Either way nothing is enqueued.  The call never calls
+ *   cudaMalloc, cudaFree or any allocating routine.
+ *   Set-up: the first call in a CUDA context looks up the array's device
+ *   address in that context (cudaGetSymbolAddress, with the caller's device
+ *   and context current) and caches it, keyed by the context's id; make that
+ *   first call before any stream capture in that context.  A call made in a
+ *   new context (after cudaDeviceReset, or under a driver context the caller
+ *   made current) looks the address up again, so no stale address is used.
  *   Sharing: all calls on a device share the array, which keeps the last
  *   call's contents (nothing needs clearing: every scratch byte a call reads
  *   it has written itself).  Calls whose executions overlap on the GPU (for

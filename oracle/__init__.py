@@ -139,8 +139,10 @@ def attn_blockwise(q, k, v, q_pos, k_pos, block, scale=None):
 def lse_merge(o_acc, lse_acc, o_tile, lse_tile):
     """Merge a completed partial into an accumulator; returns new (o, lse).
 
-    "On Context Parallelism", Peer-to-peer / Forward (the tile merge).
-    Inputs are not modified.  -inf tile rows leave the accumulator unchanged.
+    "Context parallelism: Ring Attention and Ulysses", Ring Attention: lse =
+    log(e^lse1 + e^lse2), o = o1 e^(lse1 - lse) + o2 e^(lse2 - lse) (the same
+    result as the tile merge of "On Context Parallelism", Peer-to-peer /
+    Forward).  Inputs are not modified.  -inf tile rows leave the accumulator unchanged.
     """
     o = _f64(o_acc).copy()
     lse = _f64(lse_acc).copy()

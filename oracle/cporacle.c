@@ -267,23 +267,18 @@ int orc_attn_blockwise(const double *q, const double *k, const double *v, const 
 /* ------------------------------------------------------------------------ */
 /* LSE merge of two completed partials, in place into (o_acc, lse_acc).     */
 /*                                                                          */
-/* [OCP] Peer-to-peer / Forward, the tile-merge step:                       */
-/*   merged = logaddexp(lse, tile_lse)                                      */
-/*   old    = exp(lse - merged),  tile = exp(tile_lse - merged)             */
-/*   o      = old * o + tile * tile_o,   lse = merged                       */
-/* (also [HB] "Ring Attention", the formula after the ring description).    */
-/* READING (the pages are silent): a row whose tile_lse is -inf is left     */
-/* unchanged; a row whose lse is -inf takes the tile's values.  Layouts:    */
-/* o [B][Sq][N][D], lse [B][N][Sq].                                         */
+/* [HB] "Ring Attention: passing the KV once around a ring": two partials   */
+/* (o1, lse1), (o2, lse2) of one query row combine into                     */
+/*   lse = log(e^lse1 + e^lse2),  o = o1 e^(lse1 - lse) + o2 e^(lse2 - lse) */
+/* ([OCP] Peer-to-peer / Forward merges the ring's tiles with the same      */
+/* result).  Evaluated with the larger lse factored out: with hi, lo the    */
+/* larger and smaller of the two and r = e^(lo - hi) in (0, 1],             */
+/* lse = hi + log(1 + r); the weight e^(lse_i - lse) is 1 / (1 + r) for the */
+/* partial with lse hi and r / (1 + r) for the one with lse lo.             */
+/* READING (the pages are silent): a row whose tile lse is -inf is left     */
+/* unchanged; a row whose accumulated lse is -inf takes the tile's values.  */
+/* Layouts: o [B][Sq][N][D], lse [B][N][Sq].                                */
 /* ------------------------------------------------------------------------ */
-static double orc_logaddexp(double a, double b) {
-    if (a == ORC_NEG_INF) return b;
-    if (b == ORC_NEG_INF) return a;
-    const double mx = a > b ? a : b;
-    const double mn = a > b ? b : a;
-    return mx + log1p(exp(mn - mx));
-}
-
 void orc_lse_merge(double *o_acc, double *lse_acc, const double *o_t, const double *lse_t, long B,
                    long Sq, long N, long D) {
     for (long b = 0; b < B; ++b)
@@ -299,11 +294,16 @@ void orc_lse_merge(double *o_acc, double *lse_acc, const double *o_t, const doub
                     *la = lt;
                     continue;
                 }
-                const double merged = orc_logaddexp(*la, lt);
-                const double old_scale = exp(*la - merged);
-                const double tile_scale = exp(lt - merged);
-                for (long d = 0; d < D; ++d) oa[d] = old_scale * oa[d] + tile_scale * ot[d];
-                *la = merged;
+                const int acc_is_hi = *la >= lt;
+                const double hi = acc_is_hi ? *la : lt;
+                const double lo = acc_is_hi ? lt : *la;
+                const double r = exp(lo - hi);
+                const double w_hi = 1.0 / (1.0 + r);
+                const double w_lo = r / (1.0 + r);
+                const double w_acc = acc_is_hi ? w_hi : w_lo;
+                const double w_tile = acc_is_hi ? w_lo : w_hi;
+                for (long d = 0; d < D; ++d) oa[d] = w_acc * oa[d] + w_tile * ot[d];
+                *la = hi + log1p(r);
             }
 }
 

@@ -109,6 +109,33 @@ def test_merge_and_ring_validation(cplib):
         assert ring(*bad, FAKE, 1 << 40, None) == want, flags
 
 
+def test_noalloc_ring_validation_order(cplib):
+    """The allocation-free ring runs the ring's own argument checks before its
+    scratch-size check, and refuses everything on the host (no CUDA call)."""
+    f = cplib.cp_ring_attention_fwd_noalloc
+    # q, k, v, pos, B, S, N, Nkv, D, C, scale, layout, o, o_dtype, lse, stream: the s32k workload
+    big = [FAKE, FAKE, FAKE, FAKE, 1, 32768, 32, 32, 128, 4, 0.088, 0, FAKE, 1, FAKE, None]
+    assert f(*big) == 6                                  # needs more scratch than the array holds
+    bad = list(big)
+    bad[0] = NULL
+    assert f(*bad) == 1                                  # a null pointer is reported as such
+    bad = list(big)
+    bad[14] = NULL
+    assert f(*bad) == 1
+    bad = list(big)
+    bad[8] = 80
+    assert f(*bad) == 7                                  # D
+    bad = list(big)
+    bad[5] = 32764
+    assert f(*bad) == 3                                  # S % 2C
+    bad = list(big)
+    bad[13] = 9
+    assert f(*bad) == 4                                  # o dtype
+    bad = list(big)
+    bad[12] = MISALIGNED
+    assert f(*bad) == 5                                  # fp32 o needs 32-byte alignment
+
+
 def test_allgather_and_ulysses_validation(cplib):
     n = ctypes.c_size_t(0)
     assert cplib.cp_allgather_workspace_size(1, 256, 2, 2, 64, 2, ctypes.byref(n)) == 0 and n.value > 0

@@ -302,6 +302,33 @@ def test_ring_vs_monolithic_gpu_and_bf16_output(cuda_dev):
     assert torch.equal(l_bf, lse_sh)
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["separate_merge", "fused_merge"])
+def test_ring_vs_monolithic_s32k_all_rows(cuda_dev, fused):
+    """Ring output equals attention over the whole sequence ("On Context
+    Parallelism", Peer-to-peer / Forward): the S=32768 workload in the
+    benchmark's launch configuration (prefetch on) against ONE monolithic
+    cp_attn_partial call over all 32768 positions, every row and head compared
+    on the device, o and lse, within 1e-3."""
+    w = SY.WORKLOADS["s32k"]
+    (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, "zigzag")
+    gp = torch.arange(w.S, dtype=torch.int32, device=cuda_dev)
+    qd, kd, vd = (t.to(cuda_dev) for t in (q, k, v))
+    o_m, l_m = F.cp_attn_partial(qd, kd, vd, gp, gp)
+    del qd, kd, vd
+    o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1, fused_merge=fused)
+    o_ring = F.cp_zigzag_unshard(o_sh, lay)
+    del o_sh
+    torch.cuda.synchronize()
+    assert torch.isfinite(o_ring).all().item() and torch.isfinite(l_m).all().item()
+    d_o = torch.max(torch.abs(o_ring - o_m)).item()
+    l_ring = torch.empty_like(l_m)
+    for r in range(w.C):
+        l_ring[:, :, pos[r].long()] = lse_sh[r]
+    d_l = torch.max(torch.abs(l_ring - l_m)).item()
+    assert d_o <= RING_VS_MONO, "max|o_ring - o_mono| = %g" % d_o
+    assert d_l <= RING_VS_MONO, "max|lse_ring - lse_mono| = %g" % d_l
+
+
 def _inverse_positions(pos_np):
     C, s = pos_np.shape
     inv = np.empty((C * s, 2), dtype=np.int64)

@@ -1,39 +1,40 @@
 """The allocation-free ring entry point, for callers that may not call cudaMalloc.
 
+Code running inside a custom allocator's callbacks, runtimes that forbid
+allocation after start-up, and processes whose device memory pool belongs to
+another framework cannot allocate a workspace for the ring.
 cp_ring_attention_fwd_noalloc takes its scratch from a fixed-size array inside
-the library instead of a caller workspace.  This test calls it through the C
-ABI twice in a row (different inputs, so the second call runs over the first
-call's leftover scratch) and compares each result with cp_ring_attention_fwd
-on the same inputs, within the ring tolerance the other tests use.  It also
-checks that sizes needing more scratch than the array holds are refused.
+the library instead.  This test calls it through the C ABI twice in a row
+(different inputs and sizes, so the second call runs over the first call's
+leftover scratch) and checks each result two ways: bit for bit against
+cp_ring_attention_fwd on the same inputs (both run the same kernels in the
+same order, so any leftover-scratch error shows), and against the fp64 oracle
+ring within the attention tolerance the other tests use.  It also checks that
+sizes needing more scratch than the array holds are refused.
 
 Kept in a file of its own that pytest collects last.
 """
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
 import cp_synth as SY
+import oracle as O
 from context_causal_attention_gb300 import _lib
 from context_causal_attention_gb300 import ops as F
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-3  # ring tolerance used by the parity tests
+ATOL_O = 2e-2    # attention against the fp64 oracle, as in the parity tests
+ATOL_LSE = 1e-3
 SCRATCH_LIMIT = 64 << 20  # CP_NOALLOC_SCRATCH_BYTES in include/cpattn.h
 
 
 def _p(t):
     return ctypes.c_void_p(t.data_ptr())
-
-
-def _inputs(w, dev):
-    q, k, v, _ = SY.make_qkv(w)
-    qs, ks, vs = (F.cp_zigzag_shard(t.to(dev), w.C) for t in (q, k, v))
-    pos = F.cp_zigzag_positions(w.S, w.C, device=dev)
-    return qs, ks, vs, pos
 
 
 def _noalloc(cplib, w, qs, ks, vs, pos, o_dtype, stream):
@@ -64,17 +65,28 @@ def _with_workspace(cplib, w, qs, ks, vs, pos, o_dtype, stream):
     return o, lse
 
 
-def test_noalloc_ring_matches_workspace_ring_twice(cplib, cuda_dev):
+def _f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def test_noalloc_ring_matches_workspace_ring_and_oracle_twice(cplib, cuda_dev):
     stream = torch.cuda.current_stream().cuda_stream
     cases = [(SY.WORKLOADS["s4k"], _lib.CP_F32), (SY.WORKLOADS["tiny"], _lib.CP_BF16)]
     for w, o_dtype in cases:
-        qs, ks, vs, pos = _inputs(w, cuda_dev)
+        q, k, v, _ = SY.make_qkv(w)
+        qs, ks, vs = (F.cp_zigzag_shard(t.to(cuda_dev), w.C) for t in (q, k, v))
+        pos = F.cp_zigzag_positions(w.S, w.C, device=cuda_dev)
         o_ref, l_ref = _with_workspace(cplib, w, qs, ks, vs, pos, o_dtype, stream)
         o, l = _noalloc(cplib, w, qs, ks, vs, pos, o_dtype, stream)
         torch.cuda.synchronize()
-        assert torch.isfinite(o.float()).all() and torch.isfinite(l).all()
-        assert torch.max(torch.abs(o.float() - o_ref.float())).item() <= TOL
-        assert torch.max(torch.abs(l - l_ref)).item() <= TOL
+        # same kernels, same order, same inputs: the results are identical
+        assert torch.equal(o, o_ref), w.name
+        assert torch.equal(l, l_ref), w.name
+        # and they are the ring attention of the fp64 oracle
+        o64, l64 = O.ring_fwd(*(O.shard(_f64(t), w.C) for t in (q, k, v)), pos.cpu().numpy(),
+                              nthreads=O.default_threads())
+        assert np.max(np.abs(_f64(o) - o64)) <= ATOL_O, w.name
+        assert np.max(np.abs(_f64(l) - l64)) <= ATOL_LSE, w.name
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cplib, cuda_dev):
