@@ -63,6 +63,8 @@ def lib():
     L.cp_zigzag_positions.argtypes = [vp, i64, i32, i32, i32, vp]
     L.cp_ulysses_relayout.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, i32, i32, vp]
     L.cp_attn_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp]
+    L.cp_attn_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.POINTER(sz)]
+    L.cp_attn_partial_ws.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, sz, vp]
     L.cp_lse_merge.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp]
     L.cp_ring_workspace_size.argtypes = [i64, i64, i64, i64, i64, i32, i32, i32, ctypes.POINTER(sz)]
     L.cp_ring_attention_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, i32, vp, i32, vp,
@@ -78,14 +80,14 @@ def lib():
     L.cp_mesh_workspace_size.argtypes = [i64, i64, i64, i64, i64, i32, i32, i32, ctypes.POINTER(sz)]
     L.cp_mesh_attention_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, f32, i32, i32, vp, vp, vp,
                                         sz, vp]
-    L.cp_attn_bwd_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
+    L.cp_attn_bwd_workspace_size.argtypes = [i64, i64, i64, i64, ctypes.POINTER(sz)]
     L.cp_attn_bwd_partial.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp,
                                       i32, vp, sz, vp]
     L.cp_ring_bwd_workspace_size.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
     L.cp_ring_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, vp, vp,
                                         vp, sz, vp]
     L.cp_selftest_stalled_producer.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_uint64, vp]
-    L.cp_attn_f32_workspace_size.argtypes = [i64, i64, i64, i64, ctypes.POINTER(sz)]
+    L.cp_attn_f32_workspace_size.argtypes = [i64, i64, i64, i64, i64, ctypes.POINTER(sz)]
     L.cp_attn_partial_f32.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, sz, vp]
     L.cp_ring_attention_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, i32, vp,
                                                 vp]

@@ -13,7 +13,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libcpattn.so")
-SOURCES = ["attn.cu", "attn_bwd.cu", "attn_tf32.cu", "permute.cu", "merge.cu", "ring.cu", "strategies.cu", "abi.cu", "noalloc.cu"]
+SOURCES = ["attn.cu", "attn_bwd.cu", "attn_tf32.cu", "permute.cu", "merge.cu", "ring.cu", "strategies.cu", "abi.cu",
+           "noalloc.cu", "plan.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -104,6 +104,7 @@ struct AttnArgs {
     int nsp;          // super-blocks per rank
     int pair_blocks;  // a super-block holds query blocks u and nqb-1-u (else u alone)
     FastDiv div_nsp, div_n;  // by nsp, N (work-item decoding)
+    PlanPtrs gp;             // the launch's plan in global memory (kernels with kGlobalPlan)
 };
 
 struct Bars {
@@ -289,7 +290,10 @@ __device__ __forceinline__ void exp_pack128(const uint32_t (&sa)[64], const uint
     *sum = lo + hi;
 }
 
-template <int D>
+// kGlobalPlan: the launch's plan (position tables, bits, sorted flags, costs,
+// order) was written to global memory by the pre-pass and is read from there;
+// otherwise every CTA builds it in shared memory first.
+template <int D, bool kGlobalPlan>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
@@ -300,24 +304,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);  // [C*nkt] K tables, then [C*nqt] Q tables
-    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
+    int2 *tab_s = reinterpret_cast<int2 *>(smem + K::kOffTab);  // [C*nkt] K tables, then [C*nqt] Q tables
+    int *order_s = reinterpret_cast<int *>(smem + K::kOffOrder);
     // per (rank, query block): number of key tiles it processes
-    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);
-    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
+    int *cost_s = reinterpret_cast<int *>(smem + K::kOffCost);
+    int *seg_s = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
-    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
+    int *sorted_s = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
     // bit g set: K tile g holds consecutive positions kmin, kmin+1, ... (mask = column compare)
-    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);
+    uint32_t *bits_s = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);
     const Bars bars = bars_at<D>(smem);
-    const int2 *ktab = tab;
-    const int2 *qtab = tab + a.kpr * a.nkt;
+    const int2 *ktab = kGlobalPlan ? a.gp.ktab : tab_s;
+    const int2 *qtab = kGlobalPlan ? a.gp.qtab : tab_s + a.kpr * a.nkt;
+    const int *order = kGlobalPlan ? a.gp.order : order_s;
+    const int *cost = kGlobalPlan ? a.gp.cost : cost_s;
+    const int *seg_first = kGlobalPlan ? a.gp.seg_first : seg_s;
+    const int *sorted_flag = kGlobalPlan ? a.gp.ksorted : sorted_s;
+    const uint32_t *arith_bits = kGlobalPlan ? a.gp.kbits : bits_s;
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
         *abort_flag = 0;
-        for (int w = 0; w < kMaxTables / 32; ++w) arith_bits[w] = 0u;
+        if (!kGlobalPlan)
+            for (int w = 0; w < kMaxTables / 32; ++w) bits_s[w] = 0u;
         mbar_init(bars.q_full, 1);
         mbar_init(bars.q_empty, 1);
         mbar_init(bars.drain, 1);
@@ -346,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     // position tables: (min, max) of every 128-row tile, K tiles per owner rank
     // first, then Q tiles per rank.
-    {
+    if constexpr (!kGlobalPlan) {
         const int nk = a.kpr * a.nkt, total = nk + a.C * a.nqt;
         for (int g = warp; g < total; g += kThreads / 32) {
             const int32_t *p;
@@ -375,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mn = __reduce_min_sync(0xffffffffu, mn);
             mx = __reduce_max_sync(0xffffffffu, mx);
-            if (lane == 0) tab[g] = make_int2(mn, mx);
+            if (lane == 0) tab_s[g] = make_int2(mn, mx);
             if (g < nk) {
                 const int first = __shfl_sync(0xffffffffu, vals[0], 0);
                 bool ok = true;
@@ -385,20 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (row < lim) ok &= (static_cast<long long>(vals[m]) == static_cast<long long>(first) + lane + 32 * m);
                 }
                 ok = __all_sync(0xffffffffu, ok);
-                if (lane == 0 && ok) atomicOr(arith_bits + (g >> 5), 1u << (g & 31));
+                if (lane == 0 && ok) atomicOr(bits_s + (g >> 5), 1u << (g & 31));
             }
         }
-    }
-    __syncthreads();
-    if (tid < a.kpr) {
-        int ok = 1;
-        for (int kt = 1; kt < a.nkt; ++kt) ok &= (ktab[tid * a.nkt + kt].x >= ktab[tid * a.nkt + kt - 1].x);
-        sorted_flag[tid] = ok;
-    }
-    __syncthreads();
-    // key tiles of every (rank, query block) pair, then the longest-first
-    // order of the super-blocks cut into segments (see decode_super)
-    {
+        __syncthreads();
+        if (tid < a.kpr) {
+            int ok = 1;
+            for (int kt = 1; kt < a.nkt; ++kt) ok &= (ktab[tid * a.nkt + kt].x >= ktab[tid * a.nkt + kt - 1].x);
+            sorted_s[tid] = ok;
+        }
+        __syncthreads();
+        // key tiles of every (rank, query block) pair, then the longest-first
+        // order of the super-blocks cut into segments (see decode_super)
         const int np = a.C * a.nqb;
         for (int p = tid; p < np; p += kThreads) {
             const int r = p / a.nqb, qb = p % a.nqb;
@@ -417,10 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 for (int kt = 0; kt < a.nkt; ++kt) c += (kt_o[kt].x <= qmax);
             }
-            cost[p] = c;
+            cost_s[p] = c;
         }
         __syncthreads();
-        build_segments<kThreads>(cost, a.C, a.nqb, a.pair_blocks != 0, order, seg_first);
+        build_segments<kThreads>(cost_s, a.C, a.nqb, a.pair_blocks != 0, order_s, seg_s);
     }
     tc_fence_before();
     __syncthreads();
@@ -904,7 +912,34 @@ bool make_map_f32_rows(CUtensorMap *map, const float *base, int64_t cols, int64_
 
 namespace {
 
-template <int D>
+// The plan of a forward launch (see PlanSpec): 128-row query and key tiles,
+// cost units of two query tiles (one 256-row block).
+PlanSpec fwd_plan_spec(const AttnProblem &p, bool pair_blocks) {
+    PlanSpec s{};
+    s.q_pos = p.q_pos;
+    s.k_pos = p.k_pos;
+    s.q_pos_stride = p.q_pos_stride;
+    s.k_pos_stride = p.k_pos_stride;
+    s.C = p.C;
+    s.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
+    s.kpos_shift = p.kpos_shift;
+    s.Sq = static_cast<int>(p.Sq);
+    s.Sk = static_cast<int>(p.Sk);
+    s.q_tile = 128;
+    s.k_tile = 128;
+    s.unit_is_k = 0;
+    s.q_group = 2;
+    s.pair = pair_blocks ? 1 : 0;
+    return s;
+}
+
+// Does the plan fit in the kernel's shared-memory tables?
+bool fwd_plan_on_chip(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk) {
+    const int64_t nqt = (Sq + 127) / 128, nkt = (Sk + 127) / 128;
+    return kpr * nkt + C * nqt <= kMaxTables && C * ((nqt + 1) / 2) <= kMaxPairs;
+}
+
+template <int D, bool kGP>
 cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     using K = Cfg<D>;
     CUtensorMap mq, mk, mv;
@@ -945,15 +980,20 @@ cp_status launch_typed(const AttnProblem &p, cudaStream_t stream) {
     a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
     const long long n_items = static_cast<long long>(p.C) * a.nsp * p.B * p.N;
     if (n_items <= 0) return CP_OK;
+    a.gp = PlanPtrs{};
+    if (kGP) {
+        const cp_status st = launch_plan(fwd_plan_spec(p, a.pair_blocks != 0), p.plan, &a.gp, stream);
+        if (st != CP_OK) return st;
+    }
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(attn_fwd_kernel<D, kGP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         K::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return CP_ERR_CUDA;
     const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
-    attn_fwd_kernel<D><<<grid, kThreads, K::kSmemBytes, stream>>>(mq, mk, mv, a);
+    attn_fwd_kernel<D, kGP><<<grid, kThreads, K::kSmemBytes, stream>>>(mq, mk, mv, a);
     return last_launch_status();
 }
 
@@ -972,7 +1012,18 @@ int sm_count() {
     return n;
 }
 
-cp_status validate_attn(const AttnProblem &p) {
+size_t attn_plan_need(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk) {
+    if (fwd_plan_on_chip(C, kpr, Sq, Sk)) return 0;
+    AttnProblem p{};
+    p.C = static_cast<int>(C);
+    p.k_pos_stride = (kpr == 1) ? 0 : 1;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    // unpaired query blocks give the longer order, so this covers both
+    return plan_bytes(fwd_plan_spec(p, false));
+}
+
+cp_status validate_attn(const AttnProblem &p, bool check_plan) {
     if (!p.q || !p.k || !p.v || !p.q_pos || !p.k_pos || !p.o || !p.lse) return CP_ERR_NULL;
     if (p.C < 1 || p.C > kMaxC || p.B < 1 || p.N < 1 || p.Nkv < 1 || p.Sq < 1 || p.Sk < 1) return CP_ERR_SHAPE;
     if (p.D != 64 && p.D != 128) return CP_ERR_UNSUPPORTED;
@@ -985,10 +1036,13 @@ cp_status validate_attn(const AttnProblem &p) {
     if (reinterpret_cast<uintptr_t>(p.o) & 31u) return CP_ERR_ALIGNMENT;
     const int64_t nqt = (p.Sq + 127) / 128, nkt = (p.Sk + 127) / 128;
     const int64_t kpr = (p.k_pos_stride == 0) ? 1 : p.C;
-    if (kpr * nkt + p.C * nqt > kMaxTables || p.C * ((nqt + 1) / 2) > kMaxPairs) return CP_ERR_SHAPE;
     if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.B * p.N * p.C > INT32_MAX / 4 ||
-        static_cast<int64_t>(p.C) * ((nqt + 1) / 2) * p.B * p.N > INT32_MAX)
+        static_cast<int64_t>(p.C) * ((nqt + 1) / 2) * p.B * p.N > INT32_MAX || kpr * nkt + p.C * nqt > INT32_MAX / 8)
         return CP_ERR_SHAPE;
+    if (check_plan && !fwd_plan_on_chip(p.C, kpr, p.Sq, p.Sk)) {
+        if (!p.plan || p.plan_bytes < attn_plan_need(p.C, kpr, p.Sq, p.Sk)) return CP_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(p.plan) & 255u) return CP_ERR_ALIGNMENT;
+    }
     if (p.kv_shift < 0 || p.kv_shift >= p.C || p.kpos_shift < 0 || p.kpos_shift >= p.C) return CP_ERR_ARGUMENT;
     return CP_OK;
 }
@@ -996,10 +1050,45 @@ cp_status validate_attn(const AttnProblem &p) {
 cp_status launch_attn(const AttnProblem &p, cudaStream_t stream) {
     cp_status st = validate_attn(p);
     if (st != CP_OK) return st;
-    return p.D == 128 ? launch_typed<128>(p, stream) : launch_typed<64>(p, stream);
+    const bool on_chip = fwd_plan_on_chip(p.C, (p.k_pos_stride == 0) ? 1 : p.C, p.Sq, p.Sk);
+    if (on_chip) return p.D == 128 ? launch_typed<128, false>(p, stream) : launch_typed<64, false>(p, stream);
+    return p.D == 128 ? launch_typed<128, true>(p, stream) : launch_typed<64, true>(p, stream);
 }
 
 }  // namespace cpattn
+
+extern "C" cp_status cp_attn_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv, int64_t D,
+                                            size_t *bytes) {
+    if (!bytes) return CP_ERR_NULL;
+    if (B < 1 || Sq < 1 || Sk < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
+    *bytes = cpattn::attn_plan_need(1, 1, Sq, Sk);
+    return CP_OK;
+}
+
+extern "C" cp_status cp_attn_partial_ws(const void *q, const void *k, const void *v, const int32_t *q_pos,
+                                        const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,
+                                        int64_t Nkv, int64_t D, float scale, float *o, float *lse, void *workspace,
+                                        size_t ws_bytes, cudaStream_t stream) {
+    cpattn::AttnProblem p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.q_pos = q_pos;
+    p.k_pos = k_pos;
+    p.o = o;
+    p.lse = lse;
+    p.C = 1;
+    p.B = B;
+    p.N = N;
+    p.Nkv = Nkv;
+    p.D = D;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.scale = scale;
+    p.plan = workspace;
+    p.plan_bytes = workspace ? ws_bytes : 0;
+    return cpattn::launch_attn(p, stream);
+}
 
 extern "C" cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int32_t *q_pos,
                                      const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,

@@ -137,6 +137,7 @@ struct BwdArgs {
     unsigned long long timeout_ns;
     int pair;         // a super-block holds stationary tiles u and nt-1-u (else u alone)
     FastDiv div_nsp, div_h;  // by super-blocks per rank, heads per item
+    PlanPtrs gp;      // the launch's plan in global memory (kernels with kGlobalPlan)
 };
 
 // (min, max) of the positions of one 128-row tile (one warp per tile); when
@@ -267,7 +268,9 @@ __device__ __forceinline__ void release_half(uint64_t *bar, int lane) {
 // ======================================================================
 // dK / dV: K/V-stationary
 // ======================================================================
-template <int D>
+// kGlobalPlan (both backward kernels): the plan was written to global memory
+// by the pre-pass (else every CTA builds it in shared memory).
+template <int D, bool kGlobalPlan>
 __global__ void __launch_bounds__(kBThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -278,24 +281,30 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint8_t *smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
-    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
-    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, key tile): visible query tiles
-    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
+    int2 *tab_s = reinterpret_cast<int2 *>(smem + K::kOffTab);
+    int *order_s = reinterpret_cast<int *>(smem + K::kOffOrder);
+    int *cost_s = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, key tile): visible query tiles
+    int *seg_s = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
-    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per rank
-    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per query tile
+    int *sorted_s = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per rank
+    uint32_t *bits_s = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per query tile
+    const int *order = kGlobalPlan ? a.gp.order : order_s;
+    const int *cost = kGlobalPlan ? a.gp.cost : cost_s;
+    const int *seg_first = kGlobalPlan ? a.gp.seg_first : seg_s;
+    const int *sorted_flag = kGlobalPlan ? a.gp.qsorted : sorted_s;
+    const uint32_t *arith_bits = kGlobalPlan ? a.gp.qbits : bits_s;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
     uint64_t *kv_full = bar, *kv_empty = bar + 1, *qd_full = bar + 2, *qd_empty = bar + 2 + kBStages;
     uint64_t *s_full = bar + 2 + 2 * kBStages, *p_half = s_full + 1, *p_full = s_full + 2, *o_full = s_full + 3,
              *o_empty = s_full + 4, *drain = s_full + 5;
-    const int2 *ktab = tab;                 // [kpr][nk] key tiles
-    const int2 *qtab = tab + a.kpr * a.nk;  // [C][nq] query tiles
+    const int2 *ktab = kGlobalPlan ? a.gp.ktab : tab_s;                // [kpr][nk] key tiles
+    const int2 *qtab = kGlobalPlan ? a.gp.qtab : tab_s + a.kpr * a.nk;  // [C][nq] query tiles
 
     if (tid == 0) {
         *abort_flag = 0;
-        for (int w = 0; w < kBwdMaxTables / 32; ++w) arith_bits[w] = 0u;
+        if (!kGlobalPlan)
+            for (int w = 0; w < kBwdMaxTables / 32; ++w) bits_s[w] = 0u;
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
         for (int s = 0; s < kBStages; ++s) {
@@ -321,33 +330,35 @@ __global__ void __launch_bounds__(kBThreads, 1)
         tmem_relinquish();
     }
     __syncthreads();
-    {
-        const int nkk = a.kpr * a.nk, total = nkk + a.C * a.nq;
-        for (int g = warp; g < total; g += kBThreads / 32) {
-            if (g < nkk) {
-                const int j = g / a.nk, kt = g - (g / a.nk) * a.nk;
-                tile_table(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab + g, nullptr, 0);
-            } else {
-                const int gq = g - nkk, r = gq / a.nq, qt = gq - (gq / a.nq) * a.nq;
-                tile_table(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab + g, arith_bits, gq);
+    if constexpr (!kGlobalPlan) {
+        {
+            const int nkk = a.kpr * a.nk, total = nkk + a.C * a.nq;
+            for (int g = warp; g < total; g += kBThreads / 32) {
+                if (g < nkk) {
+                    const int j = g / a.nk, kt = g - (g / a.nk) * a.nk;
+                    tile_table(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab_s + g, nullptr, 0);
+                } else {
+                    const int gq = g - nkk, r = gq / a.nq, qt = gq - (gq / a.nq) * a.nq;
+                    tile_table(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab_s + g, bits_s, gq);
+                }
             }
         }
+        __syncthreads();
+        if (tid < a.C) {
+            int ok = 1;
+            for (int qt = 1; qt < a.nq; ++qt) ok &= (qtab[tid * a.nq + qt].y >= qtab[tid * a.nq + qt - 1].y);
+            sorted_s[tid] = ok;
+        }
+        __syncthreads();
+        const int np = a.C * a.nk;
+        for (int p = tid; p < np; p += kBThreads) {
+            const int r = p / a.nk, kt = p - (p / a.nk) * a.nk;
+            const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+            cost_s[p] = count_q(qtab + r * a.nq, a.nq, ktab[owner * a.nk + kt].x, sorted_s[r] != 0);
+        }
+        __syncthreads();
+        build_segments<kBThreads>(cost_s, a.C, a.nk, a.pair != 0, order_s, seg_s);
     }
-    __syncthreads();
-    if (tid < a.C) {
-        int ok = 1;
-        for (int qt = 1; qt < a.nq; ++qt) ok &= (qtab[tid * a.nq + qt].y >= qtab[tid * a.nq + qt - 1].y);
-        sorted_flag[tid] = ok;
-    }
-    __syncthreads();
-    const int np = a.C * a.nk;
-    for (int p = tid; p < np; p += kBThreads) {
-        const int r = p / a.nk, kt = p - (p / a.nk) * a.nk;
-        const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
-        cost[p] = count_q(qtab + r * a.nq, a.nq, ktab[owner * a.nk + kt].x, sorted_flag[r] != 0);
-    }
-    __syncthreads();
-    build_segments<kBThreads>(cost, a.C, a.nk, a.pair != 0, order, seg_first);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -633,7 +644,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 // ======================================================================
 // dQ: Q-stationary
 // ======================================================================
-template <int D>
+template <int D, bool kGlobalPlan>
 __global__ void __launch_bounds__(kBThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BwdArgs a) {
@@ -642,24 +653,30 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint8_t *smem = align1024(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
-    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
-    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, query tile): visible key tiles
-    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
+    int2 *tab_s = reinterpret_cast<int2 *>(smem + K::kOffTab);
+    int *order_s = reinterpret_cast<int *>(smem + K::kOffOrder);
+    int *cost_s = reinterpret_cast<int *>(smem + K::kOffCost);  // per (rank, query tile): visible key tiles
+    int *seg_s = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
-    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per key-position rank
-    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per key tile
+    int *sorted_s = reinterpret_cast<int *>(smem + K::kOffMisc + 16);  // per key-position rank
+    uint32_t *bits_s = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);  // per key tile
+    const int *order = kGlobalPlan ? a.gp.order : order_s;
+    const int *cost = kGlobalPlan ? a.gp.cost : cost_s;
+    const int *seg_first = kGlobalPlan ? a.gp.seg_first : seg_s;
+    const int *sorted_flag = kGlobalPlan ? a.gp.ksorted : sorted_s;
+    const uint32_t *arith_bits = kGlobalPlan ? a.gp.kbits : bits_s;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
     uint64_t *qd_full = bar, *qd_empty = bar + 1, *kv_full = bar + 2, *kv_empty = bar + 2 + kBStages;
     uint64_t *s_full = bar + 2 + 2 * kBStages, *p_half = s_full + 1, *p_full = s_full + 2, *o_full = s_full + 3,
              *o_empty = s_full + 4, *drain = s_full + 5;
-    const int2 *qtab = tab;               // [C][nq] query tiles
-    const int2 *ktab = tab + a.C * a.nq;  // [kpr][nk] key tiles
+    const int2 *qtab = kGlobalPlan ? a.gp.qtab : tab_s;               // [C][nq] query tiles
+    const int2 *ktab = kGlobalPlan ? a.gp.ktab : tab_s + a.C * a.nq;  // [kpr][nk] key tiles
 
     if (tid == 0) {
         *abort_flag = 0;
-        for (int w = 0; w < kBwdMaxTables / 32; ++w) arith_bits[w] = 0u;
+        if (!kGlobalPlan)
+            for (int w = 0; w < kBwdMaxTables / 32; ++w) bits_s[w] = 0u;
         mbar_init(qd_full, 1);
         mbar_init(qd_empty, 1);
         for (int s = 0; s < kBStages; ++s) {
@@ -683,33 +700,35 @@ __global__ void __launch_bounds__(kBThreads, 1)
         tmem_relinquish();
     }
     __syncthreads();
-    {
-        const int nqq = a.C * a.nq, total = nqq + a.kpr * a.nk;
-        for (int g = warp; g < total; g += kBThreads / 32) {
-            if (g < nqq) {
-                const int r = g / a.nq, qt = g - (g / a.nq) * a.nq;
-                tile_table(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab + g, nullptr, 0);
-            } else {
-                const int gk = g - nqq, j = gk / a.nk, kt = gk - (gk / a.nk) * a.nk;
-                tile_table(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab + g, arith_bits, gk);
+    if constexpr (!kGlobalPlan) {
+        {
+            const int nqq = a.C * a.nq, total = nqq + a.kpr * a.nk;
+            for (int g = warp; g < total; g += kBThreads / 32) {
+                if (g < nqq) {
+                    const int r = g / a.nq, qt = g - (g / a.nq) * a.nq;
+                    tile_table(a.q_pos + r * a.q_pos_stride, qt * 128, a.Sq, lane, tab_s + g, nullptr, 0);
+                } else {
+                    const int gk = g - nqq, j = gk / a.nk, kt = gk - (gk / a.nk) * a.nk;
+                    tile_table(a.k_pos + j * a.k_pos_stride, kt * 128, a.Sk, lane, tab_s + g, bits_s, gk);
+                }
             }
         }
+        __syncthreads();
+        if (tid < a.kpr) {
+            int ok = 1;
+            for (int kt = 1; kt < a.nk; ++kt) ok &= (ktab[tid * a.nk + kt].x >= ktab[tid * a.nk + kt - 1].x);
+            sorted_s[tid] = ok;
+        }
+        __syncthreads();
+        const int np = a.C * a.nq;
+        for (int p = tid; p < np; p += kBThreads) {
+            const int r = p / a.nq, qt = p - (p / a.nq) * a.nq;
+            const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+            cost_s[p] = count_k(ktab + owner * a.nk, a.nk, qtab[r * a.nq + qt].y, sorted_s[owner] != 0);
+        }
+        __syncthreads();
+        build_segments<kBThreads>(cost_s, a.C, a.nq, a.pair != 0, order_s, seg_s);
     }
-    __syncthreads();
-    if (tid < a.kpr) {
-        int ok = 1;
-        for (int kt = 1; kt < a.nk; ++kt) ok &= (ktab[tid * a.nk + kt].x >= ktab[tid * a.nk + kt - 1].x);
-        sorted_flag[tid] = ok;
-    }
-    __syncthreads();
-    const int np = a.C * a.nq;
-    for (int p = tid; p < np; p += kBThreads) {
-        const int r = p / a.nq, qt = p - (p / a.nq) * a.nq;
-        const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
-        cost[p] = count_k(ktab + owner * a.nk, a.nk, qtab[r * a.nq + qt].y, sorted_flag[owner] != 0);
-    }
-    __syncthreads();
-    build_segments<kBThreads>(cost, a.C, a.nq, a.pair != 0, order, seg_first);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1031,7 +1050,33 @@ BwdArgs make_args(const BwdProblem &p, int nq, int nk, int heads_per_item) {
     return a;
 }
 
-template <int D>
+// The plans of the two backward kernels (see PlanSpec): 128-row tiles; the
+// dK/dV kernel's units are key tiles, the dQ kernel's single query tiles.
+PlanSpec bwd_plan_spec(const BwdProblem &p, bool dkdv, bool pair) {
+    PlanSpec s{};
+    s.q_pos = p.q_pos;
+    s.k_pos = p.k_pos;
+    s.q_pos_stride = p.q_pos_stride;
+    s.k_pos_stride = p.k_pos_stride;
+    s.C = p.C;
+    s.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
+    s.kpos_shift = p.kpos_shift;
+    s.Sq = static_cast<int>(p.Sq);
+    s.Sk = static_cast<int>(p.Sk);
+    s.q_tile = 128;
+    s.k_tile = 128;
+    s.unit_is_k = dkdv ? 1 : 0;
+    s.q_group = 1;
+    s.pair = pair ? 1 : 0;
+    return s;
+}
+
+bool bwd_plan_on_chip(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk) {
+    const int64_t q128 = (Sq + 127) / 128, k128 = (Sk + 127) / 128;
+    return kpr * k128 + C * q128 <= kBwdMaxTables && C * k128 <= kBwdMaxPairs && C * q128 <= kBwdMaxPairs;
+}
+
+template <int D, bool kGP>
 cp_status launch_dkdv_typed(const BwdProblem &p, cudaStream_t stream) {
     using K = CfgKV<D>;
     CUtensorMap mq, mdo, mk, mv, mnl, mnd;
@@ -1047,18 +1092,24 @@ cp_status launch_dkdv_typed(const BwdProblem &p, cudaStream_t stream) {
     a.pair = pair_units(nk, p.C, p.B * p.Nkv, sm_count()) ? 1 : 0;
     a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(nk, a.pair != 0)));
     const long long n_items = static_cast<long long>(p.C) * super_count(nk, a.pair != 0) * p.B * p.Nkv;
+    a.gp = PlanPtrs{};
+    if (kGP) {
+        const cp_status st = launch_plan(bwd_plan_spec(p, true, a.pair != 0), p.plan, &a.gp, stream);
+        if (st != CP_OK) return st;
+    }
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes);
+        attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kGP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        K::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return cuda_status(attr_err);
     const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
-    bwd_dkdv_kernel<D><<<grid, kBThreads, K::kSmemBytes, stream>>>(mq, mdo, mk, mv, mnl, mnd, a);
+    bwd_dkdv_kernel<D, kGP><<<grid, kBThreads, K::kSmemBytes, stream>>>(mq, mdo, mk, mv, mnl, mnd, a);
     return last_launch_status();
 }
 
-template <int D>
+template <int D, bool kGP>
 cp_status launch_dq_typed(const BwdProblem &p, cudaStream_t stream) {
     using K = CfgQ<D>;
     CUtensorMap mq, mdo, mk, mv;
@@ -1072,14 +1123,20 @@ cp_status launch_dq_typed(const BwdProblem &p, cudaStream_t stream) {
     a.pair = pair_units(nq, p.C, p.B * p.N, sm_count()) ? 1 : 0;
     a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(nq, a.pair != 0)));
     const long long n_items = static_cast<long long>(p.C) * super_count(nq, a.pair != 0) * p.B * p.N;
+    a.gp = PlanPtrs{};
+    if (kGP) {
+        const cp_status st = launch_plan(bwd_plan_spec(p, false, a.pair != 0), p.plan, &a.gp, stream);
+        if (st != CP_OK) return st;
+    }
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes);
+        attr_err = cudaFuncSetAttribute(bwd_dq_kernel<D, kGP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        K::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return cuda_status(attr_err);
     const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
-    bwd_dq_kernel<D><<<grid, kBThreads, K::kSmemBytes, stream>>>(mq, mdo, mk, mv, a);
+    bwd_dq_kernel<D, kGP><<<grid, kBThreads, K::kSmemBytes, stream>>>(mq, mdo, mk, mv, a);
     return last_launch_status();
 }
 
@@ -1100,7 +1157,19 @@ cp_status launch_bwd_stats(const float *o, const void *dout, const float *lse, i
     return last_launch_status();
 }
 
-cp_status validate_bwd(const BwdProblem &p) {
+size_t bwd_plan_need(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk) {
+    if (bwd_plan_on_chip(C, kpr, Sq, Sk)) return 0;
+    BwdProblem p{};
+    p.C = static_cast<int>(C);
+    p.k_pos_stride = (kpr == 1) ? 0 : 1;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    // one buffer serves both launches in turn; unpaired units: the longer order
+    const size_t a = plan_bytes(bwd_plan_spec(p, true, false)), b = plan_bytes(bwd_plan_spec(p, false, false));
+    return a > b ? a : b;
+}
+
+cp_status validate_bwd(const BwdProblem &p, bool check_plan) {
     if (!p.q || !p.k || !p.v || !p.dout || !p.q_pos || !p.k_pos || !p.nl2 || !p.nd || !p.dq || !p.dk || !p.dv)
         return CP_ERR_NULL;
     if (p.C < 1 || p.C > kMaxC || p.B < 1 || p.N < 1 || p.Nkv < 1 || p.Sq < 1 || p.Sk < 1) return CP_ERR_SHAPE;
@@ -1117,11 +1186,13 @@ cp_status validate_bwd(const BwdProblem &p) {
     if (p.sq_pad < bwd_sq_pad(p.Sq) || p.sq_pad % 128 != 0) return CP_ERR_SHAPE;
     const int64_t kpr = (p.k_pos_stride == 0) ? 1 : p.C;
     const int64_t q128 = (p.Sq + 127) / 128, k128 = (p.Sk + 127) / 128;
-    if (kpr * k128 + p.C * q128 > kBwdMaxTables) return CP_ERR_SHAPE;
-    if (p.C * k128 > kBwdMaxPairs || p.C * q128 > kBwdMaxPairs) return CP_ERR_SHAPE;
     if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || p.C * k128 * p.B * p.Nkv > INT32_MAX ||
-        p.C * q128 * p.B * p.N > INT32_MAX)
+        p.C * q128 * p.B * p.N > INT32_MAX || kpr * k128 + p.C * q128 > INT32_MAX / 8)
         return CP_ERR_SHAPE;
+    if (check_plan && !bwd_plan_on_chip(p.C, kpr, p.Sq, p.Sk)) {
+        if (!p.plan || p.plan_bytes < bwd_plan_need(p.C, kpr, p.Sq, p.Sk)) return CP_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(p.plan) & 255u) return CP_ERR_ALIGNMENT;
+    }
     if (p.kv_shift < 0 || p.kv_shift >= p.C || p.kpos_shift < 0 || p.kpos_shift >= p.C) return CP_ERR_ARGUMENT;
     return CP_OK;
 }
@@ -1129,8 +1200,14 @@ cp_status validate_bwd(const BwdProblem &p) {
 cp_status launch_bwd(const BwdProblem &p, cudaStream_t stream) {
     cp_status st = validate_bwd(p);
     if (st != CP_OK) return st;
-    st = (p.D == 128) ? launch_dkdv_typed<128>(p, stream) : launch_dkdv_typed<64>(p, stream);
-    if (st == CP_OK) st = (p.D == 128) ? launch_dq_typed<128>(p, stream) : launch_dq_typed<64>(p, stream);
+    if (bwd_plan_on_chip(p.C, (p.k_pos_stride == 0) ? 1 : p.C, p.Sq, p.Sk)) {
+        st = (p.D == 128) ? launch_dkdv_typed<128, false>(p, stream) : launch_dkdv_typed<64, false>(p, stream);
+        if (st == CP_OK)
+            st = (p.D == 128) ? launch_dq_typed<128, false>(p, stream) : launch_dq_typed<64, false>(p, stream);
+        return st;
+    }
+    st = (p.D == 128) ? launch_dkdv_typed<128, true>(p, stream) : launch_dkdv_typed<64, true>(p, stream);
+    if (st == CP_OK) st = (p.D == 128) ? launch_dq_typed<128, true>(p, stream) : launch_dq_typed<64, true>(p, stream);
     return st;
 }
 
@@ -1149,10 +1226,19 @@ cp_status read_bwd_device_status(int *code, bool clear) {
 
 using namespace cpattn;
 
-extern "C" cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t N, size_t *bytes) {
+namespace {
+inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+// workspace: the per-row statistics (nl2, nd), then the work plans when they
+// do not fit on chip
+size_t bwd_stats_bytes(int64_t CB, int64_t N, int64_t Sq) {
+    return round256(2 * static_cast<size_t>(CB) * N * bwd_sq_pad(Sq) * sizeof(float));
+}
+}  // namespace
+
+extern "C" cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t N, size_t *bytes) {
     if (!bytes) return CP_ERR_NULL;
-    if (B < 1 || Sq < 1 || N < 1) return CP_ERR_SHAPE;
-    *bytes = 2 * static_cast<size_t>(B) * N * bwd_sq_pad(Sq) * sizeof(float);
+    if (B < 1 || Sq < 1 || Sk < 1 || N < 1) return CP_ERR_SHAPE;
+    *bytes = bwd_stats_bytes(B, N, Sq) + bwd_plan_need(1, 1, Sq, Sk);
     return CP_OK;
 }
 
@@ -1162,12 +1248,16 @@ extern "C" cp_status cp_attn_bwd_partial(const void *q, const void *k, const voi
                                          int64_t Nkv, int64_t D, float scale, float *dq, float *dk, float *dv,
                                          int accumulate, void *workspace, size_t ws_bytes, cudaStream_t stream) {
     if (!o || !lse) return CP_ERR_NULL;
-    if (B < 1 || Sq < 1 || N < 1) return CP_ERR_SHAPE;
+    if (B < 1 || Sq < 1 || Sk < 1 || N < 1) return CP_ERR_SHAPE;
     const int64_t pad = bwd_sq_pad(Sq);
-    const size_t need = 2 * static_cast<size_t>(B) * N * pad * sizeof(float);
-    if (!workspace || ws_bytes < need) return CP_ERR_WORKSPACE;
+    const size_t stats = bwd_stats_bytes(B, N, Sq), plan_need = bwd_plan_need(1, 1, Sq, Sk);
+    if (!workspace || ws_bytes < stats + plan_need) return CP_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return CP_ERR_ALIGNMENT;
     BwdProblem p{};
+    if (plan_need) {
+        p.plan = static_cast<uint8_t *>(workspace) + stats;
+        p.plan_bytes = plan_need;
+    }
     p.q = q;
     p.k = k;
     p.v = v;
@@ -1203,7 +1293,7 @@ extern "C" cp_status cp_ring_bwd_workspace_size(int64_t B, int64_t S, int64_t N,
     if (!bytes) return CP_ERR_NULL;
     if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1) return CP_ERR_SHAPE;
     if (S % C != 0) return CP_ERR_DIVISIBILITY;
-    *bytes = 2 * static_cast<size_t>(C) * B * N * bwd_sq_pad(S / C) * sizeof(float);
+    *bytes = bwd_stats_bytes(static_cast<int64_t>(C) * B, N, S / C) + bwd_plan_need(C, C, S / C, S / C);
     return CP_OK;
 }
 
@@ -1217,10 +1307,14 @@ extern "C" cp_status cp_ring_attention_bwd(const void *q_sh, const void *k_sh, c
     if (C < 1 || C > kMaxC || B < 1 || S < 1 || N < 1 || Nkv < 1) return CP_ERR_SHAPE;
     if (layout == CP_ZIGZAG ? (S % (2LL * C) != 0) : (S % C != 0)) return CP_ERR_DIVISIBILITY;
     const int64_t s = S / C, pad = bwd_sq_pad(s);
-    const size_t need = 2 * static_cast<size_t>(C) * B * N * pad * sizeof(float);
-    if (!workspace || ws_bytes < need) return CP_ERR_WORKSPACE;
+    const size_t stats = bwd_stats_bytes(static_cast<int64_t>(C) * B, N, s), plan_need = bwd_plan_need(C, C, s, s);
+    if (!workspace || ws_bytes < stats + plan_need) return CP_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return CP_ERR_ALIGNMENT;
     BwdProblem p{};
+    if (plan_need) {
+        p.plan = static_cast<uint8_t *>(workspace) + stats;
+        p.plan_bytes = plan_need;
+    }
     p.q = q_sh;
     p.k = k_sh;
     p.v = v_sh;

@@ -82,6 +82,7 @@ struct TArgs {
     unsigned long long timeout_ns;
     int pair;  // a super-block holds query tiles u and nqt-1-u (else u alone)
     FastDiv div_nsp, div_n;
+    PlanPtrs gp;  // the launch's plan in global memory (kernels with kGlobalPlan)
 };
 
 // kind::tf32 instruction descriptor: D fp32 (bits 4-5 = 1), A and B tf32
@@ -134,7 +135,9 @@ __device__ __forceinline__ void tile_minmax(const int32_t *p, int row0, int rows
     }
 }
 
-template <int D>
+// kGlobalPlan: the plan was written to global memory by the pre-pass (else
+// every CTA builds it in shared memory).
+template <int D, bool kGlobalPlan>
 __global__ void __launch_bounds__(kTThreads, 1)
     attn_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmVt, const TArgs a) {
@@ -142,25 +145,31 @@ __global__ void __launch_bounds__(kTThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int2 *tab = reinterpret_cast<int2 *>(smem + K::kOffTab);
-    int *order = reinterpret_cast<int *>(smem + K::kOffOrder);
-    int *cost = reinterpret_cast<int *>(smem + K::kOffCost);
-    int *seg_first = reinterpret_cast<int *>(smem + K::kOffSeg);
+    int2 *tab_s = reinterpret_cast<int2 *>(smem + K::kOffTab);
+    int *order_s = reinterpret_cast<int *>(smem + K::kOffOrder);
+    int *cost_s = reinterpret_cast<int *>(smem + K::kOffCost);
+    int *seg_s = reinterpret_cast<int *>(smem + K::kOffSeg);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K::kOffMisc + 4);
-    int *sorted_flag = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
-    uint32_t *arith_bits = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);
+    int *sorted_s = reinterpret_cast<int *>(smem + K::kOffMisc + 16);
+    uint32_t *bits_s = reinterpret_cast<uint32_t *>(smem + K::kOffMisc + 16 + kMaxC * 4);
+    const int *order = kGlobalPlan ? a.gp.order : order_s;
+    const int *cost = kGlobalPlan ? a.gp.cost : cost_s;
+    const int *seg_first = kGlobalPlan ? a.gp.seg_first : seg_s;
+    const int *sorted_flag = kGlobalPlan ? a.gp.ksorted : sorted_s;
+    const uint32_t *arith_bits = kGlobalPlan ? a.gp.kbits : bits_s;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + K::kOffBar);
     uint64_t *q_full = bar, *q_empty = bar + 1, *k_full = bar + 2, *k_empty = bar + 2 + kTStages;
     uint64_t *s_full = bar + 2 + 2 * kTStages, *p_full = s_full + 2, *pv_done = s_full + 4, *o_full = s_full + 5,
              *o_empty = s_full + 6, *drain = s_full + 7;
     uint64_t *v_full = s_full + 8, *v_empty = v_full + kTStages;
-    const int2 *ktab = tab;                 // [kpr][nkt] 64-key tiles
-    const int2 *qtab = tab + a.kpr * a.nkt;  // [C][nqt] 128-row query tiles
+    const int2 *ktab = kGlobalPlan ? a.gp.ktab : tab_s;                 // [kpr][nkt] 64-key tiles
+    const int2 *qtab = kGlobalPlan ? a.gp.qtab : tab_s + a.kpr * a.nkt;  // [C][nqt] 128-row query tiles
 
     if (tid == 0) {
         *abort_flag = 0;
-        for (int w = 0; w < kMaxTables / 32; ++w) arith_bits[w] = 0u;
+        if (!kGlobalPlan)
+            for (int w = 0; w < kMaxTables / 32; ++w) bits_s[w] = 0u;
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
         for (int s = 0; s < kTStages; ++s) {
@@ -187,37 +196,39 @@ __global__ void __launch_bounds__(kTThreads, 1)
         tmem_relinquish();
     }
     __syncthreads();
-    {
-        const int nk = a.kpr * a.nkt, total = nk + a.C * a.nqt;
-        for (int g = warp; g < total; g += kTThreads / 32) {
-            if (g < nk) {
-                const int j = g / a.nkt, kt = g - (g / a.nkt) * a.nkt;
-                tile_minmax(a.k_pos + j * a.k_pos_stride, kt * 64, 64, a.Sk, lane, tab + g, arith_bits, g);
-            } else {
-                const int gq = g - nk, r = gq / a.nqt, qt = gq - (gq / a.nqt) * a.nqt;
-                tile_minmax(a.q_pos + r * a.q_pos_stride, qt * 128, 128, a.Sq, lane, tab + g, nullptr, 0);
+    if constexpr (!kGlobalPlan) {
+        {
+            const int nk = a.kpr * a.nkt, total = nk + a.C * a.nqt;
+            for (int g = warp; g < total; g += kTThreads / 32) {
+                if (g < nk) {
+                    const int j = g / a.nkt, kt = g - (g / a.nkt) * a.nkt;
+                    tile_minmax(a.k_pos + j * a.k_pos_stride, kt * 64, 64, a.Sk, lane, tab_s + g, bits_s, g);
+                } else {
+                    const int gq = g - nk, r = gq / a.nqt, qt = gq - (gq / a.nqt) * a.nqt;
+                    tile_minmax(a.q_pos + r * a.q_pos_stride, qt * 128, 128, a.Sq, lane, tab_s + g, nullptr, 0);
+                }
             }
         }
+        __syncthreads();
+        if (tid < a.kpr) {
+            int ok = 1;
+            for (int kt = 1; kt < a.nkt; ++kt) ok &= (ktab[tid * a.nkt + kt].x >= ktab[tid * a.nkt + kt - 1].x);
+            sorted_s[tid] = ok;
+        }
+        __syncthreads();
+        const int np = a.C * a.nqt;
+        for (int p = tid; p < np; p += kTThreads) {
+            const int r = p / a.nqt, qt = p - (p / a.nqt) * a.nqt;
+            const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
+            const int qmax = qtab[r * a.nqt + qt].y;
+            const int2 *kt_o = ktab + owner * a.nkt;
+            int c = 0;
+            for (int kt = 0; kt < a.nkt; ++kt) c += (kt_o[kt].x <= qmax);
+            cost_s[p] = c;
+        }
+        __syncthreads();
+        build_segments<kTThreads>(cost_s, a.C, a.nqt, a.pair != 0, order_s, seg_s);
     }
-    __syncthreads();
-    if (tid < a.kpr) {
-        int ok = 1;
-        for (int kt = 1; kt < a.nkt; ++kt) ok &= (ktab[tid * a.nkt + kt].x >= ktab[tid * a.nkt + kt - 1].x);
-        sorted_flag[tid] = ok;
-    }
-    __syncthreads();
-    const int np = a.C * a.nqt;
-    for (int p = tid; p < np; p += kTThreads) {
-        const int r = p / a.nqt, qt = p - (p / a.nqt) * a.nqt;
-        const int owner = (a.kpr == 1) ? 0 : (r + a.kpos_shift) % a.C;
-        const int qmax = qtab[r * a.nqt + qt].y;
-        const int2 *kt_o = ktab + owner * a.nkt;
-        int c = 0;
-        for (int kt = 0; kt < a.nkt; ++kt) c += (kt_o[kt].x <= qmax);
-        cost[p] = c;
-    }
-    __syncthreads();
-    build_segments<kTThreads>(cost, a.C, a.nqt, a.pair != 0, order, seg_first);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -562,7 +573,33 @@ __global__ void __launch_bounds__(256) tf32_transpose_kernel(const float *__rest
     }
 }
 
-template <int D>
+// The plan of a tf32 launch (see PlanSpec): 128-row query tiles, 64-key
+// tiles, one query tile per cost unit.
+PlanSpec tf32_plan_spec(const AttnProblem &p, bool pair) {
+    PlanSpec s{};
+    s.q_pos = p.q_pos;
+    s.k_pos = p.k_pos;
+    s.q_pos_stride = p.q_pos_stride;
+    s.k_pos_stride = p.k_pos_stride;
+    s.C = p.C;
+    s.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
+    s.kpos_shift = p.kpos_shift;
+    s.Sq = static_cast<int>(p.Sq);
+    s.Sk = static_cast<int>(p.Sk);
+    s.q_tile = 128;
+    s.k_tile = 64;
+    s.unit_is_k = 0;
+    s.q_group = 1;
+    s.pair = pair ? 1 : 0;
+    return s;
+}
+
+bool tf32_plan_on_chip(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk) {
+    const int64_t nqt = (Sq + 127) / 128, nkt = (Sk + 63) / 64;
+    return kpr * nkt + C * nqt <= kMaxTables && C * nqt <= kMaxPairs;
+}
+
+template <int D, bool kGP>
 cp_status launch_tf32_typed(const AttnProblem &p, const float *vt, int64_t sk_pad, cudaStream_t stream) {
     using K = CfgT<D>;
     CUtensorMap mq, mk, mv;
@@ -599,20 +636,36 @@ cp_status launch_tf32_typed(const AttnProblem &p, const float *vt, int64_t sk_pa
     a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(a.nqt, a.pair != 0)));
     a.div_n = make_fastdiv(static_cast<uint32_t>(a.N));
     const long long n_items = static_cast<long long>(p.C) * super_count(a.nqt, a.pair != 0) * p.B * p.N;
+    a.gp = PlanPtrs{};
+    if (kGP) {
+        const cp_status st = launch_plan(tf32_plan_spec(p, a.pair != 0), p.plan, &a.gp, stream);
+        if (st != CP_OK) return st;
+    }
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_tf32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes);
+        attr_err = cudaFuncSetAttribute(attn_tf32_kernel<D, kGP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        K::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return cuda_status(attr_err);
     const int grid = static_cast<int>(n_items < sm_count() ? n_items : sm_count());
-    attn_tf32_kernel<D><<<grid, kTThreads, K::kSmemBytes, stream>>>(mq, mk, mv, a);
+    attn_tf32_kernel<D, kGP><<<grid, kTThreads, K::kSmemBytes, stream>>>(mq, mk, mv, a);
     return last_launch_status();
 }
 
 }  // namespace
 
-cp_status validate_attn_tf32(const AttnProblem &p) {
+size_t tf32_plan_need(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk) {
+    if (tf32_plan_on_chip(C, kpr, Sq, Sk)) return 0;
+    AttnProblem p{};
+    p.C = static_cast<int>(C);
+    p.k_pos_stride = (kpr == 1) ? 0 : 1;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    return plan_bytes(tf32_plan_spec(p, false));  // unpaired: the longer order
+}
+
+cp_status validate_attn_tf32(const AttnProblem &p, bool check_plan) {
     if (!p.q || !p.k || !p.v || !p.q_pos || !p.k_pos || !p.o || !p.lse) return CP_ERR_NULL;
     if (p.C < 1 || p.C > kMaxC || p.B < 1 || p.N < 1 || p.Nkv < 1 || p.Sq < 1 || p.Sk < 1) return CP_ERR_SHAPE;
     if (p.D != 64 && p.D != 128) return CP_ERR_UNSUPPORTED;
@@ -625,9 +678,13 @@ cp_status validate_attn_tf32(const AttnProblem &p) {
     if (reinterpret_cast<uintptr_t>(p.o) & 31u) return CP_ERR_ALIGNMENT;
     const int64_t nqt = (p.Sq + 127) / 128, nkt = (p.Sk + 63) / 64;
     const int64_t kpr = (p.k_pos_stride == 0) ? 1 : p.C;
-    if (kpr * nkt + p.C * nqt > kMaxTables || p.C * nqt > kMaxPairs) return CP_ERR_SHAPE;
-    if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || static_cast<int64_t>(p.C) * nqt * p.B * p.N > INT32_MAX)
+    if (p.Sq > INT32_MAX / 2 || p.Sk > INT32_MAX / 2 || static_cast<int64_t>(p.C) * nqt * p.B * p.N > INT32_MAX ||
+        kpr * nkt + p.C * nqt > INT32_MAX / 8)
         return CP_ERR_SHAPE;
+    if (check_plan && !tf32_plan_on_chip(p.C, kpr, p.Sq, p.Sk)) {
+        if (!p.plan || p.plan_bytes < tf32_plan_need(p.C, kpr, p.Sq, p.Sk)) return CP_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(p.plan) & 255u) return CP_ERR_ALIGNMENT;
+    }
     if (p.kv_shift < 0 || p.kv_shift >= p.C || p.kpos_shift < 0 || p.kpos_shift >= p.C) return CP_ERR_ARGUMENT;
     return CP_OK;
 }
@@ -654,7 +711,10 @@ cp_status launch_attn_tf32(const AttnProblem &p, const float *vt, cudaStream_t s
     if (st != CP_OK) return st;
     if (!vt || !aligned16(vt)) return CP_ERR_ALIGNMENT;
     const int64_t pad = tf32_vt_pad(p.Sk);
-    return p.D == 128 ? launch_tf32_typed<128>(p, vt, pad, stream) : launch_tf32_typed<64>(p, vt, pad, stream);
+    if (tf32_plan_on_chip(p.C, (p.k_pos_stride == 0) ? 1 : p.C, p.Sq, p.Sk))
+        return p.D == 128 ? launch_tf32_typed<128, false>(p, vt, pad, stream)
+                          : launch_tf32_typed<64, false>(p, vt, pad, stream);
+    return p.D == 128 ? launch_tf32_typed<128, true>(p, vt, pad, stream) : launch_tf32_typed<64, true>(p, vt, pad, stream);
 }
 
 cp_status read_tf32_device_status(int *code, bool clear) {
@@ -670,10 +730,15 @@ cp_status read_tf32_device_status(int *code, bool clear) {
 
 }  // namespace cpattn
 
-extern "C" cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sk, int64_t Nkv, int64_t D, size_t *bytes) {
+namespace {
+inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+}  // namespace
+
+extern "C" cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t Nkv, int64_t D,
+                                                size_t *bytes) {
     if (!bytes) return CP_ERR_NULL;
-    if (B < 1 || Sk < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
-    *bytes = cpattn::tf32_vt_bytes(B, Sk, Nkv, D);
+    if (B < 1 || Sq < 1 || Sk < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
+    *bytes = round256(cpattn::tf32_vt_bytes(B, Sk, Nkv, D)) + cpattn::tf32_plan_need(1, 1, Sq, Sk);
     return CP_OK;
 }
 
@@ -697,11 +762,18 @@ extern "C" cp_status cp_attn_partial_f32(const float *q, const float *k, const f
     p.Sq = Sq;
     p.Sk = Sk;
     p.scale = scale;
-    cp_status st = cpattn::validate_attn_tf32(p);
+    cp_status st = cpattn::validate_attn_tf32(p, false);
     if (st != CP_OK) return st;
-    if (!workspace || ws_bytes < cpattn::tf32_vt_bytes(B, Sk, Nkv, D)) return CP_ERR_WORKSPACE;
+    // workspace: v transposed, then the work plan when it does not fit on chip
+    const size_t vt_bytes = round256(cpattn::tf32_vt_bytes(B, Sk, Nkv, D));
+    const size_t plan_need = cpattn::tf32_plan_need(1, 1, Sq, Sk);
+    if (!workspace || ws_bytes < vt_bytes + plan_need) return CP_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return CP_ERR_ALIGNMENT;
     float *vt = static_cast<float *>(workspace);
+    if (plan_need) {
+        p.plan = static_cast<uint8_t *>(workspace) + vt_bytes;
+        p.plan_bytes = plan_need;
+    }
     st = cpattn::launch_tf32_transpose(v, vt, B, Sk, Nkv, D, stream);
     if (st == CP_OK) st = cpattn::launch_attn_tf32(p, vt, stream);
     return st;

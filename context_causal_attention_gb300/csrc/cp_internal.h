@@ -60,10 +60,56 @@ struct AttnProblem {
     // to become non-zero; every bounded wait uses timeout_ns (0: 2 s)
     const int *hold = nullptr;
     unsigned long long timeout_ns = 0;
+    // device buffer for the launch's work plan when it does not fit in shared
+    // memory (attn_plan_need bytes, 256-byte aligned); unused otherwise
+    void *plan = nullptr;
+    size_t plan_bytes = 0;
 };
 
-// Host validation shared by cp_attn_partial and the ring.
-cp_status validate_attn(const AttnProblem &p);
+// ------------------------------------------------------------ work plans
+// A persistent attention kernel starts from a plan of its launch: the
+// (min, max) position of every query and key tile, a bit per tile saying its
+// positions are consecutive, a "sorted" flag per rank (tile minima (K) or
+// maxima (Q) non-decreasing), the streamed-tile count of every (rank,
+// stationary unit), and the longest-first order of super-blocks cut into
+// segments (cp_sched.cuh).  When the plan fits in shared memory every CTA
+// builds it there; otherwise a pre-pass (launch_plan) writes it into the
+// caller's workspace and the kernel reads it from global memory.
+struct PlanPtrs {
+    const int2 *ktab, *qtab;         // [kpr][nkt], [C][nqt]
+    const uint32_t *kbits, *qbits;   // consecutive-positions bits of K / Q tiles
+    const int *ksorted, *qsorted;    // [kpr] (K minima non-decreasing), [C] (Q maxima)
+    const int *cost;                 // [C][nunits]
+    const int *order, *seg_first;    // [C*nsp], [C*nsp + 1]
+};
+
+// What the plan of one launch covers.  Units: groups of `q_group` query tiles
+// (cost = key tiles of the owner with min position <= the group's max query
+// position), or with unit_is_k the key tiles of the owner (cost = query tiles
+// of the rank with max position >= the tile's min key position).
+struct PlanSpec {
+    const int32_t *q_pos, *k_pos;
+    long long q_pos_stride, k_pos_stride;
+    int C, kpr, kpos_shift;
+    int Sq, Sk;
+    int q_tile, k_tile;  // rows per table entry (128; key tiles 128 or 64)
+    int unit_is_k, q_group, pair;
+};
+
+// Bytes of the global plan of `s` (256-byte multiple).
+size_t plan_bytes(const PlanSpec &s);
+// Enqueue the plan pre-pass into buf (>= plan_bytes(s), 256-byte aligned);
+// *out receives the device pointers the kernel reads.
+cp_status launch_plan(const PlanSpec &s, void *buf, PlanPtrs *out, cudaStream_t stream);
+
+// Bytes of plan buffer the forward kernel needs for C query ranks of Sq rows
+// against kpr key-position ranks of Sk rows (0 when the plan fits on chip).
+size_t attn_plan_need(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk);
+
+// Host validation shared by cp_attn_partial and the ring.  With check_plan,
+// a problem whose plan does not fit on chip must come with a plan buffer
+// (else CP_ERR_WORKSPACE).
+cp_status validate_attn(const AttnProblem &p, bool check_plan = true);
 // Validate then enqueue the attention kernel on `stream`.
 cp_status launch_attn(const AttnProblem &p, cudaStream_t stream);
 
@@ -100,7 +146,9 @@ bool make_map_f32_4d(CUtensorMap *map, const float *base, int64_t d0, int64_t d1
 // ------------------------------------------------------------ tf32 path
 // The attention of launch_attn for fp32 q, k, v (tensor cores in tf32); vt is
 // v transposed by launch_tf32_transpose ([outer][Nkv][D][tf32_vt_pad(Sk)]).
-cp_status validate_attn_tf32(const AttnProblem &p);
+cp_status validate_attn_tf32(const AttnProblem &p, bool check_plan = true);
+// Plan bytes of the tf32 kernel (as attn_plan_need; 64-key tiles).
+size_t tf32_plan_need(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk);
 cp_status launch_attn_tf32(const AttnProblem &p, const float *vt, cudaStream_t stream);
 int64_t tf32_vt_pad(int64_t Sk);
 size_t tf32_vt_bytes(int64_t outer, int64_t Sk, int64_t Nkv, int64_t D);
@@ -131,6 +179,11 @@ struct BwdProblem {
     int kv_shift, kpos_shift;
     bool accumulate;
     float scale;
+    // device buffer for the work plans when they do not fit in shared memory
+    // (bwd_plan_need bytes, 256-byte aligned; the dK/dV and dQ launches use it
+    // one after the other); unused otherwise
+    void *plan = nullptr;
+    size_t plan_bytes = 0;
 };
 // Rows of the per-row statistics (a multiple of 128 >= Sq).
 inline int64_t bwd_sq_pad(int64_t Sq) { return (Sq + 127) / 128 * 128; }
@@ -138,7 +191,10 @@ inline int64_t bwd_sq_pad(int64_t Sq) { return (Sq + 127) / 128 * 128; }
 // nd[r][i] = -<dO_i, o_i> (0 for i >= Sq), rows r over C*B*N.
 cp_status launch_bwd_stats(const float *o, const void *dout, const float *lse, int64_t CB, int64_t Sq, int64_t N,
                            int64_t D, int64_t sq_pad, float *nl2, float *nd, cudaStream_t stream);
-cp_status validate_bwd(const BwdProblem &p);
+cp_status validate_bwd(const BwdProblem &p, bool check_plan = true);
+// Plan bytes of the two backward kernels for C query ranks of Sq rows against
+// kpr key-position ranks of Sk rows (0 when both plans fit on chip).
+size_t bwd_plan_need(int64_t C, int64_t kpr, int64_t Sq, int64_t Sk);
 // dK / dV launch then dQ launch (both validated first).
 cp_status launch_bwd(const BwdProblem &p, cudaStream_t stream);
 // Sticky device status word of the backward kernels (read and optionally cleared).

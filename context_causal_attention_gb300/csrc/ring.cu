@@ -37,7 +37,8 @@ constexpr size_t kAlign = 256;
 inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t o_tile = 0, lse_tile = 0, o_acc = 0, kv = 0, vt = 0, total = 0;
+    size_t o_tile = 0, lse_tile = 0, o_acc = 0, kv = 0, vt = 0, plan = 0, total = 0;
+    size_t plan_bytes = 0;  // the attention launches' work plan (0: it fits on chip)
     size_t o_tile_bytes = 0, lse_bytes = 0, o_acc_bytes = 0, kv_bytes = 0;  // kv: one K (or V) rotation
 };
 
@@ -60,6 +61,10 @@ Layout ws_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
     off += 4 * round_up(L.kv_bytes);  // 2 buffers x (K, V)
     L.vt = off;
     if (flags & CP_RING_TF32) off += round_up(tf32_vt_bytes(static_cast<int64_t>(C) * B, s, Nkv, D));
+    // one plan buffer, rebuilt by each step's attention launch in stream order
+    L.plan_bytes = (flags & CP_RING_TF32) ? tf32_plan_need(C, C, s, s) : attn_plan_need(C, C, s, s);
+    L.plan = off;
+    off += round_up(L.plan_bytes);
     L.total = off;
     return L;
 }
@@ -157,7 +162,7 @@ cp_status ring_check_args(const void *q_sh, const void *k_sh, const void *v_sh, 
     chk.Sq = S / C;
     chk.Sk = S / C;
     chk.scale = scale;
-    return tf32 ? validate_attn_tf32(chk) : validate_attn(chk);
+    return tf32 ? validate_attn_tf32(chk, false) : validate_attn(chk, false);
 }
 
 namespace {
@@ -201,6 +206,10 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
     p.Sq = s;
     p.Sk = s;
     p.scale = scale;
+    if (L.plan_bytes) {
+        p.plan = ws + L.plan;
+        p.plan_bytes = L.plan_bytes;
+    }
     // validate everything once before enqueuing any work
     {
         AttnProblem chk = p;

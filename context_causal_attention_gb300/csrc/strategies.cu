@@ -39,15 +39,18 @@ constexpr size_t kAlign = 256;
 inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct AgLayout {
-    size_t k = 0, v = 0, pos = 0, total = 0;
+    size_t k = 0, v = 0, pos = 0, plan = 0, plan_bytes = 0, total = 0;
 };
-AgLayout ag_layout(int64_t B, int64_t S, int64_t Nkv, int64_t D) {
+AgLayout ag_layout(int64_t B, int64_t S, int64_t Nkv, int64_t D, int C) {
     AgLayout L;
     const size_t kv = static_cast<size_t>(B) * S * Nkv * D * 2;
     L.k = 0;
     L.v = round_up(kv);
     L.pos = 2 * round_up(kv);
-    L.total = L.pos + round_up(static_cast<size_t>(S) * 4);
+    L.plan = L.pos + round_up(static_cast<size_t>(S) * 4);
+    // C query ranks of S/C rows against the one shared key sequence
+    L.plan_bytes = (C >= 1 && S % C == 0) ? attn_plan_need(C, 1, S / C, S) : 0;
+    L.total = L.plan + round_up(L.plan_bytes);
     return L;
 }
 
@@ -69,7 +72,7 @@ MeshLayout mesh_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, 
 }
 
 struct UlLayout {
-    size_t q = 0, k = 0, v = 0, o = 0, pos = 0, total = 0;
+    size_t q = 0, k = 0, v = 0, o = 0, pos = 0, plan = 0, plan_bytes = 0, total = 0;
 };
 UlLayout ul_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D) {
     UlLayout L;
@@ -79,7 +82,9 @@ UlLayout ul_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D) {
     L.v = L.k + round_up(kvb);
     L.o = L.v + round_up(kvb);
     L.pos = L.o + round_up(static_cast<size_t>(B) * S * N * D * 4);
-    L.total = L.pos + round_up(static_cast<size_t>(S) * 4);
+    L.plan = L.pos + round_up(static_cast<size_t>(S) * 4);
+    L.plan_bytes = attn_plan_need(1, 1, S, S);  // head groups folded into the batch: one rank
+    L.total = L.plan + round_up(L.plan_bytes);
     return L;
 }
 
@@ -101,7 +106,7 @@ extern "C" cp_status cp_allgather_workspace_size(int64_t B, int64_t S, int64_t N
                                                  size_t *bytes) {
     if (!bytes) return CP_ERR_NULL;
     if (C < 1 || B < 1 || S < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
-    *bytes = ag_layout(B, S, Nkv, D).total;
+    *bytes = ag_layout(B, S, Nkv, D, C).total;
     return CP_OK;
 }
 
@@ -113,7 +118,7 @@ extern "C" cp_status cp_allgather_attention_fwd(const void *q_sh, const void *k_
     if (!q_sh || !k_sh || !v_sh || !pos || !o_sh || !lse_sh) return CP_ERR_NULL;
     cp_status st = check_common(B, S, N, Nkv, D, C, layout);
     if (st != CP_OK) return st;
-    const AgLayout L = ag_layout(B, S, Nkv, D);
+    const AgLayout L = ag_layout(B, S, Nkv, D, C);
     if (!workspace || ws_bytes < L.total) return CP_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return CP_ERR_ALIGNMENT;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -139,6 +144,10 @@ extern "C" cp_status cp_allgather_attention_fwd(const void *q_sh, const void *k_
     p.Sq = s;
     p.Sk = S;
     p.scale = scale;
+    if (L.plan_bytes) {
+        p.plan = ws + L.plan;
+        p.plan_bytes = L.plan_bytes;
+    }
     st = validate_attn(p);  // everything checked before anything is enqueued
     if (st != CP_OK) return st;
     st = cp_zigzag_unshard(k_sh, k_full, B, S, Nkv, D, C, CP_BF16, layout, stream);
@@ -191,6 +200,10 @@ extern "C" cp_status cp_ulysses_attention_fwd(const void *q_sh, const void *k_sh
     p.Sq = S;
     p.Sk = S;
     p.scale = scale;
+    if (L.plan_bytes) {
+        p.plan = ws + L.plan;
+        p.plan_bytes = L.plan_bytes;
+    }
     st = validate_attn(p);
     if (st != CP_OK) return st;
     st = cp_ulysses_relayout(q_sh, q_h, B, S, N, D, C, CP_BF16, CP_SEQ_TO_HEAD, order, stream);
@@ -255,7 +268,7 @@ extern "C" cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, c
         p.Sq = sg;
         p.Sk = sg;
         p.scale = scale;
-        st = validate_attn(p);
+        st = validate_attn(p, false);  // the ring's workspace (inside this one) holds its plan
         if (st != CP_OK) return st;
         if (flags & ~(CP_RING_PREFETCH | CP_RING_FUSED_MERGE)) return CP_ERR_ARGUMENT;
     }

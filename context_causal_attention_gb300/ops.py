@@ -15,6 +15,7 @@ from ._lib import (CP_BF16, CP_CONTIGUOUS, CP_F32, CP_GLOBAL_ORDER, CP_HEAD_TO_S
 
 __all__ = [
     "cp_zigzag_shard", "cp_zigzag_unshard", "cp_zigzag_positions", "cp_ulysses_relayout", "cp_attn_partial",
+    "cp_attn_workspace_size",
     "cp_lse_merge", "cp_ring_workspace_size", "cp_ring_attention_fwd", "cp_ring_attention_fwd_noalloc",
     "cp_allgather_attention_fwd", "cp_ulysses_attention_fwd",
     "cp_device_status", "cp_version",
@@ -116,8 +117,16 @@ def cp_ulysses_relayout(x, C, direction=CP_SEQ_TO_HEAD, order=CP_RANK_ORDER, out
     return out
 
 
-def cp_attn_partial(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, stream=None):
-    """Partial causal attention -> (o fp32 [B,Sq,N,D], lse fp32 [B,N,Sq])."""
+def cp_attn_workspace_size(B, Sq, Sk, N, Nkv, D):
+    n = ctypes.c_size_t(0)
+    _lib.check("cp_attn_workspace_size", _lib.lib().cp_attn_workspace_size(B, Sq, Sk, N, Nkv, D, ctypes.byref(n)))
+    return n.value
+
+
+def cp_attn_partial(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, workspace=None, stream=None):
+    """Partial causal attention -> (o fp32 [B,Sq,N,D], lse fp32 [B,N,Sq]).  Long
+    sequences whose work plan does not fit on chip go through cp_attn_partial_ws
+    with a workspace (allocated here unless given)."""
     B, Sq, N, D = q.shape
     Sk, Nkv = k.shape[1], k.shape[2]
     if scale is None:
@@ -126,9 +135,19 @@ def cp_attn_partial(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, stream=
         o = torch.empty((B, Sq, N, D), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, N, Sq), dtype=torch.float32, device=q.device)
-    st = _lib.lib().cp_attn_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D,
-                                    float(scale), _ptr(o), _ptr(lse), _stream(stream))
-    _lib.check("cp_attn_partial", st)
+    L = _lib.lib()
+    need = cp_attn_workspace_size(B, Sq, Sk, N, Nkv, D)
+    if need == 0 and workspace is None:
+        st = L.cp_attn_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D, float(scale),
+                               _ptr(o), _ptr(lse), _stream(stream))
+        _lib.check("cp_attn_partial", st)
+        return o, lse
+    if workspace is None:
+        workspace = torch.empty(max(256, need), dtype=torch.uint8, device=q.device)
+    st = L.cp_attn_partial_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D, float(scale),
+                              _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream))
+    _lib.check("cp_attn_partial_ws", st)
     return o, lse
 
 
@@ -145,7 +164,7 @@ def cp_attn_partial_f32(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, wor
         lse = torch.empty((B, N, Sq), dtype=torch.float32, device=dev)
     L = _lib.lib()
     n = ctypes.c_size_t(0)
-    _lib.check("cp_attn_f32_workspace_size", L.cp_attn_f32_workspace_size(B, Sk, Nkv, D, ctypes.byref(n)))
+    _lib.check("cp_attn_f32_workspace_size", L.cp_attn_f32_workspace_size(B, Sq, Sk, Nkv, D, ctypes.byref(n)))
     if workspace is None:
         workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
     st = L.cp_attn_partial_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D, float(scale),
@@ -311,7 +330,7 @@ def cp_attn_bwd_partial(q, k, v, o, dout, lse, q_pos, k_pos, scale=None, dq=None
     dv = torch.empty((B, Sk, Nkv, D), dtype=torch.float32, device=dev) if dv is None else dv
     L = _lib.lib()
     n = ctypes.c_size_t(0)
-    _lib.check("cp_attn_bwd_workspace_size", L.cp_attn_bwd_workspace_size(B, Sq, N, ctypes.byref(n)))
+    _lib.check("cp_attn_bwd_workspace_size", L.cp_attn_bwd_workspace_size(B, Sq, Sk, N, ctypes.byref(n)))
     if workspace is None:
         workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
     st = L.cp_attn_bwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(q_pos), _ptr(k_pos), B,

@@ -60,6 +60,10 @@ WORKLOADS = {
     "s4k": Workload("s4k", B=2, S=4096, N=16, Nkv=16, D=64, C=4, relayout=True),
     "s32k": Workload("s32k", B=1, S=32768, N=32, Nkv=32, D=128, C=4, rope=True),
     "s128k": Workload("s128k", B=1, S=131072, N=8, Nkv=8, D=128, C=8),
+    # the >= 256K regime "On Context Parallelism" (Results and Conclusion)
+    # reports on, with the S=131072 workload's heads and head size
+    "s256k": Workload("s256k", B=1, S=262144, N=8, Nkv=8, D=128, C=8),
+    "s256k_c16": Workload("s256k_c16", B=1, S=262144, N=8, Nkv=8, D=128, C=16),
 }
 
 

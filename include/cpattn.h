@@ -149,9 +149,15 @@ cp_status cp_ulysses_relayout(const void *in, void *out, int64_t B, int64_t S, i
  *   q_pos  : device int32 [Sq];  k_pos : device int32 [Sk] (any values)
  *   o      : device fp32 [B][Sq][N][D], written; 32-byte aligned
  *   lse    : device fp32 [B][N][Sq], written (natural log)
- * Requires D in {64, 128}, N % Nkv == 0, scale finite and > 0,
- * ceil(Sq/128) + ceil(Sk/128) <= 2048.  Runs on the tensor cores
- * (bf16 products, fp32 accumulation and softmax).
+ * Requires D in {64, 128}, N % Nkv == 0, scale finite and > 0.  Runs on the
+ * tensor cores (bf16 products, fp32 accumulation and softmax).
+ * Work plan: the kernel starts from a plan of its launch (per-tile position
+ * ranges, per-block tile counts, the order of work items).  It is built in
+ * shared memory when ceil(Sq/128) + ceil(Sk/128) <= 2048 and
+ * ceil(Sq/256) <= 1024; beyond that it is built in device memory the caller
+ * provides: call cp_attn_partial_ws with a workspace of
+ * cp_attn_workspace_size bytes (cp_attn_partial then returns
+ * CP_ERR_WORKSPACE).
  */
 cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int32_t *q_pos,
                           const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,
@@ -159,16 +165,33 @@ cp_status cp_attn_partial(const void *q, const void *k, const void *v, const int
                           cudaStream_t stream);
 
 /*
+ * cp_attn_workspace_size / cp_attn_partial_ws -- cp_attn_partial with a
+ * caller workspace for the work plan, for any sequence length.
+ *   *bytes receives the workspace size for these sizes (0 when the plan fits
+ *   in shared memory; then workspace may be NULL).  Host only.
+ *   workspace : device, >= cp_attn_workspace_size bytes, 256-byte aligned;
+ *               overwritten by the call (stream-ordered), not read back.
+ * Everything else as cp_attn_partial.
+ */
+cp_status cp_attn_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv, int64_t D,
+                                 size_t *bytes);
+cp_status cp_attn_partial_ws(const void *q, const void *k, const void *v, const int32_t *q_pos,
+                             const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N,
+                             int64_t Nkv, int64_t D, float scale, float *o, float *lse, void *workspace,
+                             size_t ws_bytes, cudaStream_t stream);
+
+/*
  * cp_attn_f32_workspace_size / cp_attn_partial_f32 -- cp_attn_partial for fp32
  * inputs with the tensor cores in tf32 (tcgen05.mma kind::tf32: operands
  * rounded to a 10-bit mantissa, fp32 accumulation; P enters P V as tf32 too).
  * Same arguments, result and conventions as cp_attn_partial except:
  *   q : device fp32 [B][Sq][N][D]; k, v : device fp32 [B][Sk][Nkv][D]
- *   workspace : device, >= cp_attn_f32_workspace_size(B, Sk, Nkv, D) bytes,
- *               256-byte aligned (holds v transposed for the K-major operand)
- * Limits: ceil(Sk/64) + ceil(Sq/128) <= 2048 (else CP_ERR_SHAPE).
+ *   workspace : device, >= cp_attn_f32_workspace_size(B, Sq, Sk, Nkv, D)
+ *               bytes, 256-byte aligned (holds v transposed for the K-major
+ *               operand and, when ceil(Sk/64) + ceil(Sq/128) > 2048 or
+ *               ceil(Sq/128) > 1024, the launch's work plan)
  */
-cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sk, int64_t Nkv, int64_t D, size_t *bytes);
+cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t Nkv, int64_t D, size_t *bytes);
 cp_status cp_attn_partial_f32(const float *q, const float *k, const float *v, const int32_t *q_pos,
                               const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv,
                               int64_t D, float scale, float *o, float *lse, void *workspace, size_t ws_bytes,
@@ -197,8 +220,10 @@ cp_status cp_lse_merge(float *o_acc, float *lse_acc, const float *o_tile, const 
  * cp_ring_workspace_size -- bytes of device workspace cp_ring_attention_fwd
  * needs for these sizes and flags: the per-step partial (fp32 o and lse for
  * all C ranks; not with CP_RING_FUSED_MERGE), an fp32 accumulator when o_dtype
- * is CP_BF16, and with CP_RING_PREFETCH two K/V rotation buffers.  Host only;
- * *bytes is written on success.
+ * is CP_BF16, with CP_RING_PREFETCH two K/V rotation buffers, and for long
+ * shards (C * (ceil((S/C)/128) * 2) > 2048 position tables, or more than
+ * 1024 query blocks in a step) the attention launches' work plan.  Host
+ * only; *bytes is written on success.
  */
 cp_status cp_ring_workspace_size(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
                                  int flags, cp_dtype o_dtype, size_t *bytes);
@@ -353,12 +378,12 @@ cp_status cp_mesh_attention_fwd(const void *q_sh, const void *k_sh, const void *
  *   D in {64, 128}; N % Nkv == 0; scale finite and > 0
  *   dq : device fp32 [B][Sq][N][D]; dk, dv : device fp32 [B][Sk][Nkv][D];
  *        32-byte aligned; written, or added to when accumulate != 0
- *   workspace : device, >= cp_attn_bwd_workspace_size(B, Sq, N) bytes,
- *        256-byte aligned (per-row statistics)
- * Other pointers 16-byte aligned.  Limits (else CP_ERR_SHAPE):
- * ceil(Sk/128) + ceil(Sq/128) <= 2048, ceil(Sq/128) <= 1024, ceil(Sk/128) <= 1024.
+ *   workspace : device, >= cp_attn_bwd_workspace_size(B, Sq, Sk, N) bytes,
+ *        256-byte aligned (per-row statistics and, when ceil(Sk/128) +
+ *        ceil(Sq/128) > 2048 or either exceeds 1024, the kernels' work plans)
+ * Other pointers 16-byte aligned.
  */
-cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t N, size_t *bytes);
+cp_status cp_attn_bwd_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t N, size_t *bytes);
 cp_status cp_attn_bwd_partial(const void *q, const void *k, const void *v, const float *o, const void *dout,
                               const float *lse, const int32_t *q_pos, const int32_t *k_pos, int64_t B,
                               int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv, int64_t D, float scale, float *dq,

@@ -40,7 +40,20 @@ def test_attn_partial_validation(cplib):
     assert _attn(cplib, scale=-1.0) == 10
     assert _attn(cplib, q=MISALIGNED) == 5
     assert _attn(cplib, o=ctypes.c_void_p(4096 + 16)) == 5  # o needs 32-byte alignment
-    assert _attn(cplib, Sq=200000, Sk=200000) == 2  # position tables exceed the on-chip limit
+    # past the on-chip plan limit the call needs a workspace (cp_attn_partial_ws)
+    assert _attn(cplib, Sq=200000, Sk=200000) == 6
+    n = ctypes.c_size_t(0)
+    assert cplib.cp_attn_workspace_size(1, 256, 256, 2, 2, 64, ctypes.byref(n)) == 0 and n.value == 0
+    assert cplib.cp_attn_workspace_size(1, 200000, 200000, 2, 2, 64, ctypes.byref(n)) == 0 and n.value > 0
+    need = n.value
+    ws = cplib.cp_attn_partial_ws
+    wargs = [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 200000, 200000, 2, 2, 64, 0.125, FAKE, FAKE]
+    assert ws(*wargs, NULL, 0, None) == 6
+    assert ws(*wargs, FAKE, need - 1, None) == 6
+    assert ws(*wargs, ctypes.c_void_p(4096 + 128), need, None) == 5  # plan buffer 256-byte aligned
+    bad = list(wargs)
+    bad[10] = 96
+    assert ws(*bad, FAKE, need, None) == 7
 
 
 def test_shard_validation(cplib):
