@@ -382,6 +382,246 @@ def graph_replay_times(args, torch, F, step, inputs, flush_buf, parts):
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
+class StepRig:
+    """Resident device buffers and the step of one workload: zigzag-shard q, k,
+    v -> positions -> ring forward -> unshard o -> Ulysses relayout of the
+    shards.  Per-kernel CUDA events are recorded on the launching stream."""
+
+    def __init__(self, w, dev, prefetch, fused, q, k, v):
+        import torch
+        from context_causal_attention_gb300 import ops as F
+        self.F, self.torch, self.w = F, torch, w
+        self.prefetch, self.fused = prefetch, fused
+        C, S, B, N, Nkv, D = w.C, w.S, w.B, w.N, w.Nkv, w.D
+        s = S // C
+        self.lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
+        self.qd, self.kd, self.vd = (t.to(dev) for t in (q, k, v))
+        self.qs = torch.empty((C, B, s, N, D), dtype=torch.bfloat16, device=dev)
+        self.ks = torch.empty((C, B, s, Nkv, D), dtype=torch.bfloat16, device=dev)
+        self.vs = torch.empty_like(self.ks)
+        self.pos = torch.empty((C, s), dtype=torch.int32, device=dev)
+        self.o_sh = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+        self.lse_sh = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
+        self.o_full = torch.empty((B, S, N, D), dtype=torch.float32, device=dev)
+        self.ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32, fused)),
+                              dtype=torch.uint8, device=dev)
+        self.qh = torch.empty((C, B, S, N // C, D), dtype=torch.bfloat16, device=dev)
+        self.kh = torch.empty((C, B, S, Nkv // C, D), dtype=torch.bfloat16, device=dev)
+        self.vh = torch.empty_like(self.kh)
+        # long shards: each attention launch is preceded by the two plan kernels
+        nt = -(-s // 128)
+        plan = 0 if (C * 2 * nt <= 2048 and C * ((nt + 1) // 2) <= 1024) else 2
+        self.launches_per_step = 3 + 1 + C * (1 + plan) + (0 if fused else C - 1) + 1 + 3
+
+    def events(self):
+        torch = self.torch
+
+        def mk(n):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            for e in evs:
+                e.record()
+            return evs
+        return {"ring": mk(4 * self.w.C), "shard": mk(2), "unshard": mk(2), "relayout": mk(2)}
+
+    def step(self, qin, kin, vin, ev, o_out=None):
+        """One pass of the hot path.  ev: dict of event lists or None.  qin, kin,
+        vin may be pinned host tensors (the shard reads them across the host
+        link); o_out (default: the device o_full) may be a pinned host tensor."""
+        F, w, lay = self.F, self.w, self.lay
+        C, S = w.C, w.S
+
+        def mark(name, i):
+            if ev is not None:
+                ev[name][i].record()
+        mark("shard", 0)
+        F.cp_zigzag_shard(qin, C, lay, out=self.qs)
+        F.cp_zigzag_shard(kin, C, lay, out=self.ks)
+        F.cp_zigzag_shard(vin, C, lay, out=self.vs)
+        mark("shard", 1)
+        F.cp_zigzag_positions(S, C, lay, out=self.pos)
+        F.cp_ring_attention_fwd(self.qs, self.ks, self.vs, self.pos, layout=lay, prefetch=self.prefetch,
+                                o_dtype=F.CP_F32, workspace=self.ws, o=self.o_sh, lse=self.lse_sh,
+                                events=ev["ring"] if ev is not None else None, fused_merge=self.fused)
+        mark("unshard", 0)
+        F.cp_zigzag_unshard(self.o_sh, lay, out=self.o_full if o_out is None else o_out)
+        mark("unshard", 1)
+        mark("relayout", 0)
+        F.cp_ulysses_relayout(self.qs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=self.qh)
+        F.cp_ulysses_relayout(self.ks, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=self.kh)
+        F.cp_ulysses_relayout(self.vs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=self.vh)
+        mark("relayout", 1)
+
+
+def ring_step_pairs(w):
+    """Exact visible pairs per (b, h) of each ring step, all ranks together."""
+    C, s, t = w.C, w.S // w.C, w.S // (2 * w.C)
+    if w.layout == "zigzag":
+        return [C * (t * t + t * (t + 1))] + [C * 2 * t * t] * (C - 1)
+    return [C * s * (s + 1) // 2] + [(C - st) * s * s for st in range(1, C)]
+
+
+def merge_bytes_per_step(w):
+    """Algorithmic bytes of the merge of each ring step >= 1: rows whose tile
+    lse is finite move 3*4*D + 12 bytes, the others 4."""
+    C, B, N, D, s = w.C, w.B, w.N, w.D, w.S // w.C
+    rows = C * B * N * s
+    out = []
+    for st in range(1, C):
+        if w.layout == "zigzag":
+            fr = sum(B * N * (s if (rr - st) % C < rr else s // 2) for rr in range(C))
+        else:
+            fr = B * N * s * (C - st)
+        out.append(fr * (12 * D + 12) + (rows - fr) * 4)
+    return out
+
+
+def kernel_metrics(rig, evsets, peaks):
+    """Per-kernel times and rates from the events of the timed steps."""
+    w = rig.w
+    C, B, N, Nkv, D, S = w.C, w.B, w.N, w.Nkv, w.D, w.S
+    n = len(evsets)
+    attn_ms, merge_ms = [0.0] * C, [0.0] * C
+    shard_ms = unshard_ms = relayout_ms = 0.0
+    for e in evsets:
+        r = e["ring"]
+        for st in range(C):
+            attn_ms[st] += r[4 * st].elapsed_time(r[4 * st + 1]) / n
+            if st > 0:
+                merge_ms[st] += r[4 * st + 2].elapsed_time(r[4 * st + 3]) / n
+        shard_ms += e["shard"][0].elapsed_time(e["shard"][1]) / n
+        unshard_ms += e["unshard"][0].elapsed_time(e["unshard"][1]) / n
+        relayout_ms += e["relayout"][0].elapsed_time(e["relayout"][1]) / n
+    if rig.fused:
+        # the step merges inside the attention epilogue; time the standalone merge
+        # kernel on the same ring (separate-merge mode, traced) for its GB/s
+        torch, F = rig.torch, rig.F
+        ws2 = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, rig.prefetch, F.CP_F32, False)),
+                          dtype=torch.uint8, device=rig.qs.device)
+        o2, l2 = torch.empty_like(rig.o_sh), torch.empty_like(rig.lse_sh)
+        merge_ms = [0.0] * C
+        reps = 2
+        for rep_i in range(reps + 1):
+            ev2 = rig.events()["ring"]
+            F.cp_ring_attention_fwd(rig.qs, rig.ks, rig.vs, rig.pos, layout=rig.lay, prefetch=rig.prefetch,
+                                    o_dtype=F.CP_F32, workspace=ws2, o=o2, lse=l2, events=ev2, fused_merge=False)
+            torch.cuda.synchronize()
+            if rep_i == 0:
+                continue  # warm-up
+            for st in range(1, C):
+                merge_ms[st] += ev2[4 * st + 2].elapsed_time(ev2[4 * st + 3]) / reps
+        del ws2, o2, l2
+    attn_flops = [4.0 * B * N * D * p for p in ring_step_pairs(w)]
+    attn_tflops = sum(attn_flops) / (sum(attn_ms) * 1e-3) / 1e12
+    per_step_tflops = [f / (t * 1e-3) / 1e12 for f, t in zip(attn_flops, attn_ms)]
+    mb = merge_bytes_per_step(w)
+    merge_gbs = sum(mb) / (sum(merge_ms) * 1e-3) / 1e9 if C > 1 else None
+    merge_gbs_steps = [b / (t * 1e-3) / 1e9 for b, t in zip(mb, merge_ms[1:])]
+    qkv_bytes = (B * S * N * D + 2 * B * S * Nkv * D) * 2
+    hbm = peaks["hbm_gbs"]
+    shard_gbs = 2 * qkv_bytes / (shard_ms * 1e-3) / 1e9
+    relayout_gbs = 2 * qkv_bytes / (relayout_ms * 1e-3) / 1e9
+    return {
+        "attn_ms_per_ring_step": attn_ms, "attn_tflops_per_ring_step": per_step_tflops, "attn_tflops": attn_tflops,
+        "merge_ms_per_ring_step": merge_ms[1:], "merge_gbs": merge_gbs, "merge_gbs_per_ring_step": merge_gbs_steps,
+        "merge_frac_hbm_per_ring_step": [x / hbm for x in merge_gbs_steps],
+        "merge_measured_in": "separate-merge ring calls after the timed region" if rig.fused else "the timed step",
+        "shard_gbs": shard_gbs, "unshard_gbs": 2 * (B * S * N * D * 4) / (unshard_ms * 1e-3) / 1e9,
+        "relayout_gbs": relayout_gbs, "hbm_peak_gbs": hbm,
+        "merge_frac_hbm": (merge_gbs / hbm) if merge_gbs else None,
+        "shard_frac_hbm": shard_gbs / hbm, "relayout_frac_hbm": relayout_gbs / hbm,
+    }
+
+
+def time_device_steps(rig, steps, warmup, world=1, clocks=None):
+    """W untimed steps, then K timed steps bracketed by a barrier and a
+    synchronize on both sides, per-kernel events inside.  Workloads within
+    1.5x of L2 get an L2 flush between steps, outside each step's events.
+    Returns (ms per step, max over ranks), the event sets and the wall time."""
+    torch = rig.torch
+    w = rig.w
+    for _ in range(warmup):
+        rig.step(rig.qd, rig.kd, rig.vd, None)
+    torch.cuda.synchronize()
+    evsets = [rig.events() for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = needs_l2_flush(w)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=rig.qs.device) if flush else None
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    t_start.record()
+    for i in range(steps):
+        if flush:
+            flush_buf.zero_()  # evicts the previous step's data from L2 (outside the step's events)
+        step_ev[i][0].record()
+        rig.step(rig.qd, rig.kd, rig.vd, evsets[i])
+        step_ev[i][1].record()
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    if clocks is not None:
+        now = time.time()
+        # nvidia-smi stamps whole milliseconds; widen the window by one interval
+        clocks.window(now - wall - 0.05, now + 0.05)
+    ms_total = (sum(a.elapsed_time(b) for a, b in step_ev) if flush else t_start.elapsed_time(t_end))
+    return max_over_ranks(ms_total, world) / steps, evsets, wall, flush_buf
+
+
+def secondary_step_line(w, dev, steps, warmup, peaks, prefetch, fused):
+    """The device step (same rig, same timing rules) on another workload, for
+    the secondary keys of the default line."""
+    import cp_synth as SY
+    q, k, v, _ = SY.make_qkv(w)
+    rig = StepRig(w, dev, prefetch, fused, q, k, v)
+    del q, k, v
+    ms, evsets, wall, _ = time_device_steps(rig, steps, warmup)
+    km = kernel_metrics(rig, evsets, peaks)
+    out = {"workload": workload_config(w, prefetch)["workload"], "l2": workload_config(w, prefetch)["l2"],
+           "ms_per_step": ms, "value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "attn_tflops": km["attn_tflops"], "attn_tflops_per_ring_step": km["attn_tflops_per_ring_step"],
+           "attn_frac_of_burst_bf16": km["attn_tflops"] / peaks["bf16_tflops"],
+           "merge_gbs": km["merge_gbs"], "merge_frac_hbm": km["merge_frac_hbm"],
+           "merge_gbs_per_ring_step": km["merge_gbs_per_ring_step"],
+           "merge_frac_hbm_per_ring_step": km["merge_frac_hbm_per_ring_step"],
+           "merge_measured_in": km["merge_measured_in"],
+           "shard_gbs": km["shard_gbs"], "unshard_gbs": km["unshard_gbs"], "relayout_gbs": km["relayout_gbs"],
+           "relayout_frac_hbm": km["relayout_frac_hbm"], "shard_frac_hbm": km["shard_frac_hbm"],
+           "steps": steps, "warmup": warmup, "wall_s_timed": wall}
+    del rig
+    return out
+
+
+def run_secondary(args, dev, peaks, prefetch, fused):
+    """Secondary keys of the default line: the S=4096 and S=131072 workloads'
+    device steps (step TFLOP/s, relayout and per-step merge GB/s with their
+    fraction of HBM), and the S=65536 sweep point for C in {2, 4, 8},
+    contiguous against zigzag (per-rank issued key tiles and per-rank time,
+    max / mean over ranks)."""
+    import cp_synth as SY
+    torch = __import__("torch")
+    out = {}
+    for name in ("s4k", "s128k"):
+        out[name] = secondary_step_line(SY.WORKLOADS[name], dev, args.steps, args.warmup, peaks, prefetch, fused)
+        torch.cuda.empty_cache()
+    sw = []
+    for w in SY.sweep_workloads():
+        if w.S != 65536:
+            continue
+        m = sweep_measure(w, dev, reps=3, device_inputs=True)
+        sw.append({k: m[k] for k in ("S", "C", "layout", "ring_ms", "ring_tflops", "pairs_max_over_mean",
+                                     "issued_tiles_max_over_mean", "rank_ms_max_over_mean")})
+        torch.cuda.empty_cache()
+    out["sweep_S65536"] = {"what": "B=1 N=16 D=128 ring with prefetch; per-rank figures are max / mean over the C "
+                                   "virtual ranks (rank time: each rank's C partials launched on their own)",
+                           "runs": sw}
+    return out
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -401,154 +641,25 @@ def run_ours(args, w):
     lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
     prefetch = 1 if args.prefetch else 0
     fused = bool(args.fused_merge)
+    rig = StepRig(w, dev, prefetch, fused, q, k, v)
+    qd, kd, vd = rig.qd, rig.kd, rig.vd
+    qs, o_sh, lse_sh, o_full, qh = rig.qs, rig.o_sh, rig.lse_sh, rig.o_full, rig.qh
+    step = rig.step
+    launches_per_step = rig.launches_per_step
 
-    # resident buffers
-    qd, kd, vd = (t.to(dev) for t in (q, k, v))
-    qs = torch.empty((C, B, s, N, D), dtype=torch.bfloat16, device=dev)
-    ks = torch.empty((C, B, s, Nkv, D), dtype=torch.bfloat16, device=dev)
-    vs = torch.empty_like(ks)
-    pos = torch.empty((C, s), dtype=torch.int32, device=dev)
-    o_sh = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
-    lse_sh = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
-    o_full = torch.empty((B, S, N, D), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32, fused)),
-                     dtype=torch.uint8, device=dev)
-    qh = torch.empty((C, B, S, N // C, D), dtype=torch.bfloat16, device=dev)
-    kh = torch.empty((C, B, S, Nkv // C, D), dtype=torch.bfloat16, device=dev)
-    vh = torch.empty_like(kh)
-    n_ring_ev = 4 * C
-
-    def mk_events(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record()
-        return evs
-
-    def step(qin, kin, vin, ev, o_out=None):
-        """One pass of the hot path.  ev: dict of event lists or None.  qin, kin,
-        vin may be pinned host tensors (the shard reads them across the host
-        link); o_out (default: the device o_full) may be a pinned host tensor."""
-        def mark(name, i):
-            if ev is not None:
-                ev[name][i].record()
-        mark("shard", 0)
-        F.cp_zigzag_shard(qin, C, lay, out=qs)
-        F.cp_zigzag_shard(kin, C, lay, out=ks)
-        F.cp_zigzag_shard(vin, C, lay, out=vs)
-        mark("shard", 1)
-        F.cp_zigzag_positions(S, C, lay, out=pos)
-        F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch, o_dtype=F.CP_F32, workspace=ws,
-                                o=o_sh, lse=lse_sh, events=ev["ring"] if ev is not None else None,
-                                fused_merge=fused)
-        mark("unshard", 0)
-        F.cp_zigzag_unshard(o_sh, lay, out=o_full if o_out is None else o_out)
-        mark("unshard", 1)
-        mark("relayout", 0)
-        F.cp_ulysses_relayout(qs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=qh)
-        F.cp_ulysses_relayout(ks, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=kh)
-        F.cp_ulysses_relayout(vs, C, F.CP_SEQ_TO_HEAD, F.CP_GLOBAL_ORDER, out=vh)
-        mark("relayout", 1)
-
-    launches_per_step = 3 + 1 + C + (0 if fused else C - 1) + 1 + 3
-    # ---- warm-up
-    for _ in range(args.warmup):
-        step(qd, kd, vd, None)
-    torch.cuda.synchronize()
     # ---- timed region (device time), per-kernel events inside
-    evsets = [{"ring": mk_events(n_ring_ev), "shard": mk_events(2), "unshard": mk_events(2),
-               "relayout": mk_events(2)} for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush = needs_l2_flush(w)
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    t_start.record()
-    for i in range(args.steps):
-        if flush:
-            flush_buf.zero_()  # evicts the previous step's data from L2 (outside the step's events)
-        step_ev[i][0].record()
-        step(qd, kd, vd, evsets[i])
-        step_ev[i][1].record()
-    t_end.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    wall = time.perf_counter() - wall0
-    now = time.time()
-    # nvidia-smi stamps whole milliseconds; widen the window by one interval
-    clocks.window(now - wall - 0.05, now + 0.05)
-    ms_total = (sum(a.elapsed_time(b) for a, b in step_ev) if flush else t_start.elapsed_time(t_end))
+    ms_step, evsets, wall, flush_buf = time_device_steps(rig, args.steps, args.warmup, world, clocks)
     clk = clocks.stop()
-    ms_total = max_over_ranks(ms_total, world)
-    ms_step = ms_total / args.steps
     flops_step = w.flops
     value = job_throughput(flops_step, world, ms_step) / 1e12
 
     # ---- per-kernel numbers from the events
-    pairs_t = w.t
-    # exact visible pairs per (b, h) per ring step, all ranks together
-    if w.layout == "zigzag":
-        step_pairs = [C * (pairs_t * pairs_t + pairs_t * (pairs_t + 1))] + [C * 2 * pairs_t * pairs_t] * (C - 1)
-    else:
-        step_pairs = [C * s * (s + 1) // 2] + [(C - st) * s * s for st in range(1, C)]
-    attn_ms = [0.0] * C
-    merge_ms = [0.0] * C
-    shard_ms = unshard_ms = relayout_ms = 0.0
-    for e in evsets:
-        r = e["ring"]
-        for st in range(C):
-            attn_ms[st] += r[4 * st].elapsed_time(r[4 * st + 1]) / args.steps
-            if st > 0:
-                merge_ms[st] += r[4 * st + 2].elapsed_time(r[4 * st + 3]) / args.steps
-        shard_ms += e["shard"][0].elapsed_time(e["shard"][1]) / args.steps
-        unshard_ms += e["unshard"][0].elapsed_time(e["unshard"][1]) / args.steps
-        relayout_ms += e["relayout"][0].elapsed_time(e["relayout"][1]) / args.steps
-    if fused:
-        # the step merges inside the attention epilogue; time the standalone merge
-        # kernel on the same ring (separate-merge mode, traced) for its GB/s
-        ws2 = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, Nkv, D, C, prefetch, F.CP_F32, False)),
-                          dtype=torch.uint8, device=dev)
-        o2, l2 = torch.empty_like(o_sh), torch.empty_like(lse_sh)
-        merge_ms = [0.0] * C
-        reps = 2
-        for rep_i in range(reps + 1):
-            ev2 = mk_events(n_ring_ev)
-            F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=prefetch, o_dtype=F.CP_F32, workspace=ws2,
-                                    o=o2, lse=l2, events=ev2, fused_merge=False)
-            torch.cuda.synchronize()
-            if rep_i == 0:
-                continue  # warm-up
-            for st in range(1, C):
-                merge_ms[st] += ev2[4 * st + 2].elapsed_time(ev2[4 * st + 3]) / reps
-        del ws2, o2, l2
-    attn_flops = [4.0 * B * N * D * p for p in step_pairs]
-    attn_total_ms = sum(attn_ms)
-    attn_tflops = sum(attn_flops) / (attn_total_ms * 1e-3) / 1e12
-    per_step_tflops = [f / (t * 1e-3) / 1e12 for f, t in zip(attn_flops, attn_ms)]
-    # merge algorithmic bytes: rows whose tile lse is finite move 3*4*D + 12 bytes, others 4
-    rows = C * B * N * s
-    merge_gbs = None
-    if C > 1:
-        if w.layout == "zigzag":
-            fin_rows = []
-            for st in range(1, C):
-                fr = 0
-                for rr in range(C):
-                    j = (rr - st) % C
-                    fr += B * N * (s if j < rr else s // 2)
-                fin_rows.append(fr)
-        else:
-            fin_rows = [B * N * s * (C - st) for st in range(1, C)]
-        merge_bytes = sum(fr * (12 * D + 12) + (rows - fr) * 4 for fr in fin_rows)
-        merge_gbs = merge_bytes / (sum(merge_ms) * 1e-3) / 1e9
+    km = kernel_metrics(rig, evsets, peaks)
+    attn_ms, attn_tflops, per_step_tflops = km["attn_ms_per_ring_step"], km["attn_tflops"], \
+        km["attn_tflops_per_ring_step"]
+    merge_gbs = km["merge_gbs"]
     qkv_bytes = (B * S * N * D + 2 * B * S * Nkv * D) * 2
-    shard_gbs = 2 * qkv_bytes / (shard_ms * 1e-3) / 1e9
-    unshard_gbs = 2 * (B * S * N * D * 4) / (unshard_ms * 1e-3) / 1e9
-    relayout_gbs = 2 * qkv_bytes / (relayout_ms * 1e-3) / 1e9
     peak_tc, peak_name = tensor_peak(peaks, wall, clk)
     traffic = recorded_traffic(w.name, fused)
 
@@ -695,19 +806,17 @@ def run_ours(args, w):
                                               "around the device step"}},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
-        "kernels": {
-            "attn_ms_per_ring_step": attn_ms, "attn_tflops_per_ring_step": per_step_tflops,
-            "merge_ms_per_ring_step": merge_ms[1:], "merge_gbs": merge_gbs,
-            "merge_measured_in": "separate-merge ring calls after the timed region" if fused else "the timed step",
-            "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "relayout_gbs": relayout_gbs,
-            "hbm_peak_gbs": peaks["hbm_gbs"],
-            "merge_frac_hbm": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
-            "shard_frac_hbm": shard_gbs / peaks["hbm_gbs"], "relayout_frac_hbm": relayout_gbs / peaks["hbm_gbs"],
-        },
+        "kernels": km,
         "wall_s_timed": wall,
     }
     if graph_info is not None:
         line["graph"] = graph_info
+    if world == 1 and not args.no_secondary:
+        # the other configurations, same device-step timing (after the main
+        # timed region and its end-to-end runs, with their buffers freed)
+        del rig, inbuf, obuf, qd, kd, vd, qs, o_sh, lse_sh, o_full, qh, step, flush_buf
+        torch.cuda.empty_cache()
+        line["secondary"] = run_secondary(args, dev, peaks, prefetch, fused)
     if rank == 0 and not args.no_cpu_baseline:
         qkv64 = prepare_oracle_inputs(w, q, k, v)
         line["cpu_baseline"] = cpu_baseline(w, qkv64, target_s=args.cpu_seconds)
@@ -766,15 +875,113 @@ def exact_pairs_per_rank(S, C, layout):
     return [r * s * s + s * (s + 1) // 2 for r in range(C)]
 
 
+def sweep_measure(w, dev, reps, device_inputs=False):
+    """One sweep workload: ring TFLOP/s (prefetch on), per-rank pairs, issued
+    key tiles and time (each rank's C partials launched on their own, timed
+    with events), merge / shard / unshard / prefetch-copy GB/s.  Inputs are
+    N(0, 1) bf16 drawn with seed 0 (on the device when device_inputs)."""
+    import torch
+
+    from context_causal_attention_gb300 import ops as F
+    C, S, B, N, D = w.C, w.S, w.B, w.N, w.D
+    s = S // C
+    lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
+    if device_inputs:
+        g = torch.Generator(device=dev).manual_seed(0)
+        q, k, v = (torch.randn(B, S, N, D, generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+    else:
+        g = torch.Generator("cpu").manual_seed(0)
+        q, k, v = (torch.randn(B, S, N, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(3))
+    qs, ks, vs = (F.cp_zigzag_shard(t, C, lay) for t in (q, k, v))
+    pos = F.cp_zigzag_positions(S, C, lay, device=dev)
+    o = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, N, D, C, 1, F.CP_F32)), dtype=torch.uint8,
+                     device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * C)]
+    for e in ev:
+        e.record()
+
+    def ring(events=None):
+        F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1, workspace=ws, o=o, lse=lse,
+                                events=events)
+
+    for _ in range(3):
+        ring()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ring()
+    e1.record()
+    torch.cuda.synchronize()
+    ring_ms = e0.elapsed_time(e1) / reps
+    ring(ev)
+    torch.cuda.synchronize()
+    merge_ms = sum(ev[4 * st + 2].elapsed_time(ev[4 * st + 3]) for st in range(1, C))
+    attn_ms = sum(ev[4 * st].elapsed_time(ev[4 * st + 1]) for st in range(C))
+    # per-rank diagnostic: rank r's C partials launched on their own
+    o1 = torch.empty((B, s, N, D), dtype=torch.float32, device=dev)
+    l1 = torch.empty((B, N, s), dtype=torch.float32, device=dev)
+    rank_ms = []
+    for r in range(C):
+        def partials():
+            for st in range(C):
+                j = (r - st) % C
+                F.cp_attn_partial(qs[r], ks[j], vs[j], pos[r], pos[j], o=o1, lse=l1)
+        partials()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(2):
+            partials()
+        a1.record()
+        torch.cuda.synchronize()
+        rank_ms.append(a0.elapsed_time(a1) / 2)
+    # permutations and the prefetch copy (one K rotation = the bytes the ring exchange moves per step)
+    x = torch.empty_like(q)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(5):
+        F.cp_zigzag_shard(q, C, lay, out=qs)
+    t1.record()
+    torch.cuda.synchronize()
+    shard_gbs = 2 * q.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
+    t0.record()
+    for _ in range(5):
+        F.cp_zigzag_unshard(qs, lay, out=x)
+    t1.record()
+    torch.cuda.synchronize()
+    unshard_gbs = 2 * q.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
+    kbuf = torch.empty_like(ks)
+    t0.record()
+    for _ in range(5):
+        kbuf.copy_(ks)
+    t1.record()
+    torch.cuda.synchronize()
+    copy_gbs = 2 * ks.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
+    pairs = exact_pairs_per_rank(S, C, w.layout)
+    flops = 4.0 * B * N * D * S * (S + 1) / 2
+    tiles = tile_counts_per_rank(pos.cpu().numpy())
+    issued = [t["issued"] for t in tiles]
+    return {
+        "sweep": w.name, "S": S, "C": C, "layout": w.layout,
+        "ring_ms": ring_ms, "ring_tflops": flops / (ring_ms * 1e-3) / 1e12,
+        "attn_ms_in_ring": attn_ms, "merge_ms_in_ring": merge_ms,
+        "pairs_per_rank": pairs, "pairs_max_over_mean": max(pairs) / (sum(pairs) / C),
+        "rank_ms": rank_ms, "rank_ms_max_over_mean": max(rank_ms) / (sum(rank_ms) / C),
+        "issued_tiles_max_over_mean": max(issued) / (sum(issued) / C),
+        "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "kv_rotation_copy_gbs": copy_gbs,
+        "merge_rows_per_step": C * B * N * s,
+        "key_tiles_per_rank": tiles,
+    }
+
+
 def run_sweep(args):
-    """One JSON line per sweep workload: ring TFLOP/s, per-rank pairs and per-rank
-    time (each rank's C partials launched on their own, timed with events),
-    merge / shard / unshard / prefetch-copy GB/s."""
+    """One JSON line per sweep workload (see sweep_measure)."""
     import torch
 
     import cp_synth as SY
     from context_causal_attention_gb300 import build as cuda_build
-    from context_causal_attention_gb300 import ops as F
 
     cuda_build.build()
     dev = torch.device("cuda", 0)
@@ -783,95 +990,9 @@ def run_sweep(args):
     for w in SY.sweep_workloads():
         if names and w.name not in names:
             continue
-        C, S, B, N, D = w.C, w.S, w.B, w.N, w.D
-        s = S // C
-        lay = F.CP_ZIGZAG if w.layout == "zigzag" else F.CP_CONTIGUOUS
-        g = torch.Generator("cpu").manual_seed(0)
-        q, k, v = (torch.randn(B, S, N, D, generator=g).to(torch.bfloat16).to(dev) for _ in range(3))
-        qs, ks, vs = (F.cp_zigzag_shard(t, C, lay) for t in (q, k, v))
-        pos = F.cp_zigzag_positions(S, C, lay, device=dev)
-        o = torch.empty((C, B, s, N, D), dtype=torch.float32, device=dev)
-        lse = torch.empty((C, B, N, s), dtype=torch.float32, device=dev)
-        ws = torch.empty(max(256, F.cp_ring_workspace_size(B, S, N, N, D, C, 1, F.CP_F32)), dtype=torch.uint8,
-                         device=dev)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4 * C)]
-        for e in ev:
-            e.record()
-
-        def ring(events=None):
-            F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, prefetch=1, workspace=ws, o=o, lse=lse,
-                                    events=events)
-
-        for _ in range(3):
-            ring()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = max(3, args.steps)
-        e0.record()
-        for _ in range(reps):
-            ring()
-        e1.record()
-        torch.cuda.synchronize()
-        ring_ms = e0.elapsed_time(e1) / reps
-        ring(ev)
-        torch.cuda.synchronize()
-        merge_ms = sum(ev[4 * st + 2].elapsed_time(ev[4 * st + 3]) for st in range(1, C))
-        attn_ms = sum(ev[4 * st].elapsed_time(ev[4 * st + 1]) for st in range(C))
-        # per-rank diagnostic: rank r's C partials launched on their own
-        o1 = torch.empty((B, s, N, D), dtype=torch.float32, device=dev)
-        l1 = torch.empty((B, N, s), dtype=torch.float32, device=dev)
-        rank_ms = []
-        for r in range(C):
-            def partials():
-                for st in range(C):
-                    j = (r - st) % C
-                    F.cp_attn_partial(qs[r], ks[j], vs[j], pos[r], pos[j], o=o1, lse=l1)
-            partials()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record()
-            for _ in range(2):
-                partials()
-            a1.record()
-            torch.cuda.synchronize()
-            rank_ms.append(a0.elapsed_time(a1) / 2)
-        # permutations and the prefetch copy (one K rotation = the bytes the ring exchange moves per step)
-        x = torch.empty_like(q)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(5):
-            F.cp_zigzag_shard(q, C, lay, out=qs)
-        t1.record()
-        torch.cuda.synchronize()
-        shard_gbs = 2 * q.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
-        t0.record()
-        for _ in range(5):
-            F.cp_zigzag_unshard(qs, lay, out=x)
-        t1.record()
-        torch.cuda.synchronize()
-        unshard_gbs = 2 * q.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
-        kbuf = torch.empty_like(ks)
-        t0.record()
-        for _ in range(5):
-            kbuf.copy_(ks)
-        t1.record()
-        torch.cuda.synchronize()
-        copy_gbs = 2 * ks.numel() * 2 / (t0.elapsed_time(t1) / 5 * 1e-3) / 1e9
-        pairs = exact_pairs_per_rank(S, C, w.layout)
-        flops = 4.0 * B * N * D * S * (S + 1) / 2
-        rows = C * B * N * s
-        line = {
-            "sweep": w.name, "S": S, "C": C, "layout": w.layout,
-            "ring_ms": ring_ms, "ring_tflops": flops / (ring_ms * 1e-3) / 1e12,
-            "attn_ms_in_ring": attn_ms, "merge_ms_in_ring": merge_ms,
-            "pairs_per_rank": pairs, "pairs_max_over_mean": max(pairs) / (sum(pairs) / C),
-            "rank_ms": rank_ms, "rank_ms_max_over_mean": max(rank_ms) / (sum(rank_ms) / C),
-            "shard_gbs": shard_gbs, "unshard_gbs": unshard_gbs, "kv_rotation_copy_gbs": copy_gbs,
-            "hbm_peak_gbs": peaks["hbm_gbs"],
-            "merge_rows_per_step": rows,
-            "key_tiles_per_rank": tile_counts_per_rank(pos.cpu().numpy()),
-        }
+        line = sweep_measure(w, dev, reps=max(3, args.steps))
+        line["hbm_peak_gbs"] = peaks["hbm_gbs"]
         print(json.dumps(line), flush=True)
-        del q, k, v, qs, ks, vs, o, lse, ws, x, kbuf, o1, l1
         torch.cuda.empty_cache()
     return 0
 
@@ -1048,6 +1169,8 @@ def main():
     ap.add_argument("--separate-merge", dest="fused_merge", action="store_false", help="the default")
     ap.set_defaults(fused_merge=False)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary workloads (S=4096, S=131072, the S=65536 sweep point) of the default line")
     ap.add_argument("--graph", action="store_true",
                     help="also time CUDA-graph replays of the step and of each permutation (with the eager times)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
