@@ -554,6 +554,20 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (tid == 0 && *abort_flag) atomicExch(&g_cp_device_status_tf32, static_cast<int>(CP_ERR_DEVICE_TIMEOUT));
 }
 
+// out = in rounded to the nearest tf32 value (10-bit mantissa, ties away from
+// zero), n4 float4 vectors; q and k pass through it so that the tensor cores,
+// which take the top 19 bits of each fp32 operand, see rounded rather than
+// truncated values.
+__global__ void __launch_bounds__(256) tf32_round_kernel(const float4 *__restrict__ in, float4 *__restrict__ out,
+                                                         long long n4) {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 x = __ldg(in + i);
+        out[i] = make_float4(__uint_as_float(round_tf32(x.x)), __uint_as_float(round_tf32(x.y)),
+                             __uint_as_float(round_tf32(x.z)), __uint_as_float(round_tf32(x.w)));
+    }
+}
+
 // vt[o][h][d][j] = v[o][j][h][d] for j < Sk, rounded to tf32 (rows padded to sk_pad with zeros)
 __global__ void __launch_bounds__(256) tf32_transpose_kernel(const float *__restrict__ v, float *__restrict__ vt,
                                                              long long outer, int Sk, int Nkv, int D, int sk_pad) {
@@ -706,6 +720,19 @@ cp_status launch_tf32_transpose(const float *v, float *vt, int64_t outer, int64_
     return last_launch_status();
 }
 
+cp_status launch_tf32_round(const float *in, float *out, int64_t n, cudaStream_t stream) {
+    if (!in || !out) return CP_ERR_NULL;
+    if (n % 4 != 0 || !aligned16(in) || !aligned16(out)) return CP_ERR_ALIGNMENT;
+    const long long n4 = n / 4;
+    if (n4 == 0) return CP_OK;
+    long long blocks = (n4 + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    if (blocks > cap) blocks = cap;
+    tf32_round_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<const float4 *>(in),
+                                                                          reinterpret_cast<float4 *>(out), n4);
+    return last_launch_status();
+}
+
 cp_status launch_attn_tf32(const AttnProblem &p, const float *vt, cudaStream_t stream) {
     cp_status st = validate_attn_tf32(p);
     if (st != CP_OK) return st;
@@ -732,13 +759,29 @@ cp_status read_tf32_device_status(int *code, bool clear) {
 
 namespace {
 inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace of cp_attn_partial_f32: q and k rounded to tf32, v transposed
+// (and rounded), then the work plan when it does not fit on chip.
+struct F32Layout {
+    size_t qr, kr, vt, plan, plan_bytes, total;
+};
+F32Layout f32_layout(int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv, int64_t D) {
+    F32Layout L;
+    L.qr = 0;
+    L.kr = round256(static_cast<size_t>(B) * Sq * N * D * 4);
+    L.vt = L.kr + round256(static_cast<size_t>(B) * Sk * Nkv * D * 4);
+    L.plan = L.vt + round256(cpattn::tf32_vt_bytes(B, Sk, Nkv, D));
+    L.plan_bytes = cpattn::tf32_plan_need(1, 1, Sq, Sk);
+    L.total = L.plan + round256(L.plan_bytes);
+    return L;
+}
 }  // namespace
 
-extern "C" cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t Nkv, int64_t D,
-                                                size_t *bytes) {
+extern "C" cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv,
+                                                int64_t D, size_t *bytes) {
     if (!bytes) return CP_ERR_NULL;
-    if (B < 1 || Sq < 1 || Sk < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
-    *bytes = round256(cpattn::tf32_vt_bytes(B, Sk, Nkv, D)) + cpattn::tf32_plan_need(1, 1, Sq, Sk);
+    if (B < 1 || Sq < 1 || Sk < 1 || N < 1 || Nkv < 1 || D < 1) return CP_ERR_SHAPE;
+    *bytes = f32_layout(B, Sq, Sk, N, Nkv, D).total;
     return CP_OK;
 }
 
@@ -764,17 +807,21 @@ extern "C" cp_status cp_attn_partial_f32(const float *q, const float *k, const f
     p.scale = scale;
     cp_status st = cpattn::validate_attn_tf32(p, false);
     if (st != CP_OK) return st;
-    // workspace: v transposed, then the work plan when it does not fit on chip
-    const size_t vt_bytes = round256(cpattn::tf32_vt_bytes(B, Sk, Nkv, D));
-    const size_t plan_need = cpattn::tf32_plan_need(1, 1, Sq, Sk);
-    if (!workspace || ws_bytes < vt_bytes + plan_need) return CP_ERR_WORKSPACE;
+    const F32Layout L = f32_layout(B, Sq, Sk, N, Nkv, D);
+    if (!workspace || ws_bytes < L.total) return CP_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return CP_ERR_ALIGNMENT;
-    float *vt = static_cast<float *>(workspace);
-    if (plan_need) {
-        p.plan = static_cast<uint8_t *>(workspace) + vt_bytes;
-        p.plan_bytes = plan_need;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *qr = reinterpret_cast<float *>(ws + L.qr), *kr = reinterpret_cast<float *>(ws + L.kr);
+    float *vt = reinterpret_cast<float *>(ws + L.vt);
+    p.q = qr;
+    p.k = kr;
+    if (L.plan_bytes) {
+        p.plan = ws + L.plan;
+        p.plan_bytes = L.plan_bytes;
     }
-    st = cpattn::launch_tf32_transpose(v, vt, B, Sk, Nkv, D, stream);
+    st = cpattn::launch_tf32_round(q, qr, B * Sq * N * D, stream);
+    if (st == CP_OK) st = cpattn::launch_tf32_round(k, kr, B * Sk * Nkv * D, stream);
+    if (st == CP_OK) st = cpattn::launch_tf32_transpose(v, vt, B, Sk, Nkv, D, stream);
     if (st == CP_OK) st = cpattn::launch_attn_tf32(p, vt, stream);
     return st;
 }

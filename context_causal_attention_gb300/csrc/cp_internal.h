@@ -154,6 +154,8 @@ int64_t tf32_vt_pad(int64_t Sk);
 size_t tf32_vt_bytes(int64_t outer, int64_t Sk, int64_t Nkv, int64_t D);
 cp_status launch_tf32_transpose(const float *v, float *vt, int64_t outer, int64_t Sk, int64_t Nkv, int64_t D,
                                 cudaStream_t stream);
+// out = in rounded to the nearest tf32 value, n elements (n % 4 == 0, both 16-byte aligned).
+cp_status launch_tf32_round(const float *in, float *out, int64_t n, cudaStream_t stream);
 cp_status read_tf32_device_status(int *code, bool clear);
 
 // ------------------------------------------------------------ backward

@@ -11,7 +11,8 @@
 // flags (bit set): CP_RING_FUSED_MERGE folds each step's merge into the
 // attention epilogue (the partial is merged straight into the accumulator);
 // CP_RING_TF32 takes fp32 q, k, v and runs the tf32 kernel (attn_tf32.cu),
-// zero copy only (v of every rank is transposed once per call).
+// zero copy only (q and k of every rank are rounded to tf32 and v transposed
+// and rounded, once per call, into the workspace).
 // The inter-GPU exchange of the pages has two stand-ins here:
 //   no CP_RING_PREFETCH  zero copy: the kernel reads the owner's resident block;
 //   CP_RING_PREFETCH     the exchange is emulated: the K/V rotation needed by step
@@ -37,7 +38,7 @@ constexpr size_t kAlign = 256;
 inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-    size_t o_tile = 0, lse_tile = 0, o_acc = 0, kv = 0, vt = 0, plan = 0, total = 0;
+    size_t o_tile = 0, lse_tile = 0, o_acc = 0, kv = 0, vt = 0, qr = 0, kr = 0, plan = 0, total = 0;
     size_t plan_bytes = 0;  // the attention launches' work plan (0: it fits on chip)
     size_t o_tile_bytes = 0, lse_bytes = 0, o_acc_bytes = 0, kv_bytes = 0;  // kv: one K (or V) rotation
 };
@@ -61,6 +62,11 @@ Layout ws_layout(int64_t B, int64_t S, int64_t N, int64_t Nkv, int64_t D, int C,
     off += 4 * round_up(L.kv_bytes);  // 2 buffers x (K, V)
     L.vt = off;
     if (flags & CP_RING_TF32) off += round_up(tf32_vt_bytes(static_cast<int64_t>(C) * B, s, Nkv, D));
+    // tf32: q and k rounded to tf32 for the tensor cores (v is rounded in its transpose)
+    L.qr = off;
+    if (flags & CP_RING_TF32) off += round_up(static_cast<size_t>(C) * B * s * N * D * 4);
+    L.kr = off;
+    if (flags & CP_RING_TF32) off += round_up(static_cast<size_t>(C) * B * s * Nkv * D * 4);
     // one plan buffer, rebuilt by each step's attention launch in stream order
     L.plan_bytes = (flags & CP_RING_TF32) ? tf32_plan_need(C, C, s, s) : attn_plan_need(C, C, s, s);
     L.plan = off;
@@ -242,8 +248,17 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         if (st == CP_OK && cudaEventRecord(res->copy_done[b], res->side) != cudaSuccess) st = CP_ERR_CUDA;
     };
     float *vt = reinterpret_cast<float *>(ws + L.vt);
-    if (tf32) st = launch_tf32_transpose(static_cast<const float *>(v_sh), vt, static_cast<int64_t>(C) * B, s, Nkv, D,
-                                        stream);
+    float *qr = reinterpret_cast<float *>(ws + L.qr), *kr = reinterpret_cast<float *>(ws + L.kr);
+    if (tf32) {
+        st = launch_tf32_round(static_cast<const float *>(q_sh), qr, static_cast<int64_t>(C) * B * s * N * D, stream);
+        if (st == CP_OK)
+            st = launch_tf32_round(static_cast<const float *>(k_sh), kr, static_cast<int64_t>(C) * B * s * Nkv * D,
+                                   stream);
+        if (st == CP_OK)
+            st = launch_tf32_transpose(static_cast<const float *>(v_sh), vt, static_cast<int64_t>(C) * B, s, Nkv, D,
+                                       stream);
+        p.q = qr;
+    }
     if (use_prefetch) {
         if (cudaEventRecord(res->start, stream) != cudaSuccess || cudaStreamWaitEvent(res->side, res->start, 0) !=
                                                                         cudaSuccess)
@@ -255,7 +270,7 @@ cp_status ring_impl(const void *q_sh, const void *k_sh, const void *v_sh, const 
         AttnProblem ps = p;
         ps.kpos_shift = back;
         if (step == 0 || !use_prefetch) {
-            ps.k = k_sh;
+            ps.k = tf32 ? static_cast<const void *>(kr) : k_sh;
             ps.v = v_sh;
             ps.kv_shift = back;
         } else {

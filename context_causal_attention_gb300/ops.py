@@ -164,7 +164,7 @@ def cp_attn_partial_f32(q, k, v, q_pos, k_pos, scale=None, o=None, lse=None, wor
         lse = torch.empty((B, N, Sq), dtype=torch.float32, device=dev)
     L = _lib.lib()
     n = ctypes.c_size_t(0)
-    _lib.check("cp_attn_f32_workspace_size", L.cp_attn_f32_workspace_size(B, Sq, Sk, Nkv, D, ctypes.byref(n)))
+    _lib.check("cp_attn_f32_workspace_size", L.cp_attn_f32_workspace_size(B, Sq, Sk, N, Nkv, D, ctypes.byref(n)))
     if workspace is None:
         workspace = torch.empty(max(256, n.value), dtype=torch.uint8, device=dev)
     st = L.cp_attn_partial_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(q_pos), _ptr(k_pos), B, Sq, Sk, N, Nkv, D, float(scale),

@@ -182,16 +182,19 @@ cp_status cp_attn_partial_ws(const void *q, const void *k, const void *v, const 
 
 /*
  * cp_attn_f32_workspace_size / cp_attn_partial_f32 -- cp_attn_partial for fp32
- * inputs with the tensor cores in tf32 (tcgen05.mma kind::tf32: operands
- * rounded to a 10-bit mantissa, fp32 accumulation; P enters P V as tf32 too).
+ * inputs with the tensor cores in tf32 (tcgen05.mma kind::tf32, fp32
+ * accumulation).  q, k, v and P are rounded to the nearest tf32 value (10-bit
+ * mantissa, ties away from zero) before they enter the tensor cores: q and k
+ * by a pass into the workspace, v in its transpose, P in the softmax.
  * Same arguments, result and conventions as cp_attn_partial except:
  *   q : device fp32 [B][Sq][N][D]; k, v : device fp32 [B][Sk][Nkv][D]
- *   workspace : device, >= cp_attn_f32_workspace_size(B, Sq, Sk, Nkv, D)
- *               bytes, 256-byte aligned (holds v transposed for the K-major
- *               operand and, when ceil(Sk/64) + ceil(Sq/128) > 2048 or
- *               ceil(Sq/128) > 1024, the launch's work plan)
+ *   workspace : device, >= cp_attn_f32_workspace_size(B, Sq, Sk, N, Nkv, D)
+ *               bytes, 256-byte aligned (rounded q and k, v transposed for
+ *               the K-major operand and, when ceil(Sk/64) + ceil(Sq/128) >
+ *               2048 or ceil(Sq/128) > 1024, the launch's work plan)
  */
-cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t Nkv, int64_t D, size_t *bytes);
+cp_status cp_attn_f32_workspace_size(int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv, int64_t D,
+                                     size_t *bytes);
 cp_status cp_attn_partial_f32(const float *q, const float *k, const float *v, const int32_t *q_pos,
                               const int32_t *k_pos, int64_t B, int64_t Sq, int64_t Sk, int64_t N, int64_t Nkv,
                               int64_t D, float scale, float *o, float *lse, void *workspace, size_t ws_bytes,

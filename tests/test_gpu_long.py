@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 ATOL_O = 2e-2
 ATOL_LSE = 1e-3
 RING_VS_MONO = 1e-3
-TF32_ATOL = 1e-2
+TF32_ATOL_O, TF32_ATOL_LSE = 4e-3, 2e-3  # as in the tf32 parity tests
 NTH = O.default_threads()
 MAX_TABLES, MAX_PAIRS = 2048, 1024  # the kernels' on-chip plan capacity
 
@@ -225,7 +225,7 @@ def test_tf32_ring_s256k_sampled_rows(cuda_dev):
     o_sh, lse_sh = F.cp_ring_attention_fwd(qs, ks, vs, pos, tf32=True)
     torch.cuda.synchronize()
     assert torch.isfinite(o_sh).all().item()
-    _check_sampled(_sampled_ref(w, q, k, v, heads=[5], n_random=16), pos, o_sh, lse_sh, TF32_ATOL, TF32_ATOL)
+    _check_sampled(_sampled_ref(w, q, k, v, heads=[5], n_random=16), pos, o_sh, lse_sh, TF32_ATOL_O, TF32_ATOL_LSE)
     assert F.cp_device_status() == 0
 
 

@@ -425,11 +425,14 @@ def test_device_status_clean(cuda_dev):
 # --------------------------------------------------------------------------
 # tf32 input path
 # --------------------------------------------------------------------------
-# Bars: q and k enter the tensor cores truncated to tf32 (10-bit mantissa), v
-# and P rounded to it.  A CPU emulation with all four truncated gives max|do|
-# <= 4e-3 and max|dlse| <= 3.5e-3 against fp64 of the fp32 inputs on S=256-1024
-# causal problems; the bars are 1e-2 for both.
-TF32_ATOL = 1e-2
+# Bars: q, k, v and P enter the tensor cores rounded to the nearest tf32 value
+# (10-bit mantissa).  A CPU emulation of exactly that (q, k, v, P rounded, the
+# integer running max of the first 64-key tile, the fp32 sum of the unrounded
+# P), three seeds on causal S = 256-3072, N(0,1) inputs, gives max|do| <= 1.9e-3
+# and max|dlse| <= 7.9e-4 against fp64 of the fp32 inputs; the bars allow about
+# twice that.
+TF32_ATOL_O = 4e-3
+TF32_ATOL_LSE = 2e-3
 
 TF32_CASES = {
     "tiny_fp32_causal": dict(B=1, Sq=256, Sk=256, N=2, Nkv=2, D=64, qp=lambda: np.arange(256), kp=lambda: np.arange(256)),
@@ -463,7 +466,7 @@ def test_attn_partial_f32_vs_oracle(cuda_dev, name):
                                    torch.as_tensor(qp).to(cuda_dev), torch.as_tensor(kp).to(cuda_dev))
     torch.cuda.synchronize()
     o_ref, l_ref = O.attn_direct(f64(q), f64(k), f64(v), qp, kp, nthreads=NTH)
-    assert_attn_close(o, lse, o_ref, l_ref, atol_o=TF32_ATOL, atol_lse=TF32_ATOL)
+    assert_attn_close(o, lse, o_ref, l_ref, atol_o=TF32_ATOL_O, atol_lse=TF32_ATOL_LSE)
     assert F.cp_device_status() == 0
 
 
@@ -487,8 +490,8 @@ def test_attn_partial_f32_paired_tiles_gqa_ragged(cuda_dev):
     rows = np.unique(np.concatenate([np.arange(0, Sq, 23), np.arange(Sq - 3, Sq), [127, 128, 1407, 1408, 1535, 1536]]))
     o_ref, l_ref = O.attn_rows(f64(q), f64(k), f64(v), qp, kp, rows, nthreads=NTH)
     r_idx = torch.as_tensor(rows, device=cuda_dev)
-    assert np.max(np.abs(f64(o[:, r_idx]) - o_ref)) <= TF32_ATOL
-    assert np.max(np.abs(f64(lse[:, :, r_idx]) - l_ref)) <= TF32_ATOL
+    assert np.max(np.abs(f64(o[:, r_idx]) - o_ref)) <= TF32_ATOL_O
+    assert np.max(np.abs(f64(lse[:, :, r_idx]) - l_ref)) <= TF32_ATOL_LSE
     assert F.cp_device_status() == 0
 
 
@@ -503,7 +506,7 @@ def test_attn_partial_f32_tiny_workload(cuda_dev):
     torch.cuda.synchronize()
     pn = np.arange(w.S, dtype=np.int32)
     o_ref, l_ref = O.attn_direct(*(f64(t) for t in raw), pn, pn)
-    d_o, d_l = assert_attn_close(o, lse, o_ref, l_ref, atol_o=TF32_ATOL, atol_lse=TF32_ATOL)
+    d_o, d_l = assert_attn_close(o, lse, o_ref, l_ref, atol_o=TF32_ATOL_O, atol_lse=TF32_ATOL_LSE)
     print("tiny fp32 via tf32: max|do|=%.3g max|dlse|=%.3g" % (d_o, d_l))
 
 
@@ -522,7 +525,7 @@ def test_ring_tf32_vs_oracle(cuda_dev, wname, layout):
     torch.cuda.synchronize()
     lay_o = O.ZIGZAG if layout == "zigzag" else O.CONTIGUOUS
     o_ref, l_ref = O.ring_fwd(*(O.shard(f64(t), w.C, lay_o) for t in (q, k, v)), pos.cpu().numpy(), nthreads=NTH)
-    assert np.max(np.abs(f64(o_sh) - o_ref)) <= TF32_ATOL
-    assert np.max(np.abs(f64(lse_sh) - l_ref)) <= TF32_ATOL
+    assert np.max(np.abs(f64(o_sh) - o_ref)) <= TF32_ATOL_O
+    assert np.max(np.abs(f64(lse_sh) - l_ref)) <= TF32_ATOL_LSE
     with pytest.raises(F.CpError):
         F.cp_ring_attention_fwd(qs, ks, vs, pos, layout=lay, tf32=True, prefetch=1)
