@@ -20,10 +20,15 @@ namespace {
 
 // One warp merges 32 consecutive query rows i0..i0+31 of one (b, h): the two
 // lse vectors of those rows arrive in one coalesced load each, a ballot keeps
-// the rows whose tile saw anything, and those rows are merged four at a time
-// with all their o loads in flight before any is used.  Lane k computes the
-// merged lse of row i0+k and its two weights; every lane then blends one or
-// more 16-byte pieces of each row's D values.
+// the rows whose tile saw anything, and those rows are merged four per lane
+// group at a time with all their o loads in flight before any is used.  Lane k
+// computes the merged lse of row i0+k and its two weights; every lane then
+// blends one or more 16-byte pieces of each row's D values.  A row of fewer
+// than 32 float4 (D < 128) takes only part of the warp, so the warp is split
+// into 32 / (D/4) lane groups that each take their own rows.
+// kRpp: rows per slot of the warp (1 for D >= 128, 2 for D = 64; 0: 32 / (D/4),
+// computed at run time, for the other widths)
+template <int kRpp>
 __global__ void __launch_bounds__(256, 4) lse_merge_kernel(float *__restrict__ o_acc, float *__restrict__ lse_acc,
                                                         const float *__restrict__ o_t,
                                                         const float *__restrict__ lse_t, long long B,
@@ -60,19 +65,32 @@ __global__ void __launch_bounds__(256, 4) lse_merge_kernel(float *__restrict__ o
         }
         unsigned todo = __ballot_sync(0xffffffffu, lt != -INFINITY);
         const long long row0 = (b * Sq + i0) * N + h;  // o row of i0; row of i0+k is row0 + k*N
+        // rows narrower than a warp (D < 128) share it: rpp rows per slot, lane
+        // group `sub` takes one of them, lane c0 of the group its float4 columns
+        const int rpp = kRpp > 0 ? kRpp : (nvec >= 32 ? 1 : 32 / nvec);
+        const int sub = rpp == 1 ? 0 : lane / nvec;
+        const int c0 = rpp == 1 ? lane : lane - sub * nvec;
         while (todo) {
-            // next (up to) four rows of this block with a non-empty tile
+            // next (up to) 4 * rpp rows of this block with a non-empty tile; slot q
+            // of this lane's group holds row ks[q]
             int ks[4];
             float wsa[4], wst[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                ks[q] = todo ? __ffs(todo) - 1 : -1;
-                todo &= todo - 1;  // no-op once empty
+                int mine = -1;
+#pragma unroll
+                for (int g = 0; g < (kRpp > 0 ? kRpp : 32); ++g) {
+                    if (kRpp == 0 && g >= rpp) break;
+                    const int kk = todo ? __ffs(todo) - 1 : -1;
+                    todo &= todo - 1;  // no-op once empty
+                    if (g == sub) mine = kk;
+                }
+                ks[q] = mine;
                 // weights of that row, from its lane (all lanes take part)
-                wsa[q] = __shfl_sync(0xffffffffu, wa, ks[q] < 0 ? 0 : ks[q]);
-                wst[q] = __shfl_sync(0xffffffffu, wt, ks[q] < 0 ? 0 : ks[q]);
+                wsa[q] = __shfl_sync(0xffffffffu, wa, mine < 0 ? 0 : mine);
+                wst[q] = __shfl_sync(0xffffffffu, wt, mine < 0 ? 0 : mine);
             }
-            for (int c = lane; c < nvec; c += 32) {
+            for (int c = c0; c < nvec; c += 32) {
                 float4 xa[4], xt[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -129,8 +147,18 @@ cp_status launch_merge(float *o_acc, float *lse_acc, const float *o_tile, const 
     const long long cap = static_cast<long long>(sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    lse_merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_acc, lse_acc, o_tile, lse_tile, B, Sq,
-                                                                       static_cast<int>(N), static_cast<int>(D));
+    if (D >= 128)
+        lse_merge_kernel<1><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_acc, lse_acc, o_tile, lse_tile, B,
+                                                                              Sq, static_cast<int>(N),
+                                                                              static_cast<int>(D));
+    else if (D == 64)
+        lse_merge_kernel<2><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_acc, lse_acc, o_tile, lse_tile, B,
+                                                                              Sq, static_cast<int>(N),
+                                                                              static_cast<int>(D));
+    else
+        lse_merge_kernel<0><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_acc, lse_acc, o_tile, lse_tile, B,
+                                                                              Sq, static_cast<int>(N),
+                                                                              static_cast<int>(D));
     return last_launch_status();
 }
 

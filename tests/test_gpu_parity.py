@@ -132,7 +132,10 @@ def test_ulysses_relayout_bit_exact(cuda_dev, C, B, s, N, D, dtype, order):
 # --------------------------------------------------------------------------
 # LSE merge
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("B,Sq,N,D", [(2, 300, 3, 64), (1, 129, 8, 128), (1, 7, 1, 4)])
+# D=64 and D=4: several rows share a warp; D=48: lane groups that do not fill it;
+# D=256: two 16-byte pieces per lane and row
+@pytest.mark.parametrize("B,Sq,N,D", [(2, 300, 3, 64), (1, 129, 8, 128), (1, 7, 1, 4), (3, 77, 2, 48),
+                                      (1, 40, 2, 256)])
 def test_lse_merge_vs_oracle(cuda_dev, B, Sq, N, D):
     o_a, l_a, o_t, l_t = SY.merge_inputs(B, Sq, N, D, seed=3, neg_inf_frac=0.3)
     # some accumulator rows empty too, and one row empty on both sides
