@@ -290,3 +290,59 @@ def test_ring_bwd_s256k_sampled(cuda_dev):
     got_dv = np.stack([f64(dv[inv[j, 0], :, inv[j, 1]][:, heads]) for j in keys], axis=1)
     assert_grad_close("dk keys", got_dk, ref_dk)
     assert_grad_close("dv keys", got_dv, ref_dv)
+
+
+def test_allgather_ulysses_mesh_s256k_vs_ring(cuda_dev):
+    """The other strategies at S=262144, C=8: all-gather (one launch whose C
+    query ranks share one key sequence of 262144 positions: a plan in the
+    workspace), Ulysses (one launch over the whole sequence per head group) and
+    the 2 x 4 mesh, all against the ring's o (every row and head) <= 1e-3."""
+    w = SY.WORKLOADS["s256k"]
+    q, k, v, _ = SY.make_qkv(w)
+    qs, ks, vs = (F.cp_zigzag_shard(t.to(cuda_dev), w.C) for t in (q, k, v))
+    del q, k, v
+    pos = F.cp_zigzag_positions(w.S, w.C, device=cuda_dev)
+    o_ring, l_ring = F.cp_ring_attention_fwd(qs, ks, vs, pos, prefetch=1)
+    o_ag, l_ag = F.cp_allgather_attention_fwd(qs, ks, vs, pos)
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(o_ag - o_ring)).item() <= RING_VS_MONO
+    assert torch.max(torch.abs(l_ag - l_ring)).item() <= RING_VS_MONO
+    del o_ag, l_ag
+    o_ul, _ = F.cp_ulysses_attention_fwd(qs, ks, vs)
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(o_ul - o_ring)).item() <= RING_VS_MONO
+    del o_ul
+    o_me, _ = F.cp_mesh_attention_fwd(qs, ks, vs, pos, 2, 4, prefetch=1)
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(o_me - o_ring)).item() <= RING_VS_MONO
+    assert F.cp_device_status() == 0
+
+
+def test_global_plan_unsorted_positions_vs_oracle(cuda_dev):
+    """A single call past the on-chip plan limit (1100 query and 1100 key tiles)
+    with shuffled key positions and unsorted query positions, so the plan's
+    sorted flags are off and every count is a full scan; GQA 2:1.  Sampled rows
+    against the oracle, including rows that see no key (lse = -inf, o = 0)."""
+    B, Sq, Sk, N, Nkv, D = 1, 1100 * 128, 1100 * 128, 2, 1, 64
+    assert F.cp_attn_workspace_size(B, Sq, Sk, N, Nkv, D) > 0
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(B, Sq, N, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Sk, Nkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Sk, Nkv, D, generator=g).to(torch.bfloat16)
+    rng = np.random.default_rng(22)
+    kp = rng.permutation(Sk).astype(np.int32) + 1000   # positions 1000 .. Sk+999, shuffled
+    qp = rng.integers(0, Sk + 1000, Sq).astype(np.int32)  # some below 1000: they see nothing
+    o, lse = F.cp_attn_partial(q.to(cuda_dev), k.to(cuda_dev), v.to(cuda_dev), torch.as_tensor(qp).to(cuda_dev),
+                               torch.as_tensor(kp).to(cuda_dev))
+    torch.cuda.synchronize()
+    empty = np.flatnonzero(qp < 1000)[:4]
+    rows = np.unique(np.concatenate([rng.integers(0, Sq, 24), empty, [0, Sq - 1]]))
+    o_ref, l_ref = O.attn_rows(f64(q), f64(k), f64(v), qp, kp, rows, nthreads=NTH)
+    r_idx = torch.as_tensor(rows, device=cuda_dev)
+    o_g, l_g = f64(o[:, r_idx]), f64(lse[:, :, r_idx])
+    neg = np.isneginf(l_ref)
+    assert neg.any() and np.array_equal(np.isneginf(l_g), neg)
+    assert np.all(o_g[np.broadcast_to(np.transpose(neg, (0, 2, 1))[..., None], o_g.shape)] == 0)
+    assert np.max(np.abs(o_g - o_ref)) <= ATOL_O
+    assert np.max(np.abs(l_g[~neg] - l_ref[~neg])) <= ATOL_LSE
+    assert F.cp_device_status() == 0
