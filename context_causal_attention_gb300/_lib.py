@@ -87,6 +87,7 @@ def lib():
     L.cp_ring_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, vp, vp,
                                         vp, sz, vp]
     L.cp_selftest_stalled_producer.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_uint64, vp]
+    L.cp_selftest_stalled_kernel.argtypes = [i32, vp, sz, ctypes.c_uint64, vp]
     L.cp_attn_f32_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.POINTER(sz)]
     L.cp_attn_partial_f32.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, sz, vp]
     L.cp_ring_attention_fwd_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, f32, i32, vp, i32, vp,

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libcpattn.so")
 SOURCES = ["attn.cu", "attn_bwd.cu", "attn_tf32.cu", "permute.cu", "merge.cu", "ring.cu", "strategies.cu", "abi.cu",
-           "noalloc.cu", "plan.cu"]
+           "noalloc.cu", "plan.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -138,6 +138,7 @@ struct BwdArgs {
     int pair;         // a super-block holds stationary tiles u and nt-1-u (else u alone)
     FastDiv div_nsp, div_h;  // by super-blocks per rank, heads per item
     PlanPtrs gp;      // the launch's plan in global memory (kernels with kGlobalPlan)
+    const int *hold;  // failure injection (self-test only), else null
 };
 
 // (min, max) of the positions of one 128-row tile (one warp per tile); when
@@ -386,6 +387,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (lane == 0) {
             uint32_t it = 0, t = 0;
             bool ok = true;
+            if (a.hold) ok = hold_wait(a.hold, a.timeout_ns, abort_flag);
             int kv_par = -1;
             uint32_t qd_issued = 0, qd_par = 0;
             int seg = 0;  // segment cursor of decode_super
@@ -755,6 +757,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (lane == 0) {
             uint32_t it = 0, t = 0;
             bool ok = true;
+            if (a.hold) ok = hold_wait(a.hold, a.timeout_ns, abort_flag);
             int qd_par = -1;
             uint32_t kv_issued = 0, kv_par = 0;
             int seg = 0;  // segment cursor of decode_super
@@ -1045,7 +1048,8 @@ BwdArgs make_args(const BwdProblem &p, int nq, int nk, int heads_per_item) {
     a.accumulate = p.accumulate ? 1 : 0;
     a.scale = p.scale;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
-    a.timeout_ns = 2000000000ull;
+    a.timeout_ns = p.timeout_ns ? p.timeout_ns : 2000000000ull;
+    a.hold = p.hold;
     a.div_h = make_fastdiv(static_cast<uint32_t>(heads_per_item));
     return a;
 }

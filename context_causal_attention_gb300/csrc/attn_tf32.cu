@@ -83,6 +83,7 @@ struct TArgs {
     int pair;  // a super-block holds query tiles u and nqt-1-u (else u alone)
     FastDiv div_nsp, div_n;
     PlanPtrs gp;  // the launch's plan in global memory (kernels with kGlobalPlan)
+    const int *hold;  // failure injection (self-test only), else null
 };
 
 // kind::tf32 instruction descriptor: D fp32 (bits 4-5 = 1), A and B tf32
@@ -277,6 +278,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 return true;
             };
             bool ok = true;
+            if (a.hold) ok = hold_wait(a.hold, a.timeout_ns, abort_flag);
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
                 const int idx = item_of_round(rk, n_items);
@@ -644,7 +646,8 @@ cp_status launch_tf32_typed(const AttnProblem &p, const float *vt, int64_t sk_pa
     a.kv_shared = p.kv_shared ? 1 : 0;
     a.kpr = (p.k_pos_stride == 0) ? 1 : p.C;
     a.scale_log2 = static_cast<float>(static_cast<double>(p.scale) * 1.4426950408889634074);
-    a.timeout_ns = 2000000000ull;
+    a.timeout_ns = p.timeout_ns ? p.timeout_ns : 2000000000ull;
+    a.hold = p.hold;
     // query tiles u and nqt-1-u in one work item when that still leaves 8 rounds
     a.pair = pair_units(a.nqt, p.C, p.B * p.N, sm_count()) ? 1 : 0;
     a.div_nsp = make_fastdiv(static_cast<uint32_t>(super_count(a.nqt, a.pair != 0)));
@@ -685,7 +688,7 @@ cp_status validate_attn_tf32(const AttnProblem &p, bool check_plan) {
     if (p.D != 64 && p.D != 128) return CP_ERR_UNSUPPORTED;
     if (p.N % p.Nkv != 0) return CP_ERR_DIVISIBILITY;
     if (!(std::isfinite(p.scale) && p.scale > 0.f)) return CP_ERR_ARGUMENT;
-    if (p.merge_into || p.hold) return CP_ERR_UNSUPPORTED;
+    if (p.merge_into) return CP_ERR_UNSUPPORTED;
     if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.q_pos) || !aligned16(p.k_pos) ||
         !aligned16(p.lse))
         return CP_ERR_ALIGNMENT;

@@ -186,6 +186,10 @@ struct BwdProblem {
     // one after the other); unused otherwise
     void *plan = nullptr;
     size_t plan_bytes = 0;
+    // failure injection (self-test only): both producers first wait for *hold
+    // to become non-zero; every bounded wait uses timeout_ns (0: 2 s)
+    const int *hold = nullptr;
+    unsigned long long timeout_ns = 0;
 };
 // Rows of the per-row statistics (a multiple of 128 >= Sq).
 inline int64_t bwd_sq_pad(int64_t Sq) { return (Sq + 127) / 128 * 128; }

@@ -394,6 +394,20 @@ def cp_selftest_stalled_producer(q, k, v, pos, o, lse, timeout_ns, stream=None):
     _lib.check("cp_selftest_stalled_producer", st)
 
 
+CP_SELFTEST_SCRATCH_BYTES = 512 << 10
+
+
+def cp_selftest_stalled_kernel(kernel, timeout_ns, scratch=None, device="cuda", stream=None):
+    """The same self-test for kernel 0 (bf16 forward), 1 (tf32 forward) or 2
+    (backward: its dK/dV and dQ launches), on a tiny problem laid out in
+    `scratch` (allocated here unless given)."""
+    if scratch is None:
+        scratch = torch.empty(CP_SELFTEST_SCRATCH_BYTES, dtype=torch.uint8, device=device)
+    st = _lib.lib().cp_selftest_stalled_kernel(int(kernel), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                               int(timeout_ns), _stream(stream))
+    _lib.check("cp_selftest_stalled_kernel", st)
+
+
 def cp_device_status(clear=True, stream=None):
     """Synchronise the stream and return the library's device status code."""
     code = ctypes.c_int(0)

@@ -436,6 +436,23 @@ cp_status cp_selftest_stalled_producer(const void *q, const void *k, const void 
                                        float *lse, uint64_t timeout_ns, cudaStream_t stream);
 
 /*
+ * cp_selftest_stalled_kernel -- the failure-detection self-test above for any
+ * of the attention kernels (no counterpart on the pages): kernel 0 = bf16
+ * forward, 1 = tf32 forward, 2 = backward (its dK/dV launch, then its dQ
+ * launch).  The call zeroes `scratch` (device, 256-byte aligned, at least
+ * CP_SELFTEST_SCRATCH_BYTES bytes), lays a tiny problem (one head, 128 rows,
+ * D = 64) and the hold flag out in it, and launches the kernel with its TMA
+ * producer held on the flag, which nothing sets, and every bounded wait limited
+ * to timeout_ns (1 ms .. 2 s, else CP_ERR_ARGUMENT).  Each launch gives up
+ * after timeout_ns and records CP_ERR_DEVICE_TIMEOUT in the device status word
+ * (cp_device_status); the call returns CP_OK when the launches succeeded.  The
+ * context stays usable.
+ */
+#define CP_SELFTEST_SCRATCH_BYTES ((size_t)512 << 10)
+cp_status cp_selftest_stalled_kernel(int kernel, void *scratch, size_t scratch_bytes, uint64_t timeout_ns,
+                                     cudaStream_t stream);
+
+/*
  * cp_ring_attention_fwd_noalloc -- cp_ring_attention_fwd for callers that
  * cannot allocate device memory.  The source pages have no counterpart: this
  * entry point exists for callers that may not call cudaMalloc or cannot hand

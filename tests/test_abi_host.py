@@ -223,6 +223,19 @@ def test_selftest_timeout_range(cplib):
     assert cplib.cp_selftest_stalled_producer(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3_000_000_000, None) == 10
 
 
+def test_selftest_kernel_argument_checks(cplib):
+    # kernel, scratch, bytes, timeout_ns, stream: all refused before any CUDA call
+    big = 512 << 10
+    f = cplib.cp_selftest_stalled_kernel
+    assert f(3, FAKE, big, 10_000_000, None) == 10          # no such kernel
+    assert f(-1, FAKE, big, 10_000_000, None) == 10
+    assert f(1, FAKE, big, 999_999, None) == 10             # timeout below 1 ms
+    assert f(1, FAKE, big, 3_000_000_000, None) == 10       # above 2 s
+    assert f(2, NULL, big, 10_000_000, None) == 1
+    assert f(2, ctypes.c_void_p(4096 + 16), big, 10_000_000, None) == 5
+    assert f(2, FAKE, big - 1, 10_000_000, None) == 6       # scratch smaller than CP_SELFTEST_SCRATCH_BYTES
+
+
 def test_binding_refuses_cpu_tensors_before_any_call():
     """The Python binding raises before reaching the library when a tensor that
     must be on the GPU is a CPU tensor (host memory is accepted only where the

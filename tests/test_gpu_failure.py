@@ -48,3 +48,37 @@ def test_timeout_status_survives_until_read(cuda_dev):
     assert F.cp_device_status(clear=False) == CP_ERR_DEVICE_TIMEOUT
     assert F.cp_device_status() == CP_ERR_DEVICE_TIMEOUT
     assert F.cp_device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2], ids=["bf16_forward", "tf32_forward", "backward"])
+def test_every_kernel_gives_up_a_stalled_wait(cuda_dev, kernel):
+    """Each attention kernel's bounded waits: its producer held on a flag that
+    nothing sets gives up after 10 ms, the status word reads
+    CP_ERR_DEVICE_TIMEOUT (sticky until read), and the next call on the same
+    context computes correctly (the backward's two launches both give up)."""
+    assert F.cp_device_status() == 0
+    F.cp_selftest_stalled_kernel(kernel, 10_000_000)
+    torch.cuda.synchronize()
+    assert F.cp_device_status() == CP_ERR_DEVICE_TIMEOUT
+    assert F.cp_device_status() == 0
+    g = torch.Generator().manual_seed(8)
+    q, k, v, do = (torch.randn(1, 256, 2, 64, generator=g) for _ in range(4))
+    pos = torch.arange(256, dtype=torch.int32, device=cuda_dev)
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    gp = np.arange(256)
+    if kernel == 1:
+        o, l = F.cp_attn_partial_f32(q.to(cuda_dev), k.to(cuda_dev), v.to(cuda_dev), pos, pos)
+        o_ref, l_ref = O.attn_direct(f(q), f(k), f(v), gp, gp)
+        assert np.max(np.abs(f(o) - o_ref)) <= 4e-3 and np.max(np.abs(f(l) - l_ref)) <= 2e-3
+    else:
+        qb, kb, vb, dob = (t.to(torch.bfloat16) for t in (q, k, v, do))
+        o, l = F.cp_attn_partial(qb.to(cuda_dev), kb.to(cuda_dev), vb.to(cuda_dev), pos, pos)
+        o_ref, l_ref = O.attn_direct(f(qb), f(kb), f(vb), gp, gp)
+        assert np.max(np.abs(f(o) - o_ref)) <= 2e-2 and np.max(np.abs(f(l) - l_ref)) <= 1e-3
+        if kernel == 2:
+            dq, dk, dv = F.cp_attn_bwd_partial(qb.to(cuda_dev), kb.to(cuda_dev), vb.to(cuda_dev), o, dob.to(cuda_dev),
+                                               l, pos, pos)
+            ref = O.attn_bwd(f(qb), f(kb), f(vb), o_ref, f(dob), l_ref, gp, gp)
+            for got, r in zip((dq, dk, dv), ref):
+                assert np.max(np.abs(f(got) - r)) <= 1e-2 * np.max(np.abs(r))
+    assert F.cp_device_status() == 0
