@@ -294,7 +294,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, prefetch=None, device_timing=False),
+        "config": line_config(w, 1 if args.prefetch else 0, bool(args.fused_merge)),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "%d random query rows x all %d heads per step of the %s workload (fp64 C "
                                    "oracle, %d threads; the same batch as the cpu_baseline of our arm)"
@@ -329,6 +329,14 @@ def workload_config(w, prefetch, device_timing=True):
     if prefetch is not None:
         cfg["prefetch"] = prefetch
     return cfg
+
+
+def line_config(w, prefetch, fused):
+    """The `config` of the JSON line, the same for both arms (the reference arm
+    times the oracle on this workload; the GPU-side keys describe our arm's run)."""
+    return dict(workload_config(w, prefetch),
+                merge="fused into the attention epilogue (standalone merge kernel timed separately)"
+                if fused else "standalone merge kernel per ring step")
 
 
 def graph_replay_times(args, torch, F, step, inputs, flush_buf, parts):
@@ -778,9 +786,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w, prefetch),
-                       merge="fused into the attention epilogue (standalone merge kernel timed separately)"
-                       if fused else "standalone merge kernel per ring step"),
+        "config": line_config(w, prefetch, fused),
         "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": peak_tc, "unit": "TFLOP/s",
                      "frac": attn_tflops / peak_tc, "traffic": traffic,
                      "kernel": "attn_fwd_kernel<%d>" % D + (" (ring steps >= 1 also merge into the accumulator in "
