@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "cp_internal.h"
+#include "cp_hold.cuh"
 #include "cp_ptx.cuh"
 #include "cp_sched.cuh"
 

@@ -65,21 +65,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
-// Failure injection (self-tests only): wait, bounded by timeout_ns, for *hold
-// to become non-zero.  A flag that nothing sets makes the wait run out; it then
-// raises *abort_flag like any other bounded wait and returns false.
-__device__ __forceinline__ bool hold_wait(const int *hold, uint64_t timeout_ns, volatile int *abort_flag) {
-    const uint64_t t0 = global_timer_ns();
-    while (*reinterpret_cast<const volatile int *>(hold) == 0) {
-        if (global_timer_ns() - t0 > timeout_ns) {
-            *abort_flag = 1;
-            return false;
-        }
-        __nanosleep(1000);
-    }
-    return true;
-}
-
 // mbar_wait by every lane of a warp with one warp-wide answer: a lane that
 // gave up (timeout or abort) makes the whole warp give up, so the warp never
 // splits around the warp-collective tcgen05 instructions that follow.  Lanes
