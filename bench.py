@@ -580,14 +580,17 @@ def time_device_steps(rig, steps, warmup, world=1, clocks=None):
     return max_over_ranks(ms_total, world) / steps, evsets, wall, flush_buf
 
 
-def secondary_step_line(w, dev, steps, warmup, peaks, prefetch, fused):
+def secondary_step_line(w, dev, steps, warmup, peaks, prefetch, fused, graph=False):
     """The device step (same rig, same timing rules) on another workload, for
-    the secondary keys of the default line."""
+    the secondary keys of the default line; with `graph`, also the median of
+    >= 20 CUDA-graph replays of the whole step beside the same step launched
+    eagerly (L2 flushed between runs when the workload needs it)."""
+    import types
     import cp_synth as SY
     q, k, v, _ = SY.make_qkv(w)
     rig = StepRig(w, dev, prefetch, fused, q, k, v)
     del q, k, v
-    ms, evsets, wall, _ = time_device_steps(rig, steps, warmup)
+    ms, evsets, wall, flush_buf = time_device_steps(rig, steps, warmup)
     km = kernel_metrics(rig, evsets, peaks)
     out = {"workload": workload_config(w, prefetch)["workload"], "l2": workload_config(w, prefetch)["l2"],
            "ms_per_step": ms, "value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -600,6 +603,12 @@ def secondary_step_line(w, dev, steps, warmup, peaks, prefetch, fused):
            "shard_gbs": km["shard_gbs"], "unshard_gbs": km["unshard_gbs"], "relayout_gbs": km["relayout_gbs"],
            "relayout_frac_hbm": km["relayout_frac_hbm"], "shard_frac_hbm": km["shard_frac_hbm"],
            "steps": steps, "warmup": warmup, "wall_s_timed": wall}
+    if graph:
+        g = graph_replay_times(types.SimpleNamespace(steps=steps), rig.torch, rig.F, rig.step,
+                               (rig.qd, rig.kd, rig.vd), flush_buf, {})
+        g["step_value_graph_tflops"] = w.flops / (g["step_ms_graph"] * 1e-3) / 1e12
+        g["step_value_eager_tflops"] = w.flops / (g["step_ms_eager"] * 1e-3) / 1e12
+        out["graph"] = g
     del rig
     return out
 
@@ -607,14 +616,16 @@ def secondary_step_line(w, dev, steps, warmup, peaks, prefetch, fused):
 def run_secondary(args, dev, peaks, prefetch, fused):
     """Secondary keys of the default line: the S=4096 and S=131072 workloads'
     device steps (step TFLOP/s, relayout and per-step merge GB/s with their
-    fraction of HBM), and the S=65536 sweep point for C in {2, 4, 8},
+    fraction of HBM; S=4096 also as CUDA-graph replays), and the S=65536 sweep point for C in {2, 4, 8},
     contiguous against zigzag (per-rank issued key tiles and per-rank time,
     max / mean over ranks)."""
     import cp_synth as SY
     torch = __import__("torch")
     out = {}
     for name in ("s4k", "s128k"):
-        out[name] = secondary_step_line(SY.WORKLOADS[name], dev, args.steps, args.warmup, peaks, prefetch, fused)
+        # the small workload also as CUDA-graph replays (its launches are short)
+        out[name] = secondary_step_line(SY.WORKLOADS[name], dev, args.steps, args.warmup, peaks, prefetch, fused,
+                                        graph=(name == "s4k"))
         torch.cuda.empty_cache()
     sw = []
     for w in SY.sweep_workloads():
