@@ -60,6 +60,7 @@
 #include "cp_hold.cuh"
 #include "cp_ptx.cuh"
 #include "cp_sched.cuh"
+#include "cp_rounds.cuh"
 
 namespace cpattn {
 namespace {
@@ -393,10 +394,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
             uint32_t qd_issued = 0, qd_par = 0;
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
-                const int idx = item_of_round(rk, n_items);
-                if (idx < 0) continue;
-                const SuperItem sup = decode_super(idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
-                for (int part = 0; part < 2 && ok; ++part) {
+                const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+                if (rw.idx < 0) continue;
+                const SuperItem sup = decode_super(rw.idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
+                for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                     const int unit = super_part(sup.u, part, a.nk, a.pair != 0);
                     if (unit < 0) continue;
                     int r, kt, b, hk, owner, kvr, pr;
@@ -463,10 +464,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
             bool ok = true;
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
-                const int idx = item_of_round(rk, n_items);
-                if (idx < 0) continue;
-                const SuperItem sup = decode_super(idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
-                for (int part = 0; part < 2 && ok; ++part) {
+                const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+                if (rw.idx < 0) continue;
+                const SuperItem sup = decode_super(rw.idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
+                for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                     const int unit = super_part(sup.u, part, a.nk, a.pair != 0);
                     if (unit < 0) continue;
                     int r, kt, b, hk, owner, kvr, pr;
@@ -520,10 +521,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         bool ok = true;
         int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
-            const int idx = item_of_round(rk, n_items);
-            if (idx < 0) continue;
-            const SuperItem sup = decode_super(idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
-            for (int part = 0; part < 2 && ok; ++part) {
+            const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+            if (rw.idx < 0) continue;
+            const SuperItem sup = decode_super(rw.idx, a.B * a.Nkv, order, seg_first, a.div_nsp, seg);
+            for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                 const int unit = super_part(sup.u, part, a.nk, a.pair != 0);
                 if (unit < 0) continue;
                 int r, kt, b, hk, owner, kvr, pr;
@@ -763,10 +764,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
             uint32_t kv_issued = 0, kv_par = 0;
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
-                const int idx = item_of_round(rk, n_items);
-                if (idx < 0) continue;
-                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
-                for (int part = 0; part < 2 && ok; ++part) {
+                const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+                if (rw.idx < 0) continue;
+                const SuperItem sup = decode_super(rw.idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                     const int unit = super_part(sup.u, part, a.nq, a.pair != 0);
                     if (unit < 0) continue;
                     int r, qt, b, h, owner, kvr, pr;
@@ -827,10 +828,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
             bool ok = true;
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
-                const int idx = item_of_round(rk, n_items);
-                if (idx < 0) continue;
-                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
-                for (int part = 0; part < 2 && ok; ++part) {
+                const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+                if (rw.idx < 0) continue;
+                const SuperItem sup = decode_super(rw.idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                     const int unit = super_part(sup.u, part, a.nq, a.pair != 0);
                     if (unit < 0) continue;
                     int r, qt, b, h, owner, kvr, pr;
@@ -878,10 +879,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         bool ok = true;
         int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
-            const int idx = item_of_round(rk, n_items);
-            if (idx < 0) continue;
-            const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
-            for (int part = 0; part < 2 && ok; ++part) {
+            const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+            if (rw.idx < 0) continue;
+            const SuperItem sup = decode_super(rw.idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+            for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                 const int unit = super_part(sup.u, part, a.nq, a.pair != 0);
                 if (unit < 0) continue;
                 int r, qt, b, h, owner, kvr, pr;

@@ -35,6 +35,7 @@
 #include "cp_hold.cuh"
 #include "cp_ptx.cuh"
 #include "cp_sched.cuh"
+#include "cp_rounds.cuh"
 
 namespace cpattn {
 
@@ -282,10 +283,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             if (a.hold) ok = hold_wait(a.hold, a.timeout_ns, abort_flag);
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
-                const int idx = item_of_round(rk, n_items);
-                if (idx < 0) continue;
-                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
-                for (int part = 0; part < 2 && ok; ++part) {
+                const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+                if (rw.idx < 0) continue;
+                const SuperItem sup = decode_super(rw.idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                     const int unit = super_part(sup.u, part, a.nqt, a.pair != 0);
                     if (unit < 0) continue;
                     int r, qt, b, h, owner, kvr, pr;
@@ -352,10 +353,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             };
             int seg = 0;  // segment cursor of decode_super
             for (int rk = 0; rk < n_rounds && ok; ++rk) {
-                const int idx = item_of_round(rk, n_items);
-                if (idx < 0) continue;
-                const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
-                for (int part = 0; part < 2 && ok; ++part) {
+                const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+                if (rw.idx < 0) continue;
+                const SuperItem sup = decode_super(rw.idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+                for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                     const int unit = super_part(sup.u, part, a.nqt, a.pair != 0);
                     if (unit < 0) continue;
                     int r, qt, b, h, owner, kvr, pr;
@@ -416,10 +417,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
         bool ok = true;
         int seg = 0;  // segment cursor of decode_super
         for (int rk = 0; rk < n_rounds && ok; ++rk) {
-            const int idx = item_of_round(rk, n_items);
-            if (idx < 0) continue;
-            const SuperItem sup = decode_super(idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
-            for (int part = 0; part < 2 && ok; ++part) {
+            const RoundWork rw = work_of_round(rk, n_items, a.pair != 0);
+            if (rw.idx < 0) continue;
+            const SuperItem sup = decode_super(rw.idx, a.B * a.N, order, seg_first, a.div_nsp, seg);
+            for (int part = rw.p0; part < rw.p1 && ok; ++part) {
                 const int unit = super_part(sup.u, part, a.nqt, a.pair != 0);
                 if (unit < 0) continue;
                 int r, qt, b, h, owner, kvr, pr;
