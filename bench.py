@@ -1136,8 +1136,9 @@ def run_tf32(args):
     dev = torch.device("cuda", 0)
     peaks = load_peaks()
     ratio = 1.1 / 2.25
+    sweep = {x.name: x for x in SY.sweep_workloads()}
     for wname in args.tf32.split(","):
-        w = SY.WORKLOADS[wname]
+        w = SY.WORKLOADS.get(wname) or sweep[wname]
         g = torch.Generator("cpu").manual_seed(0)
         qs, ks, vs = (F.cp_zigzag_shard(torch.randn(w.B, w.S, n, w.D, generator=g).to(dev), w.C)
                       for n in (w.N, w.Nkv, w.Nkv))
