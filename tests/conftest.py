@@ -28,3 +28,17 @@ def cuda_dev(cplib):
     if not torch.cuda.is_available():
         pytest.fail("a GPU test was selected but no CUDA device is visible")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _no_kernel_gave_up(request):
+    """After every test that used the GPU, no kernel may have given up a bounded
+    wait: such a kernel leaves its outputs unwritten, which a value check would
+    report only as a mismatch.  The failure self-tests read (and so clear) the
+    status word themselves."""
+    yield
+    if "cuda_dev" not in request.fixturenames:
+        return
+    from context_causal_attention_gb300 import ops as F
+    code = F.cp_device_status()
+    assert code == 0, "a kernel gave up a bounded wait during this test (device status %d)" % code
