@@ -131,6 +131,8 @@ RING = {
     "c1": (SY.Workload("rb_c1", B=1, S=640, N=2, Nkv=2, D=64, C=1), "zigzag"),
     "c64_max": (SY.Workload("rb_c64", B=1, S=8192, N=2, Nkv=1, D=64, C=64), "zigzag"),
     "ragged_gqa_c4": (SY.Workload("rb_rg", B=1, S=1800, N=4, Nkv=2, D=128, C=4), "zigzag"),
+    # eight query heads per K/V head: dK, dV of a K/V head sum over all eight
+    "gqa8_c2": (SY.Workload("rb_g8", B=1, S=1024, N=16, Nkv=2, D=128, C=2), "zigzag"),
 }
 
 

@@ -254,7 +254,8 @@ def ring_inputs(w, cuda_dev, layout):
 
 @pytest.mark.parametrize("wname,layout", [("tiny", "zigzag"), ("s4k", "zigzag"), ("s4k_contig", "contiguous"),
                                           ("c8", "zigzag"), ("c1", "zigzag"), ("c64_max", "zigzag"),
-                                          ("c64_max_contig", "contiguous"), ("ragged_gqa", "zigzag")])
+                                          ("c64_max_contig", "contiguous"), ("ragged_gqa", "zigzag"),
+                                          ("gqa8", "zigzag"), ("gqa8_contig", "contiguous")])
 def test_ring_vs_oracle(cuda_dev, wname, layout):
     """Every ring mode (zero copy / prefetched K/V rotation x separate / fused
     merge) against the fp64 oracle ring."""
@@ -267,6 +268,9 @@ def test_ring_vs_oracle(cuda_dev, wname, layout):
         "c64_max_contig": SY.Workload("c64c", B=1, S=8192, N=2, Nkv=2, D=128, C=64, layout="contiguous"),
         # 450 rows per rank (a ragged last tile in every shard), two query heads per K/V head
         "ragged_gqa": SY.Workload("rg", B=2, S=1800, N=4, Nkv=2, D=128, C=4),
+        # eight query heads per K/V head (query head h reads K/V head h // 8)
+        "gqa8": SY.Workload("g8", B=1, S=1024, N=16, Nkv=2, D=128, C=2),
+        "gqa8_contig": SY.Workload("g8c", B=2, S=768, N=8, Nkv=1, D=64, C=3, layout="contiguous"),
     }
     w = extra.get(wname) or SY.WORKLOADS[wname]
     (q, k, v), (qs, ks, vs), pos, lay = ring_inputs(w, cuda_dev, layout)
