@@ -579,10 +579,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 2; ++i) {
                             if (j > 0) {
                                 const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
-                                if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                                if (j == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                                // both tiles read the same V stage: tile 1 needs no second wait
+                                // the waits that do not depend on the softmax come first, so
+                                // P V follows this tile's P as closely as possible; both tiles
+                                // read the same V stage, so tile 1 needs no second wait
                                 if (i == 0 && !mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                                if (j == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                                if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                                 tc_fence_after();
                                 issue_pv(i, prev_st, j > 1);
                                 if (i == 1) umma_commit(bars.v_empty + prev_st);
@@ -600,9 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // tail: P V of the last key tile, then hand O to the epilogue
                     for (int i = 0; i < 2; ++i) {
                         const uint32_t pst = (kv_it - 1) % K::kStages, pph = ((kv_it - 1) / K::kStages) & 1u;
-                        if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
-                        if (n == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                         if (i == 0 && !mbar_wait(bars.v_full + pst, pph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (n == 1 && !mbar_wait(bars.o_empty + i, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (!mbar_wait(bars.p_full + i, (kv_it - 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                         tc_fence_after();
                         issue_pv(i, prev_st, n > 1);
                         if (i == 1) umma_commit(bars.v_empty + prev_st);
