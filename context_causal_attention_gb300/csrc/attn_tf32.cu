@@ -377,9 +377,13 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     if (n <= 2) umma_commit(q_empty);
                     for (int j = 0; j < n; ++j, ++t) {
                         const uint32_t bb = t & 1u, st = t % kTStages, ph = (t / kTStages) & 1u;
-                        if (!mbar_wait(p_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        const uint32_t st2 = (t + 2) % kTStages, ph2 = ((t + 2) / kTStages) & 1u;
+                        // the waits that do not depend on the softmax come first, so P V
+                        // and the next scores follow this tile's P directly
                         if (j == 0 && !mbar_wait(o_empty, (it & 1u) ^ 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                         if (!mbar_wait(v_full + st, ph, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (j + 2 < n && !mbar_wait(k_full + st2, ph2, abort_flag, a.timeout_ns)) { ok = false; break; }
+                        if (!mbar_wait(p_full + bb, (t >> 1) & 1u, abort_flag, a.timeout_ns)) { ok = false; break; }
                         tc_fence_after();
                         // O (+)= P V: 64 keys in 8 k-steps of 8 (P columns +8; V^T k-step kk
                         // at (kk / 4) atoms + (kk % 4) * 32 bytes)
@@ -390,9 +394,6 @@ __global__ void __launch_bounds__(kTThreads, 1)
                         umma_commit(pv_done);
                         umma_commit(v_empty + st);
                         if (j + 2 < n) {
-                            const uint32_t st2 = (t + 2) % kTStages, ph2 = ((t + 2) / kTStages) & 1u;
-                            if (!mbar_wait(k_full + st2, ph2, abort_flag, a.timeout_ns)) { ok = false; break; }
-                            tc_fence_after();
                             issue_s(bb, st2);
                             if (j + 3 == n) umma_commit(q_empty);
                         }
