@@ -674,8 +674,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pa[32], pb[32];
                     float t_sum;
                     bool stored = false;
-                    // TMEM loads/stores are warp-collective: the path must be warp-uniform
-                    if (__all_sync(0xffffffffu, m_run != -INFINITY)) {
+                    if constexpr (D == 64) {
+                        // TMEM loads/stores are warp-collective: every branch around them is
+                        // warp-uniform.  A row's first visible tile takes the steady code too, after the
+                        // tile max of both halves has set its running max: with items of a
+                        // few key tiles the per-item code is a large share, and a separate
+                        // first-tile copy of the exp code ran cold in the instruction cache
+                        // once per item.  (At D = 128 the shared form cost the steady loop
+                        // more registers than it saved.)
+                        tmem_ld64_nowait(tS, sa);
+                        tmem_wait_ld(sa);
+                        tmem_ld64_nowait(tS + 64, sb);
+                        if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 0, sa);
+                        const bool first = !__all_sync(0xffffffffu, m_run != -INFINITY);
+                        if (first) {
+                            tmem_wait_ld(sb);
+                            if (need_mask) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 64, sb);
+                            if (m_run == -INFINITY) {
+                                const float m_tile = row_max128(sa, sb) * sl2;
+                                if (m_tile > -INFINITY) m_run = ceilf(m_tile);
+                            }
+                        }
+                        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                        const float s0 = exp_pack64(sa, sl2, neg_m, pa);
+                        tmem_wait_ld(sb);  // columns 64..127 read: P may overwrite them
+                        tmem_st32_nowait(tS + 64, pa);
+                        if (need_mask && !first) mask_half(arith, qpos, kmm.x, nvalid, kpos_o + kbase, 64, sb);
+                        const float s1 = exp_pack64(sb, sl2, neg_m, pb);
+                        tmem_st32_nowait(tS + 96, pb);
+                        t_sum = s0 + s1;
+                        stored = true;
+                    } else if (__all_sync(0xffffffffu, m_run != -INFINITY)) {
+                        // (TMEM loads/stores are warp-collective: the path must be warp-uniform)
                         // Steady state (max already set): pipeline the tile in two halves --
                         // the second half's TMEM load and the first half's P store overlap
                         // exp work.
