@@ -463,8 +463,9 @@ cp_status cp_selftest_stalled_kernel(int kernel, void *scratch, size_t scratch_b
  *   (zero-copy owner rotation) and no workspace argument; the caller still
  *   passes all inputs and outputs.
  *   Scratch: the call uses one file-scope device array of
- *   CP_NOALLOC_SCRATCH_BYTES bytes inside the library (every GPU on which the
- *   library is loaded keeps it until the process exits).  The ring's own
+ *   CP_NOALLOC_SCRATCH_BYTES bytes inside the library (every CUDA context
+ *   that loads the library's module holds one copy, until that context is
+ *   destroyed: at process exit, or at cudaDeviceReset).  The ring's own
  *   argument checks (pointers, enums, shapes, divisibility, alignment) run
  *   first; then sizes whose cp_ring_workspace_size(..., prefetch = 0,
  *   o_dtype, ...) exceeds CP_NOALLOC_SCRATCH_BYTES are rejected with
