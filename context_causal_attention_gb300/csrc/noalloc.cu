@@ -1,10 +1,17 @@
 // noalloc.cu -- ring attention forward that allocates nothing.
 //
-// Some callers cannot call cudaMalloc: code that runs where the device
-// allocator is off limits (inside a custom allocator's own callbacks, in a
-// runtime that forbids allocation after start-up, or in a process whose
-// memory pool is owned by another framework), or that cannot hand this library
-// a workspace.  For them cp_ring_attention_fwd_noalloc runs the same ring as
+// Some callers cannot call cudaMalloc, or cannot hand this library a
+// workspace:
+//   * code inside a custom device allocator's own callbacks: a cudaMalloc there
+//     re-enters the allocator it is serving (or waits on its lock);
+//   * runtimes that reserve all device memory at start-up and forbid allocation
+//     afterwards, so that memory use and latency stay fixed;
+//   * processes whose device memory pool belongs to another framework: memory
+//     taken outside that pool escapes its accounting and can push it out of
+//     memory;
+//   * code recorded under stream capture in the global mode, where cudaMalloc
+//     is refused.
+// For them cp_ring_attention_fwd_noalloc runs the same ring as
 // cp_ring_attention_fwd (zero-copy owner rotation, no prefetch) with its
 // scratch -- the per-step partial output and lse, and the fp32 accumulator for
 // a bf16 output -- taken from one file-scope device array of fixed size.

@@ -457,8 +457,11 @@ cp_status cp_selftest_stalled_kernel(int kernel, void *scratch, size_t scratch_b
  * cannot allocate device memory.  The source pages have no counterpart: this
  * entry point exists for callers that may not call cudaMalloc or cannot hand
  * the library a workspace -- code running inside a custom allocator's
- * callbacks, runtimes that forbid allocation after start-up, or processes
- * whose device memory pool belongs to another framework.
+ * callbacks (a cudaMalloc there re-enters the allocator), runtimes that
+ * reserve all device memory at start-up and forbid allocation afterwards,
+ * processes whose device memory pool belongs to another framework (memory
+ * taken outside it escapes its accounting), and code under stream capture in
+ * the global mode, where cudaMalloc is refused.
  *   Same arguments and result as cp_ring_attention_fwd with prefetch = 0
  *   (zero-copy owner rotation) and no workspace argument; the caller still
  *   passes all inputs and outputs.
